@@ -1,0 +1,176 @@
+"""CPU oracle of the row-wise softmax cross-entropy path (f64, plain C).
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package. The CUDA library
+never does, and this package imports nothing from it.
+
+What each function computes follows the API reference page "gizml:netops"
+(gizstack.com/docs/reference/gizml/netops.md), section Functions:
+``crossEntropyRows`` (per-row loss), ``crossEntropyLoss`` (mean in f64 in row
+order), ``crossEntropyGrad`` ((softmax - onehot) * scale) and ``argmaxInto``;
+section Methods: ``Tensor.argmax`` (first of equals, NaN never wins). The C
+source ``ce_oracle.c`` states each definition beside its code.
+
+Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
+closed forms, brute force, library routines and invariants; no function is
+parity-unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "ce_oracle.c")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(BUILD_DIR, "libceoracle.so")
+
+# Plain gcc; no fast-math, no FMA contraction, so each f64 operation rounds
+# once as written in the source.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+_default = None
+
+
+def build(source: str = SOURCE, out: str = LIB_PATH, force: bool = False) -> str:
+    """Compile the oracle's C source into a shared library (gcc)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(source)):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, source, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+
+
+class Oracle:
+    """ctypes view of one compiled copy of the oracle.
+
+    Logits are a 2-D float32 array ``[rows, stride]`` (C order); only the
+    first ``vocab`` columns of each row are read. Labels are int64 ``[rows]``.
+    ``threads`` splits rows across host threads (rows are independent; each
+    row is still computed exactly as the C source says).
+    """
+
+    def __init__(self, lib_path: str):
+        self.path = lib_path
+        lib = ctypes.CDLL(lib_path)
+        lib.oracle_version.restype = ctypes.c_int
+        lib.oracle_ce_rows.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
+        lib.oracle_ce_rows.restype = ctypes.c_int
+        lib.oracle_ce_grad.argtypes = [_vp, _i64, _i64, _i64, _vp, ctypes.c_double, _vp, _vp]
+        lib.oracle_ce_grad.restype = ctypes.c_int
+        lib.oracle_ce_mean.argtypes = [_vp, _i64]
+        lib.oracle_ce_mean.restype = ctypes.c_double
+        lib.oracle_argmax.argtypes = [_vp, _i64, _i64, _i64, _vp]
+        lib.oracle_argmax.restype = ctypes.c_int
+        self.lib = lib
+
+    # -- helpers ---------------------------------------------------------
+    @staticmethod
+    def _check(logits: np.ndarray, vocab: int):
+        if logits.dtype != np.float32 or logits.ndim != 2:
+            raise TypeError("logits must be a 2-D float32 array [rows, stride]")
+        if not logits.flags["C_CONTIGUOUS"]:
+            raise ValueError("logits must be C-contiguous")
+        rows, stride = logits.shape
+        if vocab < 1 or vocab > stride:
+            raise ValueError(f"need 1 <= vocab <= stride (vocab={vocab}, stride={stride})")
+        return rows, stride
+
+    @staticmethod
+    def _chunks(rows: int, threads: int):
+        threads = max(1, min(threads, rows))
+        step = -(-rows // threads) if rows else 0
+        return [(a, min(rows, a + step)) for a in range(0, rows, step)] if rows else []
+
+    def _run(self, fn, rows: int, threads: int):
+        parts = self._chunks(rows, threads)
+        if len(parts) <= 1:
+            for a, b in parts:
+                fn(a, b)
+            return
+        with ThreadPoolExecutor(len(parts)) as ex:
+            for f in [ex.submit(fn, a, b) for a, b in parts]:
+                f.result()
+
+    # -- the four operations --------------------------------------------
+    def ce_rows(self, logits: np.ndarray, vocab: int, labels: np.ndarray, threads: int = 1):
+        """Per-row loss (crossEntropyRows), f64 [rows]."""
+        rows, stride = self._check(logits, vocab)
+        labels = np.ascontiguousarray(labels, dtype=np.int64)
+        out = np.empty(rows, dtype=np.float64)
+
+        def fn(a, b):
+            rc = self.lib.oracle_ce_rows(logits[a:b].ctypes.data, b - a, vocab, stride,
+                                         labels[a:b].ctypes.data, out[a:b].ctypes.data)
+            if rc:
+                raise ValueError("oracle_ce_rows rejected its arguments")
+
+        self._run(fn, rows, threads)
+        return out
+
+    def ce_grad(self, logits: np.ndarray, vocab: int, labels: np.ndarray, scale: float,
+                threads: int = 1):
+        """Gradient (crossEntropyGrad) f64 [rows, vocab] and the row losses f64 [rows]."""
+        rows, stride = self._check(logits, vocab)
+        labels = np.ascontiguousarray(labels, dtype=np.int64)
+        grad = np.empty((rows, vocab), dtype=np.float64)
+        loss = np.empty(rows, dtype=np.float64)
+
+        def fn(a, b):
+            rc = self.lib.oracle_ce_grad(logits[a:b].ctypes.data, b - a, vocab, stride,
+                                         labels[a:b].ctypes.data, float(scale),
+                                         grad[a:b].ctypes.data, loss[a:b].ctypes.data)
+            if rc:
+                raise ValueError("oracle_ce_grad rejected its arguments")
+
+        self._run(fn, rows, threads)
+        return grad, loss
+
+    def ce_mean(self, loss_rows: np.ndarray) -> float:
+        """Mean of the row losses in f64 in row order (crossEntropyLoss)."""
+        loss_rows = np.ascontiguousarray(loss_rows, dtype=np.float64)
+        return float(self.lib.oracle_ce_mean(loss_rows.ctypes.data, loss_rows.shape[0]))
+
+    def ce_loss(self, logits: np.ndarray, vocab: int, labels: np.ndarray, threads: int = 1):
+        """crossEntropyLoss: the row losses' mean (f64) and the row losses."""
+        rows = self.ce_rows(logits, vocab, labels, threads)
+        return self.ce_mean(rows), rows
+
+    def argmax(self, logits: np.ndarray, vocab: int, threads: int = 1):
+        """Row argmax (argmaxInto / Tensor.argmax), int64 [rows]."""
+        rows, stride = self._check(logits, vocab)
+        out = np.empty(rows, dtype=np.int64)
+
+        def fn(a, b):
+            rc = self.lib.oracle_argmax(logits[a:b].ctypes.data, b - a, vocab, stride,
+                                        out[a:b].ctypes.data)
+            if rc:
+                raise ValueError("oracle_argmax rejected its arguments")
+
+        self._run(fn, rows, threads)
+        return out
+
+
+def load(lib_path: str | None = None) -> Oracle:
+    """The oracle built from ``ce_oracle.c`` (compiled on first use), or the
+    library at ``lib_path``."""
+    global _default
+    if lib_path is not None:
+        return Oracle(lib_path)
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+        return _default

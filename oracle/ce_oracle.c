@@ -1,0 +1,195 @@
+/*
+ * ce_oracle.c -- the plain, slow CPU oracle of the row-wise softmax
+ * cross-entropy path: per-row loss, mean loss, gradient and row argmax.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the bench's CPU
+ * baseline call this file. The CUDA library shares no code, header, table
+ * or constant with it, and neither includes nor links the other.
+ *
+ * Everything is computed in f64 from the f32 inputs (each input is widened
+ * once), one row at a time, one column at a time, in column order, with no
+ * blocking, vectorisation or fast-math. Build with plain gcc, e.g.
+ *     gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared ce_oracle.c -lm
+ *
+ * Source of every definition: the API reference page "gizml:netops"
+ * (gizstack.com/docs/reference/gizml/netops.md), section Functions:
+ * crossEntropyLoss, crossEntropyRows, crossEntropyGrad, argmaxInto; and
+ * section Methods: Tensor.argmax.
+ *
+ * Layout: row i of the logits starts at logits + i * stride; only its first
+ * `vocab` columns are read. Labels are int64, one per row. The gradient is
+ * written dense, [rows, vocab].
+ */
+#include <math.h>
+#include <stdint.h>
+
+#define ORACLE_VERSION 1
+
+int oracle_version(void) { return ORACLE_VERSION; }
+
+/*
+ * Statistics of one row, as the crossEntropyLoss entry defines them:
+ *   m  = max_j x_j                    (the row max)
+ *   s  = sum_j exp(x_j - m)           (the row's exp-sum)
+ *   loss = m + log(s) - x[label].
+ * s is split as s = 1 + t: the 1 is the term of the first column j* that
+ * holds m (exp(0) = 1) and t sums the other columns. Then
+ *   loss = (m - x[label]) + log1p(t),
+ * which is the entry's expression rearranged; it is exact in real arithmetic
+ * and keeps the value of a loss far below 1e-16 (a label at the row max with
+ * every other logit far below), where m + log(s) - x[label] cancels in any
+ * floating point format.
+ *
+ * The IEEE evaluation of the entry's expression is NaN for a row that holds a
+ * NaN, that holds +inf (x_j* - m = inf - inf), or whose entries are all -inf
+ * (every x_j - m = -inf - (-inf)). The rearranged form never forms those
+ * differences, so it flags the three cases explicitly (`degenerate`).
+ */
+typedef struct {
+    double m;     /* row max */
+    int64_t jmax; /* first column holding m */
+    double t;     /* sum of exp(x_j - m) over j != jmax */
+    int degenerate;
+} row_stats;
+
+static row_stats stats_of_row(const float *x, int64_t vocab)
+{
+    row_stats r;
+    r.m = -INFINITY;
+    r.jmax = 0;
+    r.t = 0.0;
+    r.degenerate = 0;
+
+    int any_nan = 0;
+    int seen = 0;
+    for (int64_t j = 0; j < vocab; ++j) {
+        double v = (double)x[j];
+        if (isnan(v)) {
+            any_nan = 1;
+            continue;
+        }
+        if (!seen || v > r.m) {
+            r.m = v;
+            r.jmax = j;
+            seen = 1;
+        }
+    }
+    if (any_nan || !seen || isinf(r.m)) {
+        /* NaN present, all NaN, +inf max, or every entry -inf */
+        r.degenerate = 1;
+        r.t = NAN;
+        return r;
+    }
+    double t = 0.0;
+    for (int64_t j = 0; j < vocab; ++j) {
+        if (j == r.jmax)
+            continue;
+        t += exp((double)x[j] - r.m);
+    }
+    r.t = t;
+    return r;
+}
+
+/*
+ * crossEntropyRows: each row's loss m + log(sum exp(x - m)) - x[label].
+ * A label outside [0, vocab) gives a NaN loss for its row.
+ * loss_out: rows doubles. Returns 0, or -1 on a bad argument.
+ */
+int oracle_ce_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+                   const int64_t *labels, double *loss_out)
+{
+    if (rows < 0 || vocab < 1 || stride < vocab)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *x = logits + i * stride;
+        int64_t label = labels[i];
+        row_stats st = stats_of_row(x, vocab);
+        if (st.degenerate || label < 0 || label >= vocab) {
+            loss_out[i] = NAN;
+            continue;
+        }
+        loss_out[i] = (st.m - (double)x[label]) + log1p(st.t);
+    }
+    return 0;
+}
+
+/*
+ * crossEntropyGrad: (softmax - onehot) * scale, softmax_j = exp(x_j - m) / s.
+ * The entry's "f32 of 1/sum" is a statement about the f32 arithmetic of a
+ * device; here 1/s is taken in f64 (the mathematical softmax).
+ * A degenerate row (NaN, +inf, or all -inf) gives a NaN gradient row.
+ * A label outside [0, vocab) gets no one-hot term (and a NaN loss).
+ * grad_out: rows * vocab doubles, dense. loss_out (nullable): rows doubles.
+ */
+int oracle_ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+                   const int64_t *labels, double scale, double *grad_out, double *loss_out)
+{
+    if (rows < 0 || vocab < 1 || stride < vocab)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *x = logits + i * stride;
+        double *g = grad_out + i * vocab;
+        int64_t label = labels[i];
+        int label_ok = (label >= 0 && label < vocab);
+        row_stats st = stats_of_row(x, vocab);
+        if (st.degenerate) {
+            for (int64_t j = 0; j < vocab; ++j)
+                g[j] = NAN;
+            if (loss_out)
+                loss_out[i] = NAN;
+            continue;
+        }
+        double s = 1.0 + st.t;
+        for (int64_t j = 0; j < vocab; ++j) {
+            double p = exp((double)x[j] - st.m) / s;
+            double onehot = (label_ok && j == label) ? 1.0 : 0.0;
+            g[j] = (p - onehot) * scale;
+        }
+        if (loss_out)
+            loss_out[i] = label_ok ? (st.m - (double)x[label]) + log1p(st.t) : NAN;
+    }
+    return 0;
+}
+
+/*
+ * crossEntropyLoss: the mean of the row losses, summed in f64 in row order.
+ * The mean of no rows is NaN (0/0).
+ */
+double oracle_ce_mean(const double *loss_rows, int64_t rows)
+{
+    double sum = 0.0;
+    for (int64_t i = 0; i < rows; ++i)
+        sum += loss_rows[i];
+    return sum / (double)rows;
+}
+
+/*
+ * argmaxInto / Tensor.argmax: the index of each row's largest element among
+ * its first `vocab` columns; the first of equals wins and NaN never wins. A
+ * row with no non-NaN entry gives 0. -0 and +0 are equal (the first wins).
+ * idx_out: rows int64.
+ */
+int oracle_argmax(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+                  int64_t *idx_out)
+{
+    if (rows < 0 || vocab < 1 || stride < vocab)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *x = logits + i * stride;
+        int64_t best = 0;
+        double best_v = 0.0;
+        int seen = 0;
+        for (int64_t j = 0; j < vocab; ++j) {
+            double v = (double)x[j];
+            if (isnan(v))
+                continue;
+            if (!seen || v > best_v) {
+                best = j;
+                best_v = v;
+                seen = 1;
+            }
+        }
+        idx_out[i] = best;
+    }
+    return 0;
+}
