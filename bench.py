@@ -1,0 +1,405 @@
+"""Benchmark of the row-wise softmax cross-entropy path on GB300.
+
+One step is one pass of the whole path over one batch of the training
+workload ce_8192x128256 (8192 rows x 128256 vocab, f32 logits N(0, 3^2),
+4.2 GB): ce_grad writes the gradient, each row's loss and each row's argmax
+token from one read of the logits, then ce_mean writes the f64 mean loss.
+
+Printed (one JSON line, rank 0):
+  value       fused loss + grad GB/s of the step: algorithmic bytes
+              (8 * rows * vocab + 16 * rows + 8) / device time per step
+  roofline    the dominant kernel (the fused one) against measured HBM bandwidth
+  argmax      rows/s of argmax_rows on the decode workload (256 x 151936,
+              row stride 152064), L2 flushed before every timed launch
+  e2e         the same metric with the inputs copied from pinned host memory
+              and the mean loss and tokens copied back inside the timed region
+  cpu_baseline the CPU oracle (f64) timed on the host cores on a row sample
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own batch
+on its own GPU (rows are independent: weak scaling, no collective on the
+data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "fused CE loss+grad GB/s (% of HBM peak); argmax rows/s at 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE = os.path.join(ROOT, "profiles", "k_grad_staged__ce_8192x128256.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "row_wise_softmax_ce_gb300", "csrc", f)
+                  for f in ("ce_kernels.cu", "ce_device.cuh", "ce_internal.h", "ce_api.cu")]
+
+
+def step_bytes(rows: int, vocab: int) -> int:
+    """Algorithmic bytes of one step: logits read + gradient written (4 B each
+    per element), labels read (8 B/row), loss rows and tokens written (4 B/row
+    each), mean written (8 B)."""
+    return 8 * rows * vocab + 16 * rows + 8
+
+
+def argmax_bytes(rows: int, vocab: int) -> int:
+    """Algorithmic bytes of argmax_rows: the first vocab columns read, one token written."""
+    return 4 * rows * vocab + 4 * rows
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary, or None if absent or taken on different kernel sources."""
+    if not os.path.exists(PROFILE):
+        return None
+    vals = {}
+    with open(PROFILE) as f:
+        for line in f:
+            if ":" in line and not line.startswith(("#", " ")):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_full_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[3:7]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+
+
+def time_oracle(batch, sample_rows: int, threads: int):
+    """Oracle loss rows + gradient + argmax + mean over the first sample_rows rows."""
+    import oracle
+    orc = oracle.load()
+    w = batch.workload
+    xs = batch.logits[:sample_rows].cpu().numpy()
+    ys = batch.labels[:sample_rows].cpu().numpy()
+    t0 = time.perf_counter()
+    g, l = orc.ce_grad(xs, w.vocab, ys, batch.scale, threads=threads)
+    orc.argmax(xs, w.vocab, threads=threads)
+    orc.ce_mean(l)
+    dt = time.perf_counter() - t0
+    del g
+    return dt
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    w = W.WORKLOADS[W.HEADLINE]
+    sample = args.ref_rows
+    cores = cpu_cores()
+    b = W.generate(w.with_rows(sample), device="cpu")
+    for _ in range(args.warmup):
+        time_oracle(b, sample, cores)
+    times = [time_oracle(b, sample, cores) for _ in range(args.steps)]
+    total = sum(times)
+    value = step_bytes(sample, w.vocab) * len(times) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "rows_per_step": sample, "vocab": w.vocab,
+                   "step": "oracle ce_grad + argmax + mean over the first rows of the workload"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} of {w.rows} rows per step"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import row_wise_softmax_ce_gb300 as ce
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- the training step on the headline workload
+    w = W.WORKLOADS[W.HEADLINE]
+    if ws > 1:
+        import dataclasses
+        w = dataclasses.replace(w, seed=w.seed + 1000 * rank)
+    b = W.generate(w, device=dev)
+    x, y, scale = b.logits, b.labels, b.scale
+    R, V = w.rows, w.vocab
+    grad = torch.empty((R, V), dtype=torch.float32, device=dev)
+    loss_rows = torch.empty(R, dtype=torch.float32, device=dev)
+    top = torch.empty(R, dtype=torch.float32, device=dev)
+    mean = torch.empty((), dtype=torch.float64, device=dev)
+
+    def step():
+        ce.ce_grad(x, y, scale, grad=grad, loss_rows=loss_rows, top=top)
+        ce.ce_mean(loss_rows, out=mean)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            ce.ce_grad(x, y, scale, grad=grad, loss_rows=loss_rows, top=top)
+            ev[i][1].record(stream)
+            ce.ce_mean(loss_rows, out=mean)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    step_ms_local = t_start.elapsed_time(t_end) / K
+    step_ms = max_over_ranks(step_ms_local, ws)
+    fused_ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
+    bytes_step = step_bytes(R, V)
+    value = ws * bytes_step / (step_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    fused_bytes = 8 * R * V + 16 * R   # what one ce_grad launch moves
+    achieved = fused_bytes / (fused_ms * 1e-3) / 1e9
+    traffic = profiled_traffic()
+    clk = clocks.summary()
+
+    # ---- decode argmax (rows/s), L2 flushed before every timed launch
+    wd = W.WORKLOADS[W.DECODE]
+    bd = W.generate(wd, device=dev)
+    topd = torch.empty(wd.rows, dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    for _ in range(5):
+        ce.argmax_rows(bd.logits, vocab=wd.vocab, out=topd)
+    n_arg = max(20, min(200, K))
+    times = []
+    for _ in range(n_arg):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ce.argmax_rows(bd.logits, vocab=wd.vocab, out=topd)
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    arg_ms = statistics.median(a.elapsed_time(c) for a, c in times)
+    del flush, bd
+
+    # ---- end to end: inputs from pinned host memory, results back to the host
+    xh = torch.empty((R, V), dtype=torch.float32, pin_memory=True)
+    xh.copy_(x)
+    yh = y.cpu().pin_memory()
+    mean_h = torch.empty((), dtype=torch.float64, pin_memory=True)
+    top_h = torch.empty(R, dtype=torch.float32, pin_memory=True)
+    xd = torch.empty_like(x)
+    yd = torch.empty_like(y)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        yd.copy_(yh, non_blocking=True)
+        ce.ce_grad(xd, yd, scale, grad=grad, loss_rows=loss_rows, top=top)
+        ce.ce_mean(loss_rows, out=mean)
+        mean_h.copy_(mean, non_blocking=True)
+        top_h.copy_(top, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    K2 = max(3, min(K, 20))
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K2, ws)
+    e2e_value = ws * bytes_step / (e2e_ms * 1e-3) / 1e9
+    h2d = xh.numel() * 4 + yh.numel() * 8
+    d2h = 8 + top_h.numel() * 4
+    del xh, xd
+
+    # ---- the CPU oracle on a row sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cores = cpu_cores()
+        sample = args.cpu_rows
+        dt = time_oracle(b, sample, cores)
+        cpu = {"value": round(step_bytes(sample, V) / dt / 1e9, 3), "unit": "GB/s", "cores": cores,
+               "kind": "oracle", "sample": f"first {sample} of {R} rows of {w.name} "
+                                           f"(loss rows + gradient + argmax + mean, f64), {dt:.2f} s"}
+
+    plan = ce.plan(ce.OP_GRAD, R, V)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "rows": R, "vocab": V, "stride": V, "logits": "N(0, 3^2) f32",
+                       "scale": scale, "step": "ce_grad (gradient + loss rows + argmax) then ce_mean",
+                       "l2": "no flush: inputs (4.2 GB) larger than L2", "parallelism": f"replicas x{ws}",
+                       "plan": plan},
+            "percent_of_hbm_peak": round(100 * value / ws / peak, 2),
+            "roofline": {"bound": "hbm", "kernel": "k_grad_staged", "achieved": round(achieved, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes": fused_bytes, "ms_per_launch": round(fused_ms, 4)},
+            "argmax": {"workload": wd.name, "rows_per_s": round(wd.rows / (arg_ms * 1e-3), 1),
+                       "ms": round(arg_ms, 5),
+                       "GB/s": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9, 1),
+                       "frac": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9 / peak, 4),
+                       "l2": "flushed before each launch"},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+            "gpu_launches": 2 * K,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=1024, help="rows of the CPU-oracle sample")
+    ap.add_argument("--ref-rows", type=int, default=256, help="rows per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

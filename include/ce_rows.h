@@ -1,0 +1,172 @@
+/*
+ * ce_rows.h -- C ABI of the row-wise softmax cross-entropy library for
+ * NVIDIA GB300 (sm_103a): per-row loss, mean loss, fused loss + gradient,
+ * and the row argmax that closes a decode step.
+ *
+ * Definitions follow the API reference page "gizml:netops"
+ * (gizstack.com/docs/reference/gizml/netops.md), section Functions:
+ * crossEntropyRows, crossEntropyLoss, crossEntropyGrad, argmaxInto; and
+ * section Methods: Tensor.argmax.
+ *
+ * Common conventions of every entry point:
+ *  - Logits are f32, row-major: row i starts at logits + i * stride
+ *    (elements); only its first `vocab` columns are read, the padding
+ *    columns vocab..stride-1 never are.
+ *  - Labels are int64, one per row. Outputs are written per row; the
+ *    gradient is written dense, [rows, vocab] (row i at grad + i * vocab).
+ *  - All pointers are DEVICE pointers on the current CUDA device, owned by
+ *    the caller; the library keeps none of them after the call returns and
+ *    allocates no memory per call.
+ *  - Every call only enqueues work on `stream` (NULL: the legacy default
+ *    stream) and returns; nothing waits for the GPU. A result is ready once
+ *    the stream has reached it.
+ *  - Arguments are checked on the host before anything is launched; a
+ *    rejected call returns a negative status and launches nothing:
+ *      CE_EINVAL: a required pointer is NULL (while rows > 0), rows < 0,
+ *                 vocab < 1, stride < vocab, vocab > 2^24 (the token
+ *                 written as f32 must be exact), or a non-finite scale;
+ *      CE_EALIGN: a pointer is not aligned to its element size;
+ *      CE_ECUDA:  the CUDA runtime reported an error at launch
+ *                 (ce_last_cuda_error() gives its code).
+ *  - rows == 0 is valid and launches nothing, except that ce_loss and
+ *    ce_mean still write their mean (NaN: the mean of no rows).
+ *  - A label outside [0, vocab) is found on the device: that row's loss
+ *    is NaN, its gradient row gets no one-hot term, and a device counter
+ *    (ce_device_error_count) is incremented. Nothing traps.
+ *  - A row holding a NaN or +inf, or whose entries are all -inf, has a NaN
+ *    loss and a NaN gradient row (the IEEE value of the definition). Its
+ *    argmax still follows Tensor.argmax: NaN never wins, first of equals.
+ */
+#ifndef CE_ROWS_H
+#define CE_ROWS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Symbols of this ABI are the library's only exported ones. */
+#if defined(__GNUC__)
+#define CE_API __attribute__((visibility("default")))
+#else
+#define CE_API
+#endif
+
+/* The CUDA runtime's cudaStream_t, without requiring CUDA headers. */
+typedef struct CUstream_st *ce_stream_t;
+
+enum ce_status {
+    CE_OK = 0,
+    CE_EINVAL = -1,
+    CE_EALIGN = -2,
+    CE_ECUDA = -3,
+    CE_EDEVICE = -4, /* no CUDA device, or not an sm_103 device */
+};
+
+/*
+ * crossEntropyRows (gizml:netops, Functions): each row's loss
+ *     m + log(sum_j exp(x_j - m)) - x[label],   m = max_j x_j,
+ * as f32 into loss_rows[rows], computed on the device without a host wait.
+ * The kernel evaluates the equal form (m - x[label]) + log1p(t), where t
+ * sums exp(x_j - m) over all columns but one holding m, so a loss far below
+ * the f32 resolution of m keeps its relative accuracy.
+ *   logits:    [rows, stride] f32, read only.
+ *   labels:    [rows] int64, read only.
+ *   loss_rows: [rows] f32, written; must not overlap the inputs.
+ */
+CE_API int ce_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+            const int64_t *labels, float *loss_rows, ce_stream_t stream);
+
+/*
+ * The mean step of crossEntropyLoss (gizml:netops, Functions): the mean of
+ * `rows` f32 row losses, accumulated in f64, written as one double to
+ * *loss_mean (a device pointer; the value stays on the device, so a
+ * recorded step never waits for it). The sum is a fixed-shape tree: the
+ * same inputs give the same bits on every run.
+ *   loss_rows: [rows] f32, read only.   loss_mean: 1 double, written.
+ */
+CE_API int ce_mean(const float *loss_rows, int64_t rows, double *loss_mean, ce_stream_t stream);
+
+/*
+ * crossEntropyLoss (gizml:netops, Functions): ce_rows followed by ce_mean,
+ * both enqueued on `stream`. loss_rows ([rows] f32) is required: it holds
+ * the row losses (an output) that the mean reads.
+ */
+CE_API int ce_loss(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+            const int64_t *labels, float *loss_rows, double *loss_mean, ce_stream_t stream);
+
+/*
+ * crossEntropyGrad (gizml:netops, Functions): the gradient
+ *     grad[i, j] = (softmax_ij - [j == label_i]) * scale,
+ *     softmax_ij = exp(x_ij - m_i) * f32(1 / sum_i),
+ * with `scale` (e.g. 1/rows, the gradient of the mean over rows) rounded to
+ * f32. One kernel reads each logit once from HBM and writes each gradient
+ * once; it can also write, from the same read, each row's loss (as ce_rows)
+ * and each row's argmax token as f32 (as argmax_rows).
+ *   logits:    [rows, stride] f32, read only, unless grad == logits.
+ *   labels:    [rows] int64, read only.
+ *   grad:      [rows, vocab] f32 dense, written. grad == logits (in place)
+ *              is allowed when stride == vocab; any other overlap is not.
+ *   loss_rows: [rows] f32 or NULL.   top: [rows] f32 or NULL.
+ */
+CE_API int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+            const int64_t *labels, double scale, float *grad, float *loss_rows, float *top,
+            ce_stream_t stream);
+
+/*
+ * argmaxInto (gizml:netops, Functions) with Tensor.argmax's rule (Methods):
+ * over `rows` rows of `stride` elements, the index of the largest of the
+ * first `vocab` entries -- the first of equals; NaN never wins; a row with
+ * no non-NaN entry gives 0 -- written as f32 (exact, since vocab <= 2^24)
+ * into top[rows]. Only the direct form (rows at logits + i * stride); the
+ * page's indirect form over head blocks is not provided.
+ *   logits: [rows, stride] f32, read only.   top: [rows] f32, written.
+ */
+CE_API int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top,
+                ce_stream_t stream);
+
+/* Human-readable text of a status code (a static string). */
+CE_API const char *ce_status_string(int status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+CE_API int ce_version(void);
+
+/* The cudaError_t code behind the calling thread's last CE_ECUDA. */
+CE_API int ce_last_cuda_error(void);
+
+/*
+ * Device-side error counters of the current device, for tests and
+ * diagnostics: counts[0] = rows seen with a label outside [0, vocab);
+ * counts[1] = waits on an asynchronous copy that gave up after their time
+ * limit (the output of that call is then undefined). This call WAITS for
+ * `stream` to finish. ce_device_error_reset zeroes both counters (enqueued
+ * on `stream`).
+ */
+CE_API int ce_device_error_count(ce_stream_t stream, uint64_t counts[2]);
+CE_API int ce_device_error_reset(ce_stream_t stream);
+
+/*
+ * Launch-plan override, for tests and tuning: forces the kernel family
+ * (path: 0 automatic, 1 shared-memory-staged, 2 streaming from global), the
+ * CTAs that share one row (cluster: 0 automatic, else 1..16) and the
+ * threads of a CTA (threads: 0 automatic, else 128, 256 or 512; the
+ * streaming kernels take at most 256, the staged one at most 512).
+ * Applies to every later call in the process. A forced plan that cannot
+ * launch on this device makes the calls return CE_EINVAL.
+ */
+CE_API int ce_debug_force(int path, int cluster, int threads);
+
+/*
+ * The plan the library would pick (host only, launches nothing) for
+ * op (0 ce_rows, 1 ce_grad, 2 argmax_rows) on the current device:
+ * out[0] path, out[1] cluster, out[2] threads, out[3] dynamic shared bytes
+ * per CTA, out[4] columns per CTA, out[5] CTAs in the grid.
+ */
+CE_API int ce_plan(int op, int64_t rows, int64_t vocab, int64_t stride, int64_t out[6]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CE_ROWS_H */

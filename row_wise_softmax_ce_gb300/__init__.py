@@ -1,0 +1,260 @@
+"""Row-wise softmax cross-entropy, its gradient, and the row argmax on NVIDIA
+GB300 (sm_103a).
+
+A thin binding over the C ABI of ``libcerows.so`` (declared in
+``include/ce_rows.h``): each function checks the tensors it is given,
+passes their device pointers and the current CUDA stream to the entry point
+of the same name, and returns. Every step of the computation runs in the
+library's CUDA kernels; there is no other implementation to fall back to, so
+a missing library is an error.
+
+What the operations compute (API reference page "gizml:netops", section
+Functions, and section Methods for the argmax rule):
+
+- ``ce_rows``      crossEntropyRows: each row's loss m + log(sum exp(x - m)) - x[label]
+- ``ce_mean``      the f64 mean of row losses (the last step of crossEntropyLoss)
+- ``ce_loss``      crossEntropyLoss: ``ce_rows`` then ``ce_mean``
+- ``ce_grad``      crossEntropyGrad: (softmax - onehot) * scale, optionally with
+                   the row losses and argmax tokens from the same read
+- ``argmax_rows``  argmaxInto: each row's token (first of equals, NaN never wins) as f32
+
+Logits are a CUDA float32 tensor ``[rows, cols]`` whose rows are contiguous
+(``stride(1) == 1``); its row stride ``stride(0)`` may exceed ``vocab``
+(padded rows), and ``vocab`` defaults to ``cols``. Labels are int64 ``[rows]``.
+Calls are asynchronous on ``torch.cuda.current_stream()``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcerows.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "ce_rows.h")
+
+CE_OK, CE_EINVAL, CE_EALIGN, CE_ECUDA, CE_EDEVICE = 0, -1, -2, -3, -4
+PATH_AUTO, PATH_STAGED, PATH_STREAM = 0, 1, 2
+OP_ROWS, OP_GRAD, OP_ARGMAX = 0, 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class CeError(RuntimeError):
+    """A call of the C ABI returned a non-zero status."""
+
+    def __init__(self, fn: str, status: int, text: str, cuda_error: int = 0):
+        msg = f"{fn}: {text} (status {status})"
+        if status == CE_ECUDA:
+            msg += f", cudaError {cuda_error}"
+        super().__init__(msg)
+        self.status = status
+
+
+def _bind(lib):
+    i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    sig = {
+        "ce_rows": [vp, i64, i64, i64, vp, vp, vp],
+        "ce_mean": [vp, i64, vp, vp],
+        "ce_loss": [vp, i64, i64, i64, vp, vp, vp, vp],
+        "ce_grad": [vp, i64, i64, i64, vp, ctypes.c_double, vp, vp, vp, vp],
+        "argmax_rows": [vp, i64, i64, i64, vp, vp],
+        "ce_version": [],
+        "ce_last_cuda_error": [],
+        "ce_device_error_count": [vp, ctypes.POINTER(ctypes.c_uint64)],
+        "ce_device_error_reset": [vp],
+        "ce_debug_force": [i32, i32, i32],
+        "ce_plan": [i32, i64, i64, i64, ctypes.POINTER(ctypes.c_int64)],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = i32
+    lib.ce_status_string.argtypes = [i32]
+    lib.ce_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"CUDA library {LIB_PATH} is missing: build it with "
+                    "`python -m row_wise_softmax_ce_gb300.build` (or __graft_entry__.build())")
+            _lib = _bind(ctypes.CDLL(LIB_PATH))
+        return _lib
+
+
+def declared_functions(header: str = HEADER) -> list[str]:
+    """Names of the functions that include/ce_rows.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*CE_API\s+(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def _check(fn: str, status: int):
+    if status != CE_OK:
+        L = lib()
+        raise CeError(fn, status, L.ce_status_string(status).decode(), L.ce_last_cuda_error())
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _logits_view(logits: torch.Tensor, vocab: int | None):
+    if not isinstance(logits, torch.Tensor) or logits.dtype != torch.float32:
+        raise TypeError("logits must be a float32 torch.Tensor")
+    if not logits.is_cuda:
+        raise ValueError("logits must be on a CUDA device")
+    if logits.dim() != 2:
+        raise ValueError("logits must be 2-D [rows, cols]")
+    rows, cols = logits.shape
+    if rows > 0 and cols > 1 and logits.stride(1) != 1:
+        raise ValueError("each row of logits must be contiguous (stride(1) == 1)")
+    stride = logits.stride(0) if rows > 1 else max(cols, 1)
+    vocab = cols if vocab is None else int(vocab)
+    if not 1 <= vocab <= cols:
+        raise ValueError(f"need 1 <= vocab <= logits.shape[1] (vocab={vocab}, cols={cols})")
+    if rows > 1 and stride < vocab:
+        raise ValueError("rows of logits overlap (stride(0) < vocab)")
+    return rows, vocab, max(stride, vocab)
+
+
+def _labels(labels: torch.Tensor, rows: int, device):
+    if labels.dtype != torch.int64 or labels.dim() != 1 or labels.shape[0] != rows:
+        raise ValueError(f"labels must be int64 [rows={rows}]")
+    if labels.device != device or not labels.is_contiguous():
+        raise ValueError("labels must be contiguous and on the logits' device")
+    return labels
+
+
+def _out(t, shape, dtype, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+    return t
+
+
+def ce_rows(logits: torch.Tensor, labels: torch.Tensor, vocab: int | None = None,
+            out: torch.Tensor | None = None) -> torch.Tensor:
+    """crossEntropyRows: each row's loss, f32 ``[rows]``."""
+    rows, vocab, stride = _logits_view(logits, vocab)
+    dev = logits.device
+    labels = _labels(labels, rows, dev)
+    out = _out(out, (rows,), torch.float32, dev, "out")
+    with torch.cuda.device(dev):
+        _check("ce_rows", lib().ce_rows(logits.data_ptr(), rows, vocab, stride, labels.data_ptr(),
+                                         out.data_ptr(), _stream(dev)))
+    return out
+
+
+def ce_mean(loss_rows: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Mean of f32 row losses in f64, as a 0-d float64 tensor on the device."""
+    if loss_rows.dtype != torch.float32 or loss_rows.dim() != 1 or not loss_rows.is_contiguous():
+        raise ValueError("loss_rows must be a contiguous float32 [rows] tensor")
+    dev = loss_rows.device
+    out = _out(out, (), torch.float64, dev, "out")
+    with torch.cuda.device(dev):
+        _check("ce_mean", lib().ce_mean(loss_rows.data_ptr(), loss_rows.shape[0], out.data_ptr(),
+                                         _stream(dev)))
+    return out
+
+
+def ce_loss(logits: torch.Tensor, labels: torch.Tensor, vocab: int | None = None,
+            loss_rows: torch.Tensor | None = None, out: torch.Tensor | None = None):
+    """crossEntropyLoss: the mean loss (0-d float64 on the device) and the row losses."""
+    rows, vocab, stride = _logits_view(logits, vocab)
+    dev = logits.device
+    labels = _labels(labels, rows, dev)
+    loss_rows = _out(loss_rows, (rows,), torch.float32, dev, "loss_rows")
+    out = _out(out, (), torch.float64, dev, "out")
+    with torch.cuda.device(dev):
+        _check("ce_loss", lib().ce_loss(logits.data_ptr(), rows, vocab, stride, labels.data_ptr(),
+                                         loss_rows.data_ptr(), out.data_ptr(), _stream(dev)))
+    return out, loss_rows
+
+
+def ce_grad(logits: torch.Tensor, labels: torch.Tensor, scale: float, vocab: int | None = None,
+            grad: torch.Tensor | None = None, loss_rows: bool | torch.Tensor = False,
+            top: bool | torch.Tensor = False):
+    """crossEntropyGrad: ``(softmax - onehot) * scale``, dense f32 ``[rows, vocab]``.
+
+    ``grad`` may be ``logits`` itself (in place) when the logits are dense.
+    With ``loss_rows`` / ``top`` (True or a tensor) the same kernel also
+    writes each row's loss and argmax token; the result is then a tuple
+    ``(grad, loss_rows, top)`` with None for what was not asked.
+    """
+    rows, vocab, stride = _logits_view(logits, vocab)
+    dev = logits.device
+    labels = _labels(labels, rows, dev)
+    grad = _out(grad, (rows, vocab), torch.float32, dev, "grad")
+    lr = None if loss_rows is False else _out(None if loss_rows is True else loss_rows,
+                                              (rows,), torch.float32, dev, "loss_rows")
+    tp = None if top is False else _out(None if top is True else top, (rows,), torch.float32, dev, "top")
+    with torch.cuda.device(dev):
+        _check("ce_grad", lib().ce_grad(
+            logits.data_ptr(), rows, vocab, stride, labels.data_ptr(), float(scale), grad.data_ptr(),
+            lr.data_ptr() if lr is not None else None, tp.data_ptr() if tp is not None else None,
+            _stream(dev)))
+    if loss_rows is False and top is False:
+        return grad
+    return grad, lr, tp
+
+
+def argmax_rows(logits: torch.Tensor, vocab: int | None = None,
+                out: torch.Tensor | None = None) -> torch.Tensor:
+    """argmaxInto: each row's token as f32 ``[rows]`` (first of equals; NaN never wins)."""
+    rows, vocab, stride = _logits_view(logits, vocab)
+    dev = logits.device
+    out = _out(out, (rows,), torch.float32, dev, "out")
+    with torch.cuda.device(dev):
+        _check("argmax_rows", lib().argmax_rows(logits.data_ptr(), rows, vocab, stride, out.data_ptr(),
+                                                 _stream(dev)))
+    return out
+
+
+# -- diagnostics and tuning ---------------------------------------------------
+
+def version() -> int:
+    return lib().ce_version()
+
+
+def status_string(status: int) -> str:
+    return lib().ce_status_string(status).decode()
+
+
+def device_error_count(device=None) -> tuple[int, int]:
+    """(rows seen with a bad label, waits that gave up) on the device; waits for its stream."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    counts = (ctypes.c_uint64 * 2)()
+    with torch.cuda.device(dev):
+        _check("ce_device_error_count", lib().ce_device_error_count(_stream(dev), counts))
+    return int(counts[0]), int(counts[1])
+
+
+def device_error_reset(device=None) -> None:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check("ce_device_error_reset", lib().ce_device_error_reset(_stream(dev)))
+
+
+def debug_force(path: int = 0, cluster: int = 0, threads: int = 0) -> None:
+    """Force the launch plan of later calls (0 = automatic); see ce_debug_force."""
+    _check("ce_debug_force", lib().ce_debug_force(path, cluster, threads))
+
+
+def plan(op: int, rows: int, vocab: int, stride: int | None = None) -> dict:
+    """The launch plan the library would pick for op (OP_ROWS, OP_GRAD, OP_ARGMAX)."""
+    out = (ctypes.c_int64 * 6)()
+    _check("ce_plan", lib().ce_plan(op, rows, vocab, vocab if stride is None else stride, out))
+    keys = ("path", "cluster", "threads", "smem", "cols", "ctas")
+    return dict(zip(keys, (int(v) for v in out)))

@@ -1,0 +1,314 @@
+// ce_api.cu -- the C ABI declared in include/ce_rows.h: host-side argument
+// checks, the choice of kernel and launch shape, and status codes.
+//
+// Conventions follow the pages this library implements: the operations of
+// "gizml:netops" (crossEntropyRows, crossEntropyLoss, crossEntropyGrad,
+// argmaxInto) run where the data is and do not wait for the GPU; and, as the
+// "gpukit" API page's device-op wrappers do, every entry point checks its
+// buffers and sizes first and fails closed -- a wrong size never reaches
+// the device.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "ce_internal.h"
+#include "ce_rows.h"
+
+using namespace cerows;
+
+namespace {
+
+constexpr int kVersion = 10000;            // 1.0.0
+constexpr int64_t kMaxVocab = 1ll << 24;   // tokens are written exactly as f32
+constexpr int kMaxDevices = 64;
+constexpr int kStagedTargetCols = 16384;   // 64 KB of f32 per CTA: 3 CTAs per SM
+constexpr int kStreamMinCols = 2048;       // columns per CTA, at least, when a row is split
+constexpr int64_t kMaxClusters = 1ll << 20;
+
+thread_local int t_last_cuda_error = 0;
+
+struct Force {
+    int path = 0, cluster = 0, threads = 0;
+};
+Force g_force;
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_ready[kMaxDevices] = {};
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return CE_OK;
+    t_last_cuda_error = static_cast<int>(e);
+    return CE_ECUDA;
+}
+
+bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int round_up4(int64_t v) { return static_cast<int>((v + 3) & ~int64_t(3)); }
+
+// The current device, its properties, and the kernels' attributes (set once).
+int current_device(DeviceInfo *out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        t_last_cuda_error = static_cast<int>(e);
+        return CE_EDEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return CE_EDEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_ready[dev]) {
+        DeviceInfo d;
+        d.device = dev;
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) {
+            t_last_cuda_error = static_cast<int>(e);
+            return CE_EDEVICE;
+        }
+        if (d.cc_major != 10 || d.cc_minor != 3) return CE_EDEVICE;  // built for sm_103a only
+        if ((e = set_kernel_attributes(d)) != cudaSuccess) return cuda_status(e);
+        g_dev[dev] = d;
+        g_ready[dev] = true;
+    }
+    *out = g_dev[dev];
+    return CE_OK;
+}
+
+// Launch shape of a streaming kernel (ce_rows, argmax_rows, and the fused
+// path for rows too long to stage): split a row over C CTAs when there are
+// too few rows to give every SM several CTAs.
+void plan_stream(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster) {
+    p.path = kPathStream;
+    p.threads = threads ? threads : kStreamMaxThreads;
+    if (cluster) {
+        p.cluster = cluster;
+    } else {
+        const int64_t ctas_per_sm = 2048 / p.threads;
+        const int64_t target = 4 * ctas_per_sm * dev.sms;  // about four waves
+        int64_t c = ceil_div(target, rows);
+        c = std::min<int64_t>(c, std::min<int64_t>(kMaxCluster, ceil_div(vocab, kStreamMinCols)));
+        p.cluster = static_cast<int>(std::max<int64_t>(1, c));
+    }
+    p.cols = round_up4(ceil_div(vocab, p.cluster));
+    p.smem = 0;
+    p.clusters = std::min<int64_t>(rows, kMaxClusters);
+}
+
+// Launch shape of the staged fused kernel: the fewest CTAs per row whose
+// slices are at most kStagedTargetCols columns (at most 16 CTAs).
+bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster) {
+    p.path = kPathStaged;
+    p.threads = threads ? threads : kStagedMaxThreads;
+    if (p.threads > kStagedMaxThreads) return false;
+    int64_t c = cluster ? cluster : std::max<int64_t>(1, ceil_div(vocab, kStagedTargetCols));
+    if (c > kMaxCluster) c = kMaxCluster;
+    p.cluster = static_cast<int>(c);
+    p.cols = round_up4(ceil_div(vocab, c));
+    p.smem = kStagedHeaderBytes + 4 * (p.cols + 4);
+    p.clusters = std::min<int64_t>(rows, kMaxClusters);
+    if (p.smem > dev.max_smem_optin) return false;
+    int active = 0;
+    if (max_active_clusters(p, kOpGrad, &active) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return active >= 1;
+}
+
+int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *out) {
+    Force f;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        f = g_force;
+    }
+    Plan p;
+    if (op == kOpGrad) {
+        if (f.path == kPathStaged) {
+            if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster)) return CE_EINVAL;
+        } else if (f.path == kPathStream) {
+            plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
+        } else if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster)) {
+            plan_stream(p, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
+        }
+    } else {
+        plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
+    }
+    if (p.cluster < 1 || p.cluster > kMaxCluster) return CE_EINVAL;
+    if (p.path == kPathStream && p.threads > kStreamMaxThreads) return CE_EINVAL;
+    *out = p;
+    return CE_OK;
+}
+
+int check_logits(const float *logits, int64_t rows, int64_t vocab, int64_t stride) {
+    if (rows < 0 || vocab < 1 || vocab > kMaxVocab || stride < vocab) return CE_EINVAL;
+    if (rows > 0 && logits == nullptr) return CE_EINVAL;
+    if (rows > 0 && stride > (INT64_MAX / 4) / rows) return CE_EINVAL;  // byte offsets fit int64
+    if (misaligned(logits, 4)) return CE_EALIGN;
+    return CE_OK;
+}
+
+bool ranges_overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+Args make_args(const float *logits, int64_t rows, int64_t vocab, int64_t stride, const int64_t *labels) {
+    Args a = {};
+    a.logits = logits;
+    a.rows = rows;
+    a.vocab = static_cast<int>(vocab);
+    a.stride = stride;
+    a.labels = labels;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ce_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, const int64_t *labels,
+            float *loss_rows, ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (rows > 0 && (labels == nullptr || loss_rows == nullptr)) return CE_EINVAL;
+    if (misaligned(labels, 8) || misaligned(loss_rows, 4)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(kOpRows, rows, vocab, dev, &p))) return st;
+    Args a = make_args(logits, rows, vocab, stride, labels);
+    a.loss = loss_rows;
+    return cuda_status(launch_rows_stream(p, a, true, stream));
+}
+
+int ce_mean(const float *loss_rows, int64_t rows, double *loss_mean, ce_stream_t stream) {
+    if (rows < 0 || loss_mean == nullptr || (rows > 0 && loss_rows == nullptr)) return CE_EINVAL;
+    if (misaligned(loss_rows, 4) || misaligned(loss_mean, 8)) return CE_EALIGN;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    return cuda_status(launch_mean(loss_rows, rows, loss_mean, stream));
+}
+
+int ce_loss(const float *logits, int64_t rows, int64_t vocab, int64_t stride, const int64_t *labels,
+            float *loss_rows, double *loss_mean, ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (loss_mean == nullptr || (rows > 0 && (labels == nullptr || loss_rows == nullptr))) return CE_EINVAL;
+    if (misaligned(labels, 8) || misaligned(loss_rows, 4) || misaligned(loss_mean, 8)) return CE_EALIGN;
+    if ((st = ce_rows(logits, rows, vocab, stride, labels, loss_rows, stream))) return st;
+    return ce_mean(loss_rows, rows, loss_mean, stream);
+}
+
+int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t stride, const int64_t *labels,
+            double scale, float *grad, float *loss_rows, float *top, ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (!std::isfinite(scale)) return CE_EINVAL;
+    if (rows > 0 && (labels == nullptr || grad == nullptr)) return CE_EINVAL;
+    if (misaligned(labels, 8) || misaligned(grad, 4) || misaligned(loss_rows, 4) || misaligned(top, 4))
+        return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    const int64_t in_bytes = ((rows - 1) * stride + vocab) * 4;
+    const int64_t out_bytes = rows * vocab * 4;
+    if (grad == logits) {
+        if (stride != vocab) return CE_EINVAL;  // in place needs the same layout
+    } else if (ranges_overlap(grad, out_bytes, logits, in_bytes)) {
+        return CE_EINVAL;
+    }
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(kOpGrad, rows, vocab, dev, &p))) return st;
+    Args a = make_args(logits, rows, vocab, stride, labels);
+    a.scale = static_cast<float>(scale);
+    a.grad = grad;
+    a.loss = loss_rows;
+    a.top = top;
+    if (p.path == kPathStaged) return cuda_status(launch_grad_staged(p, a, stream));
+    return cuda_status(launch_grad_stream(p, a, stream));
+}
+
+int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top,
+                ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (rows > 0 && top == nullptr) return CE_EINVAL;
+    if (misaligned(top, 4)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(kOpArgmax, rows, vocab, dev, &p))) return st;
+    Args a = make_args(logits, rows, vocab, stride, nullptr);
+    a.top = top;
+    return cuda_status(launch_rows_stream(p, a, false, stream));
+}
+
+const char *ce_status_string(int status) {
+    switch (status) {
+    case CE_OK: return "ok";
+    case CE_EINVAL: return "invalid argument (null pointer, size, stride, vocab > 2^24, scale or forced plan)";
+    case CE_EALIGN: return "pointer not aligned to its element size";
+    case CE_ECUDA: return "CUDA runtime error at launch (see ce_last_cuda_error)";
+    case CE_EDEVICE: return "no usable sm_103 CUDA device";
+    default: return "unknown status";
+    }
+}
+
+int ce_version(void) { return kVersion; }
+
+int ce_last_cuda_error(void) { return t_last_cuda_error; }
+
+int ce_device_error_count(ce_stream_t stream, uint64_t counts[2]) {
+    if (counts == nullptr) return CE_EINVAL;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    unsigned long long v[2] = {0ull, 0ull};
+    if ((st = cuda_status(read_status(v, stream)))) return st;
+    counts[0] = v[0];
+    counts[1] = v[1];
+    return CE_OK;
+}
+
+int ce_device_error_reset(ce_stream_t stream) {
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    return cuda_status(reset_status(stream));
+}
+
+int ce_debug_force(int path, int cluster, int threads) {
+    if (path < 0 || path > 2 || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
+    if (threads != 0 && threads != 128 && threads != 256 && threads != 512) return CE_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_force.path = path;
+    g_force.cluster = cluster;
+    g_force.threads = threads;
+    return CE_OK;
+}
+
+int ce_plan(int op, int64_t rows, int64_t vocab, int64_t stride, int64_t out[6]) {
+    if (out == nullptr || op < 0 || op > 2) return CE_EINVAL;
+    if (rows < 1 || vocab < 1 || vocab > kMaxVocab || stride < vocab) return CE_EINVAL;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    Plan p;
+    if ((st = make_plan(static_cast<Op>(op), rows, vocab, dev, &p))) return st;
+    out[0] = p.path;
+    out[1] = p.cluster;
+    out[2] = p.threads;
+    out[3] = p.smem;
+    out[4] = p.cols;
+    out[5] = p.clusters * p.cluster;
+    return CE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,259 @@
+// ce_device.cuh -- device-side building blocks of the row-wise softmax
+// cross-entropy kernels for sm_103a: inline-PTX wrappers (mbarrier, bulk
+// asynchronous copies, thread-block clusters and distributed shared memory,
+// streaming loads and stores) and the per-row online state.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace cerows {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr int kNoIndex = 0x7fffffff;  // "no column seen yet"
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// mbarrier in this CTA's shared memory
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// make mbarrier initialisation visible to the async proxy and the cluster
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// order this thread's earlier generic-proxy shared accesses before later
+// async-proxy (bulk copy) accesses
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete, for at most
+// `limit_ns` nanoseconds and 2^24 polls. Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = 200000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 63 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+    return false;
+}
+
+// Bulk asynchronous copy (the TMA engine, no tensor map) from global memory
+// into this CTA's shared memory; completion is signalled on `bar` as bytes.
+// dst and src must be 16-byte aligned and bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy: lines read once are the first to be evicted.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// thread-block cluster
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// every thread of every CTA of the cluster calls these, in uniform control flow
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_smem(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// global loads and stores
+// read-only data read once: skip L1
+__device__ __forceinline__ float4 ld_stream_f4(const float4 *p) {
+    float4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float ld_stream_f1(const float *p) {
+    float v;
+    asm("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Online row state.
+//
+// Over the columns pushed so far: m is their max (NaN is skipped: it never
+// compares greater), idx the first column holding m (kNoIndex if none), and
+// t = sum of exp(x_j - m) over every pushed column but one that holds m --
+// so the row's exp-sum is 1 + t. Keeping the "1" out of t lets the loss be
+// formed as (m - x[label]) + log1p(t) without cancellation.
+//
+// Push x (column j):
+//   x >  m:  t <- (1 + t) * exp(m - x),  m <- x,  idx <- j
+//   x == m:  t <- t + 1                  (a tie; idx keeps the first)
+//   else:    t <- t + exp(x - m)         (NaN x makes t NaN, and it stays NaN)
+// x == m also covers -inf == -inf and +inf == +inf, where x - m is NaN.
+// In the first two cases exp takes -|x - m|, so one exp serves both.
+//
+// Merge two states: the winner has the larger m (ties: smaller idx); then
+//   t <- t_w + (1 + t_l) * exp(m_l - m_w).
+// The merge is symmetric, so a butterfly gives every lane the same bits.
+
+struct RowState {
+    float m;
+    float t;
+    int idx;
+};
+
+__device__ __forceinline__ RowState empty_state() { return RowState{-INFINITY, 0.0f, kNoIndex}; }
+
+template <bool kStats>
+__device__ __forceinline__ void push(RowState &s, float x, int j) {
+    const bool gt = x > s.m;
+    const bool eq = x == s.m;
+    if (kStats) {
+        const float e = eq ? 1.0f : expf(-fabsf(x - s.m));
+        s.t = gt ? fmaf(s.t, e, e) : s.t + e;
+    }
+    s.idx = gt ? j : (eq ? min(s.idx, j) : s.idx);
+    s.m = gt ? x : s.m;
+}
+
+template <bool kStats>
+__device__ __forceinline__ void push4(RowState &s, float4 v, int j) {
+    push<kStats>(s, v.x, j);
+    push<kStats>(s, v.y, j + 1);
+    push<kStats>(s, v.z, j + 2);
+    push<kStats>(s, v.w, j + 3);
+}
+
+template <bool kStats>
+__device__ __forceinline__ RowState merge(const RowState a, const RowState b) {
+    const bool b_wins = (b.m > a.m) || (b.m == a.m && b.idx < a.idx);
+    RowState r;
+    r.m = b_wins ? b.m : a.m;
+    r.idx = b_wins ? b.idx : a.idx;
+    r.t = 0.0f;
+    if (kStats) {
+        const float wt = b_wins ? b.t : a.t;
+        const float lt = b_wins ? a.t : b.t;
+        const float lm = b_wins ? a.m : b.m;
+        const float e = (lm == r.m) ? 1.0f : expf(lm - r.m);
+        r.t = fmaf(1.0f + lt, e, wt);
+    }
+    return r;
+}
+
+template <bool kStats>
+__device__ __forceinline__ RowState shfl_xor_state(const RowState &s, int o) {
+    RowState q;
+    q.m = __shfl_xor_sync(kFullMask, s.m, o);
+    q.t = kStats ? __shfl_xor_sync(kFullMask, s.t, o) : 0.0f;
+    q.idx = __shfl_xor_sync(kFullMask, s.idx, o);
+    return q;
+}
+
+template <bool kStats>
+__device__ __forceinline__ RowState warp_reduce(RowState s) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s = merge<kStats>(s, shfl_xor_state<kStats>(s, o));
+    return s;
+}
+
+// Reduce over the CTA; every thread gets the result. `red` holds >= 32
+// states in shared memory. Contains two __syncthreads.
+template <bool kStats>
+__device__ __forceinline__ RowState block_reduce(RowState s, RowState *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    s = warp_reduce<kStats>(s);
+    if (lane == 0) red[warp] = s;
+    __syncthreads();
+    RowState r = lane < nwarps ? red[lane] : empty_state();
+    r = warp_reduce<kStats>(r);
+    __syncthreads();
+    return r;
+}
+
+// What a CTA publishes to its cluster peers for one row.
+struct __align__(16) Xchg {
+    float m;
+    float t;
+    int idx;
+    float xl;  // x[label], if the label column lies in this CTA's slice
+};
+
+__device__ __forceinline__ Xchg ld_peer_xchg(const Xchg *x, uint32_t rank) {
+    const float4 v = ld_dsmem_f4(peer_smem(x, rank));
+    return Xchg{v.x, v.y, __float_as_int(v.z), v.w};
+}
+
+}  // namespace cerows

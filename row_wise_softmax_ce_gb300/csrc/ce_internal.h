@@ -1,0 +1,60 @@
+// ce_internal.h -- launch plans and kernel launchers shared by the C ABI
+// (ce_api.cu) and the kernels (ce_kernels.cu). Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace cerows {
+
+enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2 };
+enum Op : int { kOpRows = 0, kOpGrad = 1, kOpArgmax = 2 };
+
+// Per-CTA shared bytes the staged kernel reserves before its row buffer.
+constexpr int kStagedHeaderBytes = 1024;
+constexpr int kMaxCluster = 16;
+// Largest CTA each kernel family is compiled for (its __launch_bounds__).
+constexpr int kStagedMaxThreads = 512;
+constexpr int kStreamMaxThreads = 256;
+
+struct Plan {
+    int path = kPathStream;
+    int cluster = 1;       // CTAs per row (a thread-block cluster)
+    int threads = 256;     // threads per CTA
+    int smem = 0;          // dynamic shared bytes per CTA
+    int cols = 0;          // columns per CTA (a multiple of 4)
+    int64_t clusters = 0;  // clusters in the grid (each loops over rows)
+};
+
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    int max_smem_optin = 0;  // per block
+    int cc_major = 0, cc_minor = 0;
+};
+
+// Arguments of one launch; unused pointers are null.
+struct Args {
+    const float *logits;
+    int64_t rows;
+    int vocab;
+    int64_t stride;
+    const int64_t *labels;
+    float scale;
+    float *grad;
+    float *loss;
+    float *top;
+};
+
+cudaError_t set_kernel_attributes(const DeviceInfo &dev);
+cudaError_t max_active_clusters(const Plan &p, Op op, int *n);
+
+cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStream_t s);
+cudaError_t launch_grad_staged(const Plan &p, const Args &a, cudaStream_t s);
+cudaError_t launch_grad_stream(const Plan &p, const Args &a, cudaStream_t s);
+cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s);
+
+cudaError_t read_status(unsigned long long out[2], cudaStream_t s);
+cudaError_t reset_status(cudaStream_t s);
+
+}  // namespace cerows

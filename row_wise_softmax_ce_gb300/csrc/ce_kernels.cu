@@ -1,0 +1,466 @@
+// ce_kernels.cu -- sm_103a kernels of the row-wise softmax cross-entropy
+// path and their launchers.
+//
+// What they compute is defined on the API reference page "gizml:netops"
+// (gizstack.com/docs/reference/gizml/netops.md), section Functions:
+//   crossEntropyRows  each row's loss m + log(sum exp(x - m)) - x[label]
+//   crossEntropyLoss  the mean of the row losses in f64
+//   crossEntropyGrad  (softmax - onehot) * scale, softmax = exp(x - m) * f32(1/sum)
+//   argmaxInto        each row's token (first of equals, NaN never wins) as f32
+// and section Methods: Tensor.argmax (the tie and NaN rules).
+//
+// Kernel families (every one HBM-bound; none uses tensor cores):
+//   k_rows_stream   one read of each logit: the online (m, t, idx) state of
+//                   each thread's columns, merged over the CTA and then over
+//                   the CTAs of a thread-block cluster that share one row
+//                   through distributed shared memory. Writes the row loss
+//                   and/or the argmax token.
+//   k_grad_staged   fused loss + gradient: the cluster's CTAs bulk-copy
+//                   (TMA engine) their slices of a row into shared memory,
+//                   compute the state from there, exchange it over DSMEM,
+//                   then write the gradient from shared memory. HBM sees
+//                   each logit read once and each gradient written once.
+//   k_grad_stream   the same for rows too long to stage: two reads.
+//   k_mean          the mean of the row losses, an f64 fixed-shape tree.
+//
+// Every kernel loops over rows (row = cluster id, + number of clusters), so
+// any row count fits one launch.
+#include <cmath>
+#include <cstdint>
+
+#include "ce_device.cuh"
+#include "ce_internal.h"
+
+namespace cerows {
+
+// [0] rows seen with a label outside [0, vocab); [1] bounded waits that gave up.
+__device__ unsigned long long g_status[2];
+
+namespace {
+
+constexpr int kChunks = 4;  // bulk copies (and mbarriers) per staged slice
+constexpr int kUnroll = 4;  // 16-byte loads in flight per thread (streaming)
+
+struct alignas(16) StagedHeader {
+    uint64_t bar[kChunks];
+    Xchg xchg;
+    RowState red[32];
+    float bc[4];
+};
+static_assert(sizeof(StagedHeader) <= kStagedHeaderBytes, "staged header too large");
+
+__device__ __forceinline__ bool label_valid(int64_t label, int vocab) { return label >= 0 && label < vocab; }
+
+// The row loss from the merged state: (m - x[label]) + log1p(t); NaN for a
+// bad label, or a row whose max is +-inf (a +inf entry, or all -inf / NaN),
+// or whose t is NaN (a NaN entry).
+__device__ __forceinline__ float row_loss(const RowState &g, float xl, bool lab_ok) {
+    if (!lab_ok || !isfinite(g.m) || isnan(g.t)) return __int_as_float(0x7fffffff);
+    return (g.m - xl) + log1pf(g.t);
+}
+
+__device__ __forceinline__ float row_token(const RowState &g) {
+    return static_cast<float>(g.idx == kNoIndex ? 0 : g.idx);
+}
+
+// Push the columns [j0, j0 + n) of one row, read from global memory at p
+// (p -> column j0): a scalar head up to the first 16-byte boundary, 16-byte
+// vectors, a scalar tail. Each thread sees its columns in increasing order.
+template <bool kStats>
+__device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int j0, int n) {
+    RowState st = empty_state();
+    const int tid = threadIdx.x, T = blockDim.x;
+    const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+    const int head = min(n, (4 - off) & 3);
+    const int nvec = (n - head) >> 2;
+    const int tail = n - head - 4 * nvec;
+    const float4 *pv = reinterpret_cast<const float4 *>(p + head);
+    const int jv = j0 + head;
+    if (tid < head) push<kStats>(st, ld_stream_f1(p + tid), j0 + tid);
+    int k = tid;
+    for (; k + (kUnroll - 1) * T < nvec; k += kUnroll * T) {
+        float4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream_f4(pv + k + u * T);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) push4<kStats>(st, v[u], jv + 4 * (k + u * T));
+    }
+    for (; k < nvec; k += T) push4<kStats>(st, ld_stream_f4(pv + k), jv + 4 * k);
+    if (tid < tail) push<kStats>(st, ld_stream_f1(p + head + 4 * nvec + tid), jv + 4 * nvec + tid);
+    return st;
+}
+
+// ---------------------------------------------------------------------------
+// k_rows_stream: row loss (kStats) and/or argmax token; one read per logit.
+template <bool kStats>
+__global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, int cols) {
+    __shared__ RowState red[32];
+    __shared__ Xchg xchg;
+    const uint32_t rank = cluster_rank(), C = cluster_size();
+    const int tid = threadIdx.x;
+    const int c0 = static_cast<int>(rank) * cols;
+    const int n = max(0, min(a.vocab, c0 + cols) - c0);
+    bool pending = false;  // a cluster arrive without its wait
+    for (int64_t row = cluster_id_x(); row < a.rows; row += cluster_count_x()) {
+        // the label and x[label], fetched early by the CTA that writes the loss
+        int64_t label = 0;
+        float xl = 0.0f;
+        bool lab_ok = true;
+        if (kStats && rank == 0 && tid == 0) {
+            label = a.labels[row];
+            lab_ok = label_valid(label, a.vocab);
+            if (lab_ok) xl = a.logits[row * a.stride + label];
+        }
+        RowState st = empty_state();
+        if (n > 0) st = scan_global<kStats>(a.logits + row * a.stride + c0, c0, n);
+        st = block_reduce<kStats>(st, red);
+        if (pending) cluster_wait();  // peers finished reading the previous row's xchg
+        if (tid == 0) xchg = Xchg{st.m, st.t, st.idx, 0.0f};
+        cluster_arrive();
+        cluster_wait();
+        if (rank == 0 && tid == 0) {
+            RowState g = empty_state();
+            for (uint32_t r = 0; r < C; ++r) {
+                const Xchg q = ld_peer_xchg(&xchg, r);
+                g = merge<kStats>(g, RowState{q.m, q.t, q.idx});
+            }
+            if (kStats && a.loss) {
+                a.loss[row] = row_loss(g, xl, lab_ok);
+                if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+            }
+            if (a.top) a.top[row] = row_token(g);
+        }
+        cluster_arrive();
+        pending = true;
+    }
+    if (pending) cluster_wait();  // no CTA leaves while a peer may still read its xchg
+}
+
+// ---------------------------------------------------------------------------
+// k_grad_staged: fused loss + gradient (+ token) from shared-memory slices.
+//
+// CTA `rank` of a cluster owns columns [rank * cols, rank * cols + cols) of
+// the cluster's row. Its slice sits in shared memory at buf[off + k] for
+// column c0 + k, where off = the slice's start modulo 16 bytes (in floats),
+// so that the 16-byte-aligned body lands 16-byte aligned and can be copied
+// by kChunks bulk copies; the at most 3 + 3 unaligned end columns are
+// copied by plain loads.
+__global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, int cols) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    StagedHeader &h = *reinterpret_cast<StagedHeader *>(smem);
+    float *buf = reinterpret_cast<float *>(smem + kStagedHeaderBytes);
+    const uint32_t rank = cluster_rank(), C = cluster_size();
+    const int tid = threadIdx.x, T = blockDim.x;
+    const int c0 = static_cast<int>(rank) * cols;
+    const int n = max(0, min(a.vocab, c0 + cols) - c0);
+    const float scale = a.scale;
+
+    uint64_t policy = 0;
+    if (tid == 0) {
+        for (int c = 0; c < kChunks; ++c) mbar_init(&h.bar[c], 1);
+        fence_mbar_init();
+        policy = l2_policy_evict_first();
+    }
+    __syncthreads();
+
+    bool failed = false;
+    bool pending = false;
+    uint32_t parity = 0;
+    for (int64_t row = cluster_id_x(); row < a.rows; row += cluster_count_x(), parity ^= 1u) {
+        const float *p = a.logits + row * a.stride + c0;
+        const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+        const int head = min(n, (4 - off) & 3);
+        const int nvec = (n - head) >> 2;
+        const int tail = n - head - 4 * nvec;
+        const int vpc = (nvec + kChunks - 1) / kChunks;  // vectors per chunk
+        float4 *bufv = reinterpret_cast<float4 *>(buf + off + head);
+        const int jv = c0 + head;
+
+        // 1. start the bulk copies of the aligned body
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            for (int c = 0; c < kChunks; ++c) {
+                const int v0 = min(nvec, c * vpc), v1 = min(nvec, v0 + vpc);
+                const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
+                mbar_arrive_expect_tx(&h.bar[c], bytes);
+                if (bytes) bulk_copy_g2s(bufv + v0, p + head + 4 * v0, bytes, &h.bar[c], policy);
+            }
+        }
+        // 2. the unaligned end columns, and the label
+        if (tid < head) buf[off + tid] = p[tid];
+        if (tid >= 32 && tid - 32 < tail) buf[off + head + 4 * nvec + (tid - 32)] = p[head + 4 * nvec + (tid - 32)];
+        const int64_t label = a.labels[row];
+        const bool lab_ok = label_valid(label, a.vocab);
+        const int lab_local = (lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
+        __syncthreads();
+
+        // 3. pass 1: the state of this thread's columns, from shared memory
+        RowState st = empty_state();
+        if (tid < head) push<true>(st, buf[off + tid], c0 + tid);
+        {
+            int ready = 0, c = 0;
+            for (int k = tid; k < nvec; k += T) {
+                while (k >= ready) {
+                    if (!failed) failed = !mbar_wait_bounded(&h.bar[c], parity);
+                    ready += vpc;
+                    ++c;
+                }
+                push4<true>(st, bufv[k], jv + 4 * k);
+            }
+        }
+        if (tid < tail) push<true>(st, buf[off + head + 4 * nvec + tid], jv + 4 * nvec + tid);
+        // every thread sees every chunk complete before any reads it in pass 2
+        for (int c = 0; c < kChunks; ++c)
+            if (!failed) failed = !mbar_wait_bounded(&h.bar[c], parity);
+        st = block_reduce<true>(st, h.red);
+
+        // 4. exchange over the cluster
+        if (pending) cluster_wait();
+        if (tid == 0) h.xchg = Xchg{st.m, st.t, st.idx, lab_local >= 0 ? buf[off + lab_local] : 0.0f};
+        cluster_arrive();
+        cluster_wait();
+        if (tid == 0) {
+            RowState g = empty_state();
+            float xl = 0.0f;
+            const uint32_t owner = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
+            for (uint32_t r = 0; r < C; ++r) {
+                const Xchg q = ld_peer_xchg(&h.xchg, r);
+                g = merge<true>(g, RowState{q.m, q.t, q.idx});
+                if (r == owner) xl = q.xl;
+            }
+            const bool bad = !isfinite(g.m) || isnan(g.t);
+            h.bc[0] = g.m;
+            h.bc[1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);  // f32(1/sum)
+            if (rank == 0) {
+                if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
+                if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+                if (a.top) a.top[row] = row_token(g);
+            }
+        }
+        __syncthreads();
+        cluster_arrive();
+        pending = true;
+        const float M = h.bc[0], rcp = h.bc[1];
+
+        // 5. pass 2: the gradient, from shared memory to HBM
+        float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;
+        const int goff = static_cast<int>((reinterpret_cast<uintptr_t>(gp) >> 2) & 3);
+        if (goff == off) {
+            if (tid < head) {
+                const float pr = expf(buf[off + tid] - M) * rcp;
+                gp[tid] = (tid == lab_local ? pr - 1.0f : pr) * scale;
+            }
+            float4 *gv = reinterpret_cast<float4 *>(gp + head);
+            const int lab_vec = lab_local >= head ? (lab_local - head) >> 2 : -1;
+            for (int k = tid; k < nvec; k += T) {
+                const float4 v = bufv[k];
+                float4 pr;
+                pr.x = expf(v.x - M) * rcp;
+                pr.y = expf(v.y - M) * rcp;
+                pr.z = expf(v.z - M) * rcp;
+                pr.w = expf(v.w - M) * rcp;
+                if (k == lab_vec) {
+                    const int lane = (lab_local - head) & 3;
+                    pr.x -= lane == 0 ? 1.0f : 0.0f;
+                    pr.y -= lane == 1 ? 1.0f : 0.0f;
+                    pr.z -= lane == 2 ? 1.0f : 0.0f;
+                    pr.w -= lane == 3 ? 1.0f : 0.0f;
+                }
+                __stcs(gv + k, make_float4(pr.x * scale, pr.y * scale, pr.z * scale, pr.w * scale));
+            }
+            if (tid < tail) {
+                const int kk = head + 4 * nvec + tid;
+                const float pr = expf(buf[off + kk] - M) * rcp;
+                gp[kk] = (kk == lab_local ? pr - 1.0f : pr) * scale;
+            }
+        } else {
+            // the gradient row is aligned differently from the logits row
+            for (int k = tid; k < n; k += T) {
+                const float pr = expf(buf[off + k] - M) * rcp;
+                __stcs(gp + k, (k == lab_local ? pr - 1.0f : pr) * scale);
+            }
+        }
+        __syncthreads();  // buf is free for the next row's copies
+    }
+    if (pending) cluster_wait();
+    if (__syncthreads_or(failed) && tid == 0) {
+        atomicAdd(&g_status[1], 1ull);
+        // give copies still in flight a last bounded chance to land
+        for (int c = 0; c < kChunks; ++c) (void)mbar_wait_bounded(&h.bar[c], parity ^ 1u, 10000000ull);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// k_grad_stream: fused loss + gradient for rows too long to stage; the
+// cluster's CTAs read their slices twice (state, then gradient).
+__global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, int cols) {
+    __shared__ RowState red[32];
+    __shared__ Xchg xchg;
+    __shared__ float bc[2];
+    const uint32_t rank = cluster_rank(), C = cluster_size();
+    const int tid = threadIdx.x, T = blockDim.x;
+    const int c0 = static_cast<int>(rank) * cols;
+    const int n = max(0, min(a.vocab, c0 + cols) - c0);
+    const float scale = a.scale;
+    bool pending = false;
+    for (int64_t row = cluster_id_x(); row < a.rows; row += cluster_count_x()) {
+        const float *p = a.logits + row * a.stride + c0;
+        const int64_t label = a.labels[row];
+        const bool lab_ok = label_valid(label, a.vocab);
+        const int lab_local = (lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
+        // x[label] is read before any CTA of the cluster writes (grad may alias logits)
+        const float xl_own = (tid == 0 && lab_local >= 0) ? p[lab_local] : 0.0f;
+        RowState st = empty_state();
+        if (n > 0) st = scan_global<true>(p, c0, n);
+        st = block_reduce<true>(st, red);
+        if (pending) cluster_wait();
+        if (tid == 0) xchg = Xchg{st.m, st.t, st.idx, xl_own};
+        cluster_arrive();
+        cluster_wait();
+        if (tid == 0) {
+            RowState g = empty_state();
+            float xl = 0.0f;
+            const uint32_t owner = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
+            for (uint32_t r = 0; r < C; ++r) {
+                const Xchg q = ld_peer_xchg(&xchg, r);
+                g = merge<true>(g, RowState{q.m, q.t, q.idx});
+                if (r == owner) xl = q.xl;
+            }
+            const bool bad = !isfinite(g.m) || isnan(g.t);
+            bc[0] = g.m;
+            bc[1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);
+            if (rank == 0) {
+                if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
+                if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+                if (a.top) a.top[row] = row_token(g);
+            }
+        }
+        __syncthreads();
+        cluster_arrive();
+        pending = true;
+        const float M = bc[0], rcp = bc[1];
+        float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;
+        // coherent loads: with grad == logits this thread writes what it read
+        for (int k = tid; k < n; k += T) {
+            const float pr = expf(__ldcs(p + k) - M) * rcp;
+            __stcs(gp + k, (k == lab_local ? pr - 1.0f : pr) * scale);
+        }
+        __syncthreads();  // bc is rewritten for the next row
+    }
+    if (pending) cluster_wait();
+}
+
+// ---------------------------------------------------------------------------
+// k_mean: one CTA. Thread k sums rows k, k + T, ... in f64; a butterfly over
+// each warp, then over the warps' sums. Fixed shape: same bits every run.
+__global__ void __launch_bounds__(1024) k_mean(const float *__restrict__ loss, int64_t rows,
+                                               double *__restrict__ out) {
+    __shared__ double part[32];
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) s += static_cast<double>(loss[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFullMask, s, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    if (lane == 0) part[warp] = s;
+    __syncthreads();
+    if (warp == 0) {
+        double r = lane < nwarps ? part[lane] : 0.0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(kFullMask, r, o);
+        if (lane == 0) *out = r / static_cast<double>(rows);
+    }
+}
+
+cudaError_t launch_clustered(const void *fn, const Plan &p, void **args, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.clusters * p.cluster), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+const void *kernel_of(const Plan &p, Op op) {
+    if (op == kOpGrad)
+        return p.path == kPathStaged ? reinterpret_cast<const void *>(&k_grad_staged)
+                                     : reinterpret_cast<const void *>(&k_grad_stream);
+    if (op == kOpRows) return reinterpret_cast<const void *>(&k_rows_stream<true>);
+    return reinterpret_cast<const void *>(&k_rows_stream<false>);
+}
+
+}  // namespace
+
+cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
+    const void *fns[] = {reinterpret_cast<const void *>(&k_rows_stream<true>),
+                         reinterpret_cast<const void *>(&k_rows_stream<false>),
+                         reinterpret_cast<const void *>(&k_grad_staged),
+                         reinterpret_cast<const void *>(&k_grad_stream)};
+    for (const void *f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_grad_staged),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
+}
+
+cudaError_t max_active_clusters(const Plan &p, Op op, int *n) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.cluster), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads), 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(p.smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(n, kernel_of(p, op), &cfg);
+}
+
+cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStream_t s) {
+    Args aa = a;
+    int cols = p.cols;
+    void *args[] = {&aa, &cols};
+    return launch_clustered(kernel_of(p, stats ? kOpRows : kOpArgmax), p, args, s);
+}
+
+cudaError_t launch_grad_staged(const Plan &p, const Args &a, cudaStream_t s) {
+    Args aa = a;
+    int cols = p.cols;
+    void *args[] = {&aa, &cols};
+    return launch_clustered(reinterpret_cast<const void *>(&k_grad_staged), p, args, s);
+}
+
+cudaError_t launch_grad_stream(const Plan &p, const Args &a, cudaStream_t s) {
+    Args aa = a;
+    int cols = p.cols;
+    void *args[] = {&aa, &cols};
+    return launch_clustered(reinterpret_cast<const void *>(&k_grad_stream), p, args, s);
+}
+
+cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s) {
+    k_mean<<<1, 1024, 0, s>>>(loss, rows, out);
+    return cudaGetLastError();
+}
+
+cudaError_t read_status(unsigned long long out[2], cudaStream_t s) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_status, sizeof(unsigned long long) * 2, 0,
+                                              cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(s);
+}
+
+cudaError_t reset_status(cudaStream_t s) {
+    static const unsigned long long zero[2] = {0ull, 0ull};
+    return cudaMemcpyToSymbolAsync(g_status, zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+}
+
+}  // namespace cerows

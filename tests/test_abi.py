@@ -1,0 +1,112 @@
+"""The C-ABI library loads and exports every function include/ce_rows.h
+declares; host-side argument checks reject bad calls before any launch.
+CPU only: no call here reaches a kernel."""
+import ctypes
+
+import pytest
+
+import row_wise_softmax_ce_gb300 as ce
+from row_wise_softmax_ce_gb300 import build as cuda_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return ce.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = ce.declared_functions()
+    assert set(names) >= {"ce_rows", "ce_mean", "ce_loss", "ce_grad", "argmax_rows", "ce_status_string",
+                          "ce_version", "ce_last_cuda_error", "ce_device_error_count",
+                          "ce_device_error_reset", "ce_debug_force", "ce_plan"}
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_only_declared_functions_are_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", ce.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {n for n in exported if n.startswith(("ce_", "argmax_"))}
+    assert ours == set(ce.declared_functions()), ours ^ set(ce.declared_functions())
+
+
+def test_version_and_status_strings(lib):
+    assert ce.version() == 10000
+    for st in (ce.CE_OK, ce.CE_EINVAL, ce.CE_EALIGN, ce.CE_ECUDA, ce.CE_EDEVICE, 12345):
+        assert isinstance(ce.status_string(st), str) and ce.status_string(st)
+
+
+V = ctypes.c_void_p
+
+
+@pytest.mark.parametrize("args", [
+    (V(256), -1, 10, 10),        # rows < 0
+    (V(256), 4, 0, 10),          # vocab < 1
+    (V(256), 4, 10, 9),          # stride < vocab
+    (V(256), 4, (1 << 24) + 1, (1 << 24) + 1),  # token not exact in f32
+    (None, 4, 10, 10),           # null logits
+])
+def test_bad_sizes_rejected_before_launch(lib, args):
+    logits, rows, vocab, stride = args
+    assert lib.ce_rows(logits, rows, vocab, stride, V(512), V(1024), None) == ce.CE_EINVAL
+    assert lib.argmax_rows(logits, rows, vocab, stride, V(1024), None) == ce.CE_EINVAL
+    assert lib.ce_grad(logits, rows, vocab, stride, V(512), 1.0, V(4096), None, None, None) == ce.CE_EINVAL
+
+
+def test_misaligned_pointers_rejected(lib):
+    assert lib.ce_rows(V(258), 4, 10, 10, V(512), V(1024), None) == ce.CE_EALIGN
+    assert lib.ce_rows(V(256), 4, 10, 10, V(516), V(1024), None) == ce.CE_EALIGN     # labels need 8 B
+    assert lib.argmax_rows(V(256), 4, 10, 10, V(1026), None) == ce.CE_EALIGN
+    assert lib.ce_mean(V(256), 4, V(260), None) == ce.CE_EALIGN                       # double out
+
+
+def test_null_outputs_and_bad_scale_rejected(lib):
+    assert lib.ce_rows(V(256), 4, 10, 10, None, V(1024), None) == ce.CE_EINVAL
+    assert lib.ce_rows(V(256), 4, 10, 10, V(512), None, None) == ce.CE_EINVAL
+    assert lib.argmax_rows(V(256), 4, 10, 10, None, None) == ce.CE_EINVAL
+    assert lib.ce_mean(V(256), 4, None, None) == ce.CE_EINVAL
+    assert lib.ce_loss(V(256), 4, 10, 10, V(512), V(1024), None, None) == ce.CE_EINVAL
+    for s in (float("nan"), float("inf")):
+        assert lib.ce_grad(V(256), 4, 10, 10, V(512), s, V(4096), None, None, None) == ce.CE_EINVAL
+    assert lib.ce_grad(V(256), 4, 10, 10, V(512), 1.0, None, None, None, None) == ce.CE_EINVAL
+
+
+def test_grad_overlap_rules(lib):
+    # in place needs stride == vocab; a partial overlap is rejected
+    assert lib.ce_grad(V(4096), 4, 10, 12, V(512), 1.0, V(4096), None, None, None) == ce.CE_EINVAL
+    assert lib.ce_grad(V(4096), 4, 10, 10, V(512), 1.0, V(4100), None, None, None) == ce.CE_EINVAL
+
+
+def test_zero_rows_is_a_no_op_without_device(lib):
+    # nothing is launched, so no device is needed
+    assert lib.ce_rows(None, 0, 10, 10, None, None, None) == ce.CE_OK
+    assert lib.argmax_rows(None, 0, 10, 10, None, None) == ce.CE_OK
+    assert lib.ce_grad(None, 0, 10, 10, None, 1.0, None, None, None, None) == ce.CE_OK
+
+
+def test_debug_force_validation(lib):
+    assert lib.ce_debug_force(3, 0, 0) == ce.CE_EINVAL
+    assert lib.ce_debug_force(0, 17, 0) == ce.CE_EINVAL
+    assert lib.ce_debug_force(0, 0, 1024) == ce.CE_EINVAL
+    assert lib.ce_debug_force(0, 0, 96) == ce.CE_EINVAL
+    assert lib.ce_debug_force(0, 0, 0) == ce.CE_OK
+
+
+def test_no_device_here_reports_edevice(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    assert lib.ce_rows(V(256), 4, 10, 10, V(512), V(1024), None) == ce.CE_EDEVICE
+    out = (ctypes.c_int64 * 6)()
+    assert lib.ce_plan(1, 8192, 128256, 128256, out) == ce.CE_EDEVICE
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 10)
+    with pytest.raises(ValueError):
+        ce.argmax_rows(x)
+    with pytest.raises(TypeError):
+        ce.argmax_rows(x.double())
