@@ -150,6 +150,12 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def l2_flush(buf: torch.Tensor) -> None:
+    """Evict L2 by reading a buffer of twice its size (a read leaves clean
+    lines, so the timed kernel pays no write-back of the flush)."""
+    torch.sum(buf)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -176,20 +182,28 @@ def barrier(ws: int):
 # CPU oracle timing
 
 
-def time_oracle(batch, sample_rows: int, threads: int):
-    """Oracle loss rows + gradient + argmax + mean over the first sample_rows rows."""
+def time_oracle(batch, sample_rows: int, threads: int, chunk: int = 1024):
+    """Wall time of the oracle's loss rows + gradient + argmax + mean over the
+    first sample_rows rows, taken in chunks of rows (bounded host memory)."""
+    import numpy as np
     import oracle
     orc = oracle.load()
     w = batch.workload
-    xs = batch.logits[:sample_rows].cpu().numpy()
-    ys = batch.labels[:sample_rows].cpu().numpy()
+    total = 0.0
+    losses = []
+    for a in range(0, sample_rows, chunk):
+        b = min(sample_rows, a + chunk)
+        xs = batch.logits[a:b].cpu().numpy()
+        ys = batch.labels[a:b].cpu().numpy()
+        t0 = time.perf_counter()
+        g, l = orc.ce_grad(xs, w.vocab, ys, batch.scale, threads=threads)
+        orc.argmax(xs, w.vocab, threads=threads)
+        total += time.perf_counter() - t0
+        losses.append(l)
+        del g
     t0 = time.perf_counter()
-    g, l = orc.ce_grad(xs, w.vocab, ys, batch.scale, threads=threads)
-    orc.argmax(xs, w.vocab, threads=threads)
-    orc.ce_mean(l)
-    dt = time.perf_counter() - t0
-    del g
-    return dt
+    orc.ce_mean(np.concatenate(losses))
+    return total + time.perf_counter() - t0
 
 
 def cpu_cores() -> int:
@@ -293,13 +307,13 @@ def run_ours(args):
     bd = W.generate(wd, device=dev)
     topd = torch.empty(wd.rows, dtype=torch.float32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    flush = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
     for _ in range(5):
         ce.argmax_rows(bd.logits, vocab=wd.vocab, out=topd)
     n_arg = max(20, min(200, K))
     times = []
     for _ in range(n_arg):
-        flush.fill_(1.0)
+        l2_flush(flush)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         ce.argmax_rows(bd.logits, vocab=wd.vocab, out=topd)
@@ -351,7 +365,7 @@ def run_ours(args):
         dt = time_oracle(b, sample, cores)
         cpu = {"value": round(step_bytes(sample, V) / dt / 1e9, 3), "unit": "GB/s", "cores": cores,
                "kind": "oracle", "sample": f"first {sample} of {R} rows of {w.name} "
-                                           f"(loss rows + gradient + argmax + mean, f64), {dt:.2f} s"}
+                                           f"(loss rows + gradient + argmax + mean, f64), {dt:.2f} s wall"}
 
     plan = ce.plan(ce.OP_GRAD, R, V)
     if rank == 0:
@@ -386,16 +400,84 @@ def run_ours(args):
     return 0
 
 
+def run_case(args):
+    """One operation on a chosen number of rows of a workload, with an optional
+    forced launch plan: for launch-shape sweeps and small profiler captures."""
+    import row_wise_softmax_ce_gb300 as ce
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    name = args.workload or (W.DECODE if args.case == "argmax" else W.HEADLINE)
+    w = W.WORKLOADS[name]
+    if args.rows:
+        w = w.with_rows(args.rows)
+    b = W.generate(w, device=dev)
+    R, V = w.rows, w.vocab
+    out = torch.empty(R, dtype=torch.float32, device=dev)
+    if args.case == "grad":
+        grad = torch.empty((R, V), dtype=torch.float32, device=dev)
+        op = lambda: ce.ce_grad(b.logits, b.labels, b.scale, vocab=V, grad=grad, loss_rows=out)
+        nbytes, opn = 8 * R * V + 12 * R, ce.OP_GRAD
+    elif args.case == "rows":
+        op = lambda: ce.ce_rows(b.logits, b.labels, vocab=V, out=out)
+        nbytes, opn = 4 * R * V + 12 * R, ce.OP_ROWS
+    else:
+        op = lambda: ce.argmax_rows(b.logits, vocab=V, out=out)
+        nbytes, opn = argmax_bytes(R, V), ce.OP_ARGMAX
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev) if args.flush else None
+    peak, kind = peaks()
+    for force in (args.force.split(";") if args.force else ["0,0,0"]):
+        ce.debug_force(*[int(v) for v in force.split(",")])
+        try:
+            for _ in range(max(1, args.warmup)):
+                op()
+            torch.cuda.synchronize()
+            evs = []
+            for _ in range(args.steps):
+                if flush is not None:
+                    l2_flush(flush)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                op()
+                e1.record(stream)
+                evs.append((e0, e1))
+            torch.cuda.synchronize()
+            plan = ce.plan(opn, R, V, w.stride)
+        except ce.CeError as e:
+            print(json.dumps({"case": args.case, "workload": w.name, "force": force, "error": str(e)}), flush=True)
+            continue
+        finally:
+            ce.debug_force(0, 0, 0)
+        ms = [a.elapsed_time(c) for a, c in evs]
+        med = statistics.median(ms)
+        print(json.dumps({"case": args.case, "workload": w.name, "rows": R, "vocab": V, "force": force,
+                          "plan": plan, "ms_median": round(med, 5), "ms_min": round(min(ms), 5),
+                          "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1),
+                          "frac": round(nbytes / (med * 1e-3) / 1e9 / peak, 4), "peak_kind": kind,
+                          "flush": bool(args.flush)}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=1024, help="rows of the CPU-oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=8192, help="rows of the CPU-oracle sample")
     ap.add_argument("--ref-rows", type=int, default=256, help="rows per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["grad", "rows", "argmax"],
+                    help="time one operation only (sweeps, profiler captures)")
+    ap.add_argument("--workload", choices=sorted(W.WORKLOADS), help="with --case: the workload")
+    ap.add_argument("--rows", type=int, default=0, help="with --case: rows of the workload to use")
+    ap.add_argument("--force", default="", help="with --case: path,cluster,threads (see ce_debug_force)")
+    ap.add_argument("--flush", action="store_true", help="with --case: flush L2 before each launch")
     args = ap.parse_args()
+    if args.case:
+        return run_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

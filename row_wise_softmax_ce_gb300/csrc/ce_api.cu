@@ -108,7 +108,7 @@ bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
     if (c > kMaxCluster) c = kMaxCluster;
     p.cluster = static_cast<int>(c);
     p.cols = round_up4(ceil_div(vocab, c));
-    p.smem = kStagedHeaderBytes + 4 * (p.cols + 4);
+    p.smem = kStagedHeaderBytes + 4 * (p.cols + 8);
     p.clusters = std::min<int64_t>(rows, kMaxClusters);
     if (p.smem > dev.max_smem_optin) return false;
     int active = 0;

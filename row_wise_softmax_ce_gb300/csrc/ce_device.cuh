@@ -46,27 +46,30 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+// One poll of the phase with the given parity. A thread whose phase has not
+// completed is suspended in hardware (it issues nothing) until the phase
+// completes or about `suspend_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t suspend_ns = 1000000u) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
         : "memory");
     return done != 0;
 }
 
 // Wait for the phase of `bar` with the given parity to complete, for at most
-// `limit_ns` nanoseconds and 2^24 polls. Returns false if it gave up.
+// `limit_ns` nanoseconds and 2^20 polls. Returns false if it gave up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns = 200000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 0; i < (1u << 24); ++i) {
+    for (uint32_t i = 0; i < (1u << 20); ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 63 && global_timer_ns() - t0 > limit_ns) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
     return false;
 }
@@ -111,13 +114,16 @@ __device__ __forceinline__ uint32_t cluster_count_x() {
     asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
     return r;
 }
-// every thread of every CTA of the cluster calls these, in uniform control flow
+// Every thread of every CTA of the cluster calls these, in uniform control
+// flow, alternating arrive and wait. The arrive is relaxed: a thread whose
+// shared-memory writes peers must see calls fence_cluster() first.
 __device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 // address of the same shared variable in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t peer_smem(const void *p, uint32_t rank) {
     uint32_t r;
@@ -196,6 +202,36 @@ __device__ __forceinline__ void push4(RowState &s, float4 v, int j) {
     push<kStats>(s, v.w, j + 3);
 }
 
+__device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
+
+// exp(d) for d <= 0 by the change of base exp(d) = 2^(d * log2(e)), with the
+// hardware base-2 exponential ex2.approx.ftz.f32 (relative error below 2^-22;
+// results below 2^-126 flush to 0, i.e. an absolute error below 1.2e-38).
+// Rounding the product d * log2(e) adds a relative error of about
+// |d| * 2^-24 to the result -- at most 2.2e-8 absolute, since |d| * exp(d)
+// <= 1/e for d <= 0.
+__device__ __forceinline__ float exp_le0(float d) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d * 1.4426950408889634f));
+    return y;
+}
+
+// Push four consecutive columns j..j+3. Common case: none of them exceeds the
+// running max m (and m is above -inf), so each adds exp(x - m) -- a tie adds
+// exactly 1 and keeps the first index, a NaN makes t NaN. Otherwise (a new
+// max, or no finite value yet, or all four NaN) the exact scalar update runs.
+// exp is CUDA's __expf intrinsic (documented error 2 + 1.2|x| ulp, so below
+// 1.3e-7 absolute on any exp(x - m) <= 1).
+template <bool kStats>
+__device__ __forceinline__ void push_vec(RowState &s, float4 v, int j) {
+    const float mv = max4(v);
+    if (mv <= s.m && s.m != -INFINITY) {
+        if (kStats) s.t += (exp_le0(v.x - s.m) + exp_le0(v.y - s.m)) + (exp_le0(v.z - s.m) + exp_le0(v.w - s.m));
+    } else {
+        push4<kStats>(s, v, j);
+    }
+}
+
 template <bool kStats>
 __device__ __forceinline__ RowState merge(const RowState a, const RowState b) {
     const bool b_wins = (b.m > a.m) || (b.m == a.m && b.idx < a.idx);
@@ -207,7 +243,7 @@ __device__ __forceinline__ RowState merge(const RowState a, const RowState b) {
         const float wt = b_wins ? b.t : a.t;
         const float lt = b_wins ? a.t : b.t;
         const float lm = b_wins ? a.m : b.m;
-        const float e = (lm == r.m) ? 1.0f : expf(lm - r.m);
+        const float e = (lm == r.m) ? 1.0f : exp_le0(lm - r.m);
         r.t = fmaf(1.0f + lt, e, wt);
     }
     return r;
@@ -229,17 +265,20 @@ __device__ __forceinline__ RowState warp_reduce(RowState s) {
     return s;
 }
 
-// Reduce over the CTA; every thread gets the result. `red` holds >= 32
-// states in shared memory. Contains two __syncthreads.
+// Reduce over the CTA into warp 0: every lane of warp 0 returns the CTA's
+// state (other warps return garbage). `red` holds >= 32 states in shared
+// memory. Contains one __syncthreads.
 template <bool kStats>
-__device__ __forceinline__ RowState block_reduce(RowState s, RowState *red) {
+__device__ __forceinline__ RowState block_reduce_w0(RowState s, RowState *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     s = warp_reduce<kStats>(s);
     if (lane == 0) red[warp] = s;
     __syncthreads();
-    RowState r = lane < nwarps ? red[lane] : empty_state();
-    r = warp_reduce<kStats>(r);
-    __syncthreads();
+    RowState r = empty_state();
+    if (warp == 0) {
+        if (lane < nwarps) r = red[lane];
+        r = warp_reduce<kStats>(r);
+    }
     return r;
 }
 
@@ -254,6 +293,23 @@ struct __align__(16) Xchg {
 __device__ __forceinline__ Xchg ld_peer_xchg(const Xchg *x, uint32_t rank) {
     const float4 v = ld_dsmem_f4(peer_smem(x, rank));
     return Xchg{v.x, v.y, __float_as_int(v.z), v.w};
+}
+
+// In warp 0: merge the C published states of the cluster (lane r reads CTA
+// r's), a fixed tree, so every CTA of the cluster gets the same bits. Lane 0
+// returns the row state; *xl gets the x[label] published by CTA `owner`.
+template <bool kStats>
+__device__ __forceinline__ RowState cluster_merge_w0(const Xchg *x, uint32_t C, uint32_t owner, float *xl) {
+    const int lane = threadIdx.x & 31;
+    RowState s = empty_state();
+    float v = 0.0f;
+    if (lane < static_cast<int>(C)) {
+        const Xchg q = ld_peer_xchg(x, static_cast<uint32_t>(lane));
+        s = RowState{q.m, q.t, q.idx};
+        v = q.xl;
+    }
+    *xl = __shfl_sync(kFullMask, v, static_cast<int>(owner));
+    return warp_reduce<kStats>(s);
 }
 
 }  // namespace cerows

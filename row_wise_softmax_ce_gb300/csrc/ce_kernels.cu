@@ -83,9 +83,9 @@ __device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream_f4(pv + k + u * T);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) push4<kStats>(st, v[u], jv + 4 * (k + u * T));
+        for (int u = 0; u < kUnroll; ++u) push_vec<kStats>(st, v[u], jv + 4 * (k + u * T));
     }
-    for (; k < nvec; k += T) push4<kStats>(st, ld_stream_f4(pv + k), jv + 4 * k);
+    for (; k < nvec; k += T) push_vec<kStats>(st, ld_stream_f4(pv + k), jv + 4 * k);
     if (tid < tail) push<kStats>(st, ld_stream_f1(p + head + 4 * nvec + tid), jv + 4 * nvec + tid);
     return st;
 }
@@ -113,22 +113,25 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
         }
         RowState st = empty_state();
         if (n > 0) st = scan_global<kStats>(a.logits + row * a.stride + c0, c0, n);
-        st = block_reduce<kStats>(st, red);
+        st = block_reduce_w0<kStats>(st, red);
         if (pending) cluster_wait();  // peers finished reading the previous row's xchg
-        if (tid == 0) xchg = Xchg{st.m, st.t, st.idx, 0.0f};
+        if (tid == 0) {
+            xchg = Xchg{st.m, st.t, st.idx, 0.0f};
+            fence_cluster();
+        }
         cluster_arrive();
         cluster_wait();
-        if (rank == 0 && tid == 0) {
-            RowState g = empty_state();
-            for (uint32_t r = 0; r < C; ++r) {
-                const Xchg q = ld_peer_xchg(&xchg, r);
-                g = merge<kStats>(g, RowState{q.m, q.t, q.idx});
+        if (rank == 0 && tid < 32) {
+            float unused;
+            const RowState g = cluster_merge_w0<kStats>(&xchg, C, 0u, &unused);
+            if (tid == 0) {
+                if (kStats && a.loss) {
+                    a.loss[row] = row_loss(g, xl, lab_ok);
+                    if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+                }
+                if (a.top) a.top[row] = row_token(g);
             }
-            if (kStats && a.loss) {
-                a.loss[row] = row_loss(g, xl, lab_ok);
-                if (!lab_ok) atomicAdd(&g_status[0], 1ull);
-            }
-            if (a.top) a.top[row] = row_token(g);
+            fence_cluster();
         }
         cluster_arrive();
         pending = true;
@@ -139,16 +142,26 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
 // ---------------------------------------------------------------------------
 // k_grad_staged: fused loss + gradient (+ token) from shared-memory slices.
 //
-// CTA `rank` of a cluster owns columns [rank * cols, rank * cols + cols) of
-// the cluster's row. Its slice sits in shared memory at buf[off + k] for
-// column c0 + k, where off = the slice's start modulo 16 bytes (in floats),
-// so that the 16-byte-aligned body lands 16-byte aligned and can be copied
-// by kChunks bulk copies; the at most 3 + 3 unaligned end columns are
-// copied by plain loads.
+// CTA `rank` of a cluster owns columns [c0, c0 + n), c0 = rank * cols, of the
+// cluster's row. Its slice sits in shared memory on the 16-byte grid of the
+// logits: float i of buf holds column c0 - off + i, where off = the slice's
+// start modulo 16 bytes (in floats). The aligned body (whole 16-byte vectors)
+// arrives by kChunks bulk copies; the at most two partial end vectors are
+// filled by plain loads, with -inf in the lanes outside the slice (-inf adds
+// nothing to a max or an exp-sum). Every pass then works on whole vectors:
+//   sweep 1  each thread's max m over its vectors, and the first vector
+//            holding it;
+//   sweep 2  t = sum of exp(x - m) over its columns but the first one
+//            holding m (that element is set to -inf for the sweep);
+//   merge    over the CTA, then over the cluster through DSMEM, in rank
+//            order, so every CTA holds the same row state;
+//   write    grad = (exp(x - M) * f32(1/(1 + T)) - onehot) * scale,
+//            16-byte streaming stores.
 __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, int cols) {
     extern __shared__ __align__(128) unsigned char smem[];
     StagedHeader &h = *reinterpret_cast<StagedHeader *>(smem);
     float *buf = reinterpret_cast<float *>(smem + kStagedHeaderBytes);
+    float4 *buf4 = reinterpret_cast<float4 *>(buf);
     const uint32_t rank = cluster_rank(), C = cluster_size();
     const int tid = threadIdx.x, T = blockDim.x;
     const int c0 = static_cast<int>(rank) * cols;
@@ -170,114 +183,148 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         const float *p = a.logits + row * a.stride + c0;
         const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
         const int head = min(n, (4 - off) & 3);
-        const int nvec = (n - head) >> 2;
-        const int tail = n - head - 4 * nvec;
-        const int vpc = (nvec + kChunks - 1) / kChunks;  // vectors per chunk
-        float4 *bufv = reinterpret_cast<float4 *>(buf + off + head);
-        const int jv = c0 + head;
+        const int nvec = (n - head) >> 2;       // whole body vectors
+        const int qa = (off + head) >> 2;       // first body vector (0 or 1)
+        const int nq = (off + n + 3) >> 2;      // vectors covering the slice
+        const int vpc = (nvec + kChunks - 1) / kChunks;
+        const int jbase = c0 - off;             // column of float 0 of buf
 
-        // 1. start the bulk copies of the aligned body
+        // 1. bulk copies of the body
         if (tid == 0) {
             fence_proxy_async_smem();
             for (int c = 0; c < kChunks; ++c) {
                 const int v0 = min(nvec, c * vpc), v1 = min(nvec, v0 + vpc);
                 const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
                 mbar_arrive_expect_tx(&h.bar[c], bytes);
-                if (bytes) bulk_copy_g2s(bufv + v0, p + head + 4 * v0, bytes, &h.bar[c], policy);
+                if (bytes) bulk_copy_g2s(buf4 + qa + v0, p - off + 4 * (qa + v0), bytes, &h.bar[c], policy);
             }
         }
-        // 2. the unaligned end columns, and the label
-        if (tid < head) buf[off + tid] = p[tid];
-        if (tid >= 32 && tid - 32 < tail) buf[off + head + 4 * nvec + (tid - 32)] = p[head + 4 * nvec + (tid - 32)];
+        // 2. the partial end vectors: column or -inf
+        if (tid < 4 && qa == 1) {
+            buf[tid] = (tid >= off && tid - off < n) ? p[tid - off] : -INFINITY;
+        }
+        if (tid >= 32 && tid < 36 && qa + nvec < nq) {
+            const int i = 4 * (qa + nvec) + (tid - 32);
+            buf[i] = (i >= off && i - off < n) ? p[i - off] : -INFINITY;
+        }
         const int64_t label = a.labels[row];
         const bool lab_ok = label_valid(label, a.vocab);
         const int lab_local = (lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
         __syncthreads();
 
-        // 3. pass 1: the state of this thread's columns, from shared memory
-        RowState st = empty_state();
-        if (tid < head) push<true>(st, buf[off + tid], c0 + tid);
+        // 3. sweep 1: max and its first vector
+        float m = -INFINITY;
+        int qm = -1;
         {
-            int ready = 0, c = 0;
-            for (int k = tid; k < nvec; k += T) {
-                while (k >= ready) {
-                    if (!failed) failed = !mbar_wait_bounded(&h.bar[c], parity);
-                    ready += vpc;
-                    ++c;
+            int ready = qa, c = 0;
+            for (int q = tid; q < nq; q += T) {
+                if (q >= qa && q < qa + nvec) {
+                    while (q >= ready) {
+                        if (!failed) failed = !mbar_wait_bounded(&h.bar[c], parity);
+                        ready += vpc;
+                        ++c;
+                    }
                 }
-                push4<true>(st, bufv[k], jv + 4 * k);
+                const float mv = max4(buf4[q]);
+                if (mv > m) {
+                    m = mv;
+                    qm = q;
+                }
             }
         }
-        if (tid < tail) push<true>(st, buf[off + head + 4 * nvec + tid], jv + 4 * nvec + tid);
-        // every thread sees every chunk complete before any reads it in pass 2
-        for (int c = 0; c < kChunks; ++c)
-            if (!failed) failed = !mbar_wait_bounded(&h.bar[c], parity);
-        st = block_reduce<true>(st, h.red);
+        // x[label]: read by the thread that owns (and has waited for) its vector
+        const int lab_f = lab_local >= 0 ? off + lab_local : -1;  // float index of the label
+        const int lab_q = lab_f >> 2;
+        if (lab_q >= 0 && lab_q % T == tid) h.bc[2] = buf[lab_f];
+        __syncthreads();  // x[label] is read before any element is masked below
 
-        // 4. exchange over the cluster
+        // 4. sweep 2: e = exp(x - m) over this thread's vectors, kept in shared
+        //    memory for the write; t sums all of them but the first element
+        //    holding m (masked to -inf for the sweep, then given e = 1).
+        RowState st;
+        if (m != -INFINITY) {
+            const float4 vm = buf4[qm];
+            const int lm = vm.x == m ? 0 : vm.y == m ? 1 : vm.z == m ? 2 : 3;
+            buf[4 * qm + lm] = -INFINITY;
+            float t = 0.0f;
+            for (int q = tid; q < nq; q += T) {
+                const float4 v = buf4[q];
+                const float4 e = make_float4(exp_le0(v.x - m), exp_le0(v.y - m), exp_le0(v.z - m), exp_le0(v.w - m));
+                t += (e.x + e.y) + (e.z + e.w);
+                buf4[q] = e;
+            }
+            buf[4 * qm + lm] = 1.0f;
+            st = RowState{m, t, jbase + 4 * qm + lm};
+        } else {
+            // no value above -inf among this thread's columns: the exact
+            // update; e is 0 for -inf and NaN for NaN
+            st = empty_state();
+            for (int q = tid; q < nq; q += T) {
+                for (int l = 0; l < 4; ++l) {
+                    const int i = 4 * q + l;
+                    const float x = buf[i];
+                    if (i >= off && i - off < n) push<true>(st, x, jbase + i);
+                    buf[i] = x != x ? x : 0.0f;
+                }
+            }
+        }
+        st = block_reduce_w0<true>(st, h.red);
+
+        // 5. exchange over the cluster
         if (pending) cluster_wait();
-        if (tid == 0) h.xchg = Xchg{st.m, st.t, st.idx, lab_local >= 0 ? buf[off + lab_local] : 0.0f};
+        if (tid == 0) {
+            h.xchg = Xchg{st.m, st.t, st.idx, lab_local >= 0 ? h.bc[2] : 0.0f};
+            fence_cluster();
+        }
         cluster_arrive();
         cluster_wait();
-        if (tid == 0) {
-            RowState g = empty_state();
-            float xl = 0.0f;
+        if (tid < 32) {
+            float xl;
             const uint32_t owner = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
-            for (uint32_t r = 0; r < C; ++r) {
-                const Xchg q = ld_peer_xchg(&h.xchg, r);
-                g = merge<true>(g, RowState{q.m, q.t, q.idx});
-                if (r == owner) xl = q.xl;
+            const RowState g = cluster_merge_w0<true>(&h.xchg, C, owner, &xl);
+            if (tid == 0) {
+                const bool bad = !isfinite(g.m) || isnan(g.t);
+                h.bc[0] = g.m;
+                h.bc[1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);  // f32(1/sum)
+                if (rank == 0) {
+                    if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
+                    if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+                    if (a.top) a.top[row] = row_token(g);
+                }
             }
-            const bool bad = !isfinite(g.m) || isnan(g.t);
-            h.bc[0] = g.m;
-            h.bc[1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);  // f32(1/sum)
-            if (rank == 0) {
-                if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
-                if (!lab_ok) atomicAdd(&g_status[0], 1ull);
-                if (a.top) a.top[row] = row_token(g);
-            }
+            fence_cluster();
         }
         __syncthreads();
         cluster_arrive();
         pending = true;
-        const float M = h.bc[0], rcp = h.bc[1];
 
-        // 5. pass 2: the gradient, from shared memory to HBM
-        float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;
+        // 6. the gradient, from shared memory to HBM:
+        //    softmax = e * exp(m - M) * r, grad = softmax * scale (- scale at the label)
+        const float M = h.bc[0], rcp = h.bc[1];
+        const float shift = (m != -INFINITY && M != m) ? exp_le0(m - M) : 1.0f;
+        const float sr = shift * rcp;
+        const float c = sr * scale;
+        float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;  // column c0
         const int goff = static_cast<int>((reinterpret_cast<uintptr_t>(gp) >> 2) & 3);
-        if (goff == off) {
-            if (tid < head) {
-                const float pr = expf(buf[off + tid] - M) * rcp;
-                gp[tid] = (tid == lab_local ? pr - 1.0f : pr) * scale;
+        for (int q = tid; q < nq; q += T) {
+            const float4 e = buf4[q];
+            float4 g = make_float4(e.x * c, e.y * c, e.z * c, e.w * c);
+            if (q == lab_q) {
+                const int l = lab_f & 3;
+                const float gl = (buf[lab_f] * sr - 1.0f) * scale;
+                g.x = l == 0 ? gl : g.x;
+                g.y = l == 1 ? gl : g.y;
+                g.z = l == 2 ? gl : g.z;
+                g.w = l == 3 ? gl : g.w;
             }
-            float4 *gv = reinterpret_cast<float4 *>(gp + head);
-            const int lab_vec = lab_local >= head ? (lab_local - head) >> 2 : -1;
-            for (int k = tid; k < nvec; k += T) {
-                const float4 v = bufv[k];
-                float4 pr;
-                pr.x = expf(v.x - M) * rcp;
-                pr.y = expf(v.y - M) * rcp;
-                pr.z = expf(v.z - M) * rcp;
-                pr.w = expf(v.w - M) * rcp;
-                if (k == lab_vec) {
-                    const int lane = (lab_local - head) & 3;
-                    pr.x -= lane == 0 ? 1.0f : 0.0f;
-                    pr.y -= lane == 1 ? 1.0f : 0.0f;
-                    pr.z -= lane == 2 ? 1.0f : 0.0f;
-                    pr.w -= lane == 3 ? 1.0f : 0.0f;
-                }
-                __stcs(gv + k, make_float4(pr.x * scale, pr.y * scale, pr.z * scale, pr.w * scale));
-            }
-            if (tid < tail) {
-                const int kk = head + 4 * nvec + tid;
-                const float pr = expf(buf[off + kk] - M) * rcp;
-                gp[kk] = (kk == lab_local ? pr - 1.0f : pr) * scale;
-            }
-        } else {
-            // the gradient row is aligned differently from the logits row
-            for (int k = tid; k < n; k += T) {
-                const float pr = expf(buf[off + k] - M) * rcp;
-                __stcs(gp + k, (k == lab_local ? pr - 1.0f : pr) * scale);
+            if (goff == off && q >= qa && q < qa + nvec) {
+                __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
+            } else {
+                const int i = 4 * q - off;  // column - c0 of lane 0
+                if (i >= 0 && i < n) __stcs(gp + i, g.x);
+                if (i + 1 >= 0 && i + 1 < n) __stcs(gp + i + 1, g.y);
+                if (i + 2 >= 0 && i + 2 < n) __stcs(gp + i + 2, g.z);
+                if (i + 3 >= 0 && i + 3 < n) __stcs(gp + i + 3, g.w);
             }
         }
         __syncthreads();  // buf is free for the next row's copies
@@ -312,28 +359,29 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
         const float xl_own = (tid == 0 && lab_local >= 0) ? p[lab_local] : 0.0f;
         RowState st = empty_state();
         if (n > 0) st = scan_global<true>(p, c0, n);
-        st = block_reduce<true>(st, red);
+        st = block_reduce_w0<true>(st, red);
         if (pending) cluster_wait();
-        if (tid == 0) xchg = Xchg{st.m, st.t, st.idx, xl_own};
+        if (tid == 0) {
+            xchg = Xchg{st.m, st.t, st.idx, xl_own};
+            fence_cluster();
+        }
         cluster_arrive();
         cluster_wait();
-        if (tid == 0) {
-            RowState g = empty_state();
-            float xl = 0.0f;
+        if (tid < 32) {
+            float xl;
             const uint32_t owner = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
-            for (uint32_t r = 0; r < C; ++r) {
-                const Xchg q = ld_peer_xchg(&xchg, r);
-                g = merge<true>(g, RowState{q.m, q.t, q.idx});
-                if (r == owner) xl = q.xl;
+            const RowState g = cluster_merge_w0<true>(&xchg, C, owner, &xl);
+            if (tid == 0) {
+                const bool bad = !isfinite(g.m) || isnan(g.t);
+                bc[0] = g.m;
+                bc[1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);
+                if (rank == 0) {
+                    if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
+                    if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+                    if (a.top) a.top[row] = row_token(g);
+                }
             }
-            const bool bad = !isfinite(g.m) || isnan(g.t);
-            bc[0] = g.m;
-            bc[1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);
-            if (rank == 0) {
-                if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
-                if (!lab_ok) atomicAdd(&g_status[0], 1ull);
-                if (a.top) a.top[row] = row_token(g);
-            }
+            fence_cluster();
         }
         __syncthreads();
         cluster_arrive();
@@ -342,7 +390,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
         float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;
         // coherent loads: with grad == logits this thread writes what it read
         for (int k = tid; k < n; k += T) {
-            const float pr = expf(__ldcs(p + k) - M) * rcp;
+            const float pr = exp_le0(__ldcs(p + k) - M) * rcp;
             __stcs(gp + k, (k == lab_local ? pr - 1.0f : pr) * scale);
         }
         __syncthreads();  // bc is rewritten for the next row
