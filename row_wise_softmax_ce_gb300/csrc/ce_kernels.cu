@@ -59,6 +59,18 @@ __device__ __forceinline__ float row_loss(const RowState &g, float xl, bool lab_
     return (g.m - xl) + log1pf(g.t);
 }
 
+// A 16-byte vector of shared-memory grid index q holding columns
+// c0 - off + 4q ... +3 of the row: the slice's columns, -inf elsewhere.
+__device__ __forceinline__ float4 load_edge(const float *p, int off, int n, int q) {
+    float v[4];
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+        const int i = 4 * q + l - off;  // column - c0
+        v[l] = (i >= 0 && i < n) ? p[i] : -INFINITY;
+    }
+    return make_float4(v[0], v[1], v[2], v[3]);
+}
+
 __device__ __forceinline__ float row_token(const RowState &g) {
     return static_cast<float>(g.idx == kNoIndex ? 0 : g.idx);
 }
@@ -199,18 +211,18 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                 if (bytes) bulk_copy_g2s(buf4 + qa + v0, p - off + 4 * (qa + v0), bytes, &h.bar[c], policy);
             }
         }
-        // 2. the partial end vectors: column or -inf
-        if (tid < 4 && qa == 1) {
-            buf[tid] = (tid >= off && tid - off < n) ? p[tid - off] : -INFINITY;
-        }
-        if (tid >= 32 && tid < 36 && qa + nvec < nq) {
-            const int i = 4 * (qa + nvec) + (tid - 32);
-            buf[i] = (i >= off && i - off < n) ? p[i - off] : -INFINITY;
-        }
+        // 2. the partial end vectors (at most two) are loaded by the threads
+        //    that own them, lanes outside the slice being -inf; the label
+        const int qe0 = qa == 1 ? 0 : -1;                      // leading partial vector
+        const int qe1 = qa + nvec < nq ? qa + nvec : -1;       // trailing partial vector
+        float4 edge0 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), edge1 = edge0;
+        if (qe0 >= 0 && qe0 % T == tid) edge0 = load_edge(p, off, n, qe0);
+        if (qe1 >= 0 && qe1 % T == tid) edge1 = load_edge(p, off, n, qe1);
         const int64_t label = a.labels[row];
         const bool lab_ok = label_valid(label, a.vocab);
         const int lab_local = (lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
-        __syncthreads();
+        const int lab_f = lab_local >= 0 ? off + lab_local : -1;  // float index of the label
+        const int lab_q = lab_f >> 2;
 
         // 3. sweep 1: max and its first vector
         float m = -INFINITY;
@@ -224,6 +236,8 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                         ready += vpc;
                         ++c;
                     }
+                } else {
+                    buf4[q] = q == qe0 ? edge0 : edge1;
                 }
                 const float mv = max4(buf4[q]);
                 if (mv > m) {
@@ -232,11 +246,9 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                 }
             }
         }
-        // x[label]: read by the thread that owns (and has waited for) its vector
-        const int lab_f = lab_local >= 0 ? off + lab_local : -1;  // float index of the label
-        const int lab_q = lab_f >> 2;
+        // x[label]: read by the thread that owns its vector, before it masks
+        // anything below (only that thread writes that vector)
         if (lab_q >= 0 && lab_q % T == tid) h.bc[2] = buf[lab_f];
-        __syncthreads();  // x[label] is read before any element is masked below
 
         // 4. sweep 2: e = exp(x - m) over this thread's vectors, kept in shared
         //    memory for the write; t sums all of them but the first element
@@ -306,18 +318,11 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         const float c = sr * scale;
         float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;  // column c0
         const int goff = static_cast<int>((reinterpret_cast<uintptr_t>(gp) >> 2) & 3);
+        const bool vec_store = goff == off;
         for (int q = tid; q < nq; q += T) {
             const float4 e = buf4[q];
-            float4 g = make_float4(e.x * c, e.y * c, e.z * c, e.w * c);
-            if (q == lab_q) {
-                const int l = lab_f & 3;
-                const float gl = (buf[lab_f] * sr - 1.0f) * scale;
-                g.x = l == 0 ? gl : g.x;
-                g.y = l == 1 ? gl : g.y;
-                g.z = l == 2 ? gl : g.z;
-                g.w = l == 3 ? gl : g.w;
-            }
-            if (goff == off && q >= qa && q < qa + nvec) {
+            const float4 g = make_float4(e.x * c, e.y * c, e.z * c, e.w * c);
+            if (vec_store && static_cast<unsigned>(q - qa) < static_cast<unsigned>(nvec)) {
                 __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
             } else {
                 const int i = 4 * q - off;  // column - c0 of lane 0
@@ -327,6 +332,9 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                 if (i + 3 >= 0 && i + 3 < n) __stcs(gp + i + 3, g.w);
             }
         }
+        // the label column: its owner stored e * c there above; this later
+        // store by the same thread replaces it
+        if (lab_q >= 0 && lab_q % T == tid) __stcs(gp + lab_local, (buf[lab_f] * sr - 1.0f) * scale);
         __syncthreads();  // buf is free for the next row's copies
     }
     if (pending) cluster_wait();
