@@ -148,7 +148,8 @@ CE_API int ce_device_error_reset(ce_stream_t stream);
 
 /*
  * Launch-plan override, for tests and tuning: forces the kernel family
- * (path: 0 automatic, 1 shared-memory-staged, 2 streaming from global), the
+ * (path: 0 automatic, 1 shared-memory-staged, 2 streaming from global,
+ * 3 persistent ring of bulk copies -- 256 threads only), the
  * CTAs that share one row (cluster: 0 automatic, else 1..16) and the
  * threads of a CTA (threads: 0 automatic, else 128, 256 or 512; the
  * streaming kernels take at most 256, the staged one at most 512).

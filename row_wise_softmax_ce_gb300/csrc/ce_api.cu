@@ -102,21 +102,45 @@ void plan_stream(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
 // slices are at most kStagedTargetCols columns (at most 16 CTAs).
 bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster) {
     p.path = kPathStaged;
-    p.threads = threads ? threads : kStagedMaxThreads;
+    p.threads = threads ? threads : 256;
     if (p.threads > kStagedMaxThreads) return false;
     int64_t c = cluster ? cluster : std::max<int64_t>(1, ceil_div(vocab, kStagedTargetCols));
     if (c > kMaxCluster) c = kMaxCluster;
     p.cluster = static_cast<int>(c);
     p.cols = round_up4(ceil_div(vocab, c));
-    p.smem = kStagedHeaderBytes + 4 * (p.cols + 8);
-    p.clusters = std::min<int64_t>(rows, kMaxClusters);
+    // the kernel's fixed ranges cover any row misalignment: 4 * kChunks * W floats
+    const int w = ((p.cols + 9) / 4 + 3) / 4;
+    p.smem = kStagedHeaderBytes + 16 * 4 * w;
     if (p.smem > dev.max_smem_optin) return false;
     int active = 0;
     if (max_active_clusters(p, kOpGrad, &active) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
     }
-    return active >= 1;
+    if (active < 1) return false;
+    p.clusters = std::min<int64_t>(rows, active);  // persistent: every cluster resident at once
+    return true;
+}
+
+// Launch shape of the persistent ring kernel: one 256-thread CTA per SM;
+// the fewest CTAs per row whose slices are at most 128 KB (so that the second
+// read of a slice finds it in L2); as many clusters as fit at once.
+bool plan_ring(Plan &p, int64_t rows, int64_t vocab, int cluster) {
+    p.path = kPathRing;
+    p.threads = kRingThreads;
+    int64_t c = cluster ? cluster : std::max<int64_t>(1, ceil_div(vocab * 4, 128 * 1024));
+    if (c > kMaxCluster) c = kMaxCluster;
+    p.cluster = static_cast<int>(c);
+    p.cols = round_up4(ceil_div(vocab, c));
+    p.smem = kRingSmemBytes;
+    int active = 0;
+    if (max_active_clusters(p, kOpGrad, &active) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (active < 1) return false;
+    p.clusters = std::min<int64_t>(rows, active);
+    return true;
 }
 
 int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *out) {
@@ -127,7 +151,10 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
     }
     Plan p;
     if (op == kOpGrad) {
-        if (f.path == kPathStaged) {
+        if (f.path == kPathRing) {
+            if (f.threads && f.threads != kRingThreads) return CE_EINVAL;
+            if (!plan_ring(p, rows, vocab, f.cluster)) return CE_EINVAL;
+        } else if (f.path == kPathStaged) {
             if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster)) return CE_EINVAL;
         } else if (f.path == kPathStream) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
@@ -230,6 +257,7 @@ int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t stride, co
     a.grad = grad;
     a.loss = loss_rows;
     a.top = top;
+    if (p.path == kPathRing) return cuda_status(launch_grad_ring(p, a, stream));
     if (p.path == kPathStaged) return cuda_status(launch_grad_staged(p, a, stream));
     return cuda_status(launch_grad_stream(p, a, stream));
 }
@@ -285,7 +313,7 @@ int ce_device_error_reset(ce_stream_t stream) {
 }
 
 int ce_debug_force(int path, int cluster, int threads) {
-    if (path < 0 || path > 2 || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
+    if (path < 0 || path > 3 || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
     if (threads != 0 && threads != 128 && threads != 256 && threads != 512) return CE_EINVAL;
     std::lock_guard<std::mutex> lock(g_mu);
     g_force.path = path;

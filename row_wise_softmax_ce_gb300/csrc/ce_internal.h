@@ -7,7 +7,7 @@
 
 namespace cerows {
 
-enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2 };
+enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2, kPathRing = 3 };
 enum Op : int { kOpRows = 0, kOpGrad = 1, kOpArgmax = 2 };
 
 // Per-CTA shared bytes the staged kernel reserves before its row buffer.
@@ -16,6 +16,12 @@ constexpr int kMaxCluster = 16;
 // Largest CTA each kernel family is compiled for (its __launch_bounds__).
 constexpr int kStagedMaxThreads = 512;
 constexpr int kStreamMaxThreads = 256;
+// The persistent ring kernel: CTA size (8 consumer warps + 1 producer warp),
+// chunks in flight (16 KB each), and its dynamic shared memory (header + ring).
+constexpr int kRingThreads = 288;
+constexpr int kRingSlots = 13;
+constexpr int kRingHeaderBytes = 2048;
+constexpr int kRingSmemBytes = kRingHeaderBytes + kRingSlots * (kRingThreads - 32) * 4 * 16;
 
 struct Plan {
     int path = kPathStream;
@@ -52,6 +58,7 @@ cudaError_t max_active_clusters(const Plan &p, Op op, int *n);
 cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStream_t s);
 cudaError_t launch_grad_staged(const Plan &p, const Args &a, cudaStream_t s);
 cudaError_t launch_grad_stream(const Plan &p, const Args &a, cudaStream_t s);
+cudaError_t launch_grad_ring(const Plan &p, const Args &a, cudaStream_t s);
 cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s);
 
 cudaError_t read_status(unsigned long long out[2], cudaStream_t s);

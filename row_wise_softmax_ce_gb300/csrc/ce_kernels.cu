@@ -152,23 +152,28 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
 }
 
 // ---------------------------------------------------------------------------
-// k_grad_staged: fused loss + gradient (+ token) from shared-memory slices.
+// k_grad_staged: fused loss + gradient (+ token) from shared-memory slices,
+// persistent, with the next row's slice prefetched as this one is written.
 //
 // CTA `rank` of a cluster owns columns [c0, c0 + n), c0 = rank * cols, of the
-// cluster's row. Its slice sits in shared memory on the 16-byte grid of the
-// logits: float i of buf holds column c0 - off + i, where off = the slice's
-// start modulo 16 bytes (in floats). The aligned body (whole 16-byte vectors)
-// arrives by kChunks bulk copies; the at most two partial end vectors are
-// filled by plain loads, with -inf in the lanes outside the slice (-inf adds
-// nothing to a max or an exp-sum). Every pass then works on whole vectors:
+// cluster's rows (cluster cid of G takes rows cid, cid + G, ...). A row's
+// slice sits in shared memory on the 16-byte grid of the logits: float i of
+// buf holds column c0 - off + i, off = the slice's start modulo 16 bytes (in
+// floats). The grid is cut into kChunks fixed ranges of W vectors; chunk c of
+// every row lands in range c, whatever that row's off. The aligned body of a
+// range arrives by one bulk copy (mbarrier bar[c], one phase per row); the at
+// most two partial end vectors are loaded by the threads that own them, with
+// -inf outside the slice. Thread t owns, in every pass, the vectors c*W + t +
+// T*i of each range c. Per row:
 //   sweep 1  each thread's max m over its vectors, and the first vector
 //            holding it;
-//   sweep 2  t = sum of exp(x - m) over its columns but the first one
-//            holding m (that element is set to -inf for the sweep);
-//   merge    over the CTA, then over the cluster through DSMEM, in rank
-//            order, so every CTA holds the same row state;
-//   write    grad = (exp(x - M) * f32(1/(1 + T)) - onehot) * scale,
-//            16-byte streaming stores.
+//   sweep 2  e = exp(x - m), kept in place; t = their sum but for the first
+//            element holding m;
+//   merge    over the CTA, then over the cluster through DSMEM in rank order,
+//            so every CTA holds the same row state;
+//   write    grad = e * exp(m - M) * f32(1/(1 + T)) * scale (the label column
+//            less scale) range by range; as soon as a range is written the
+//            bulk copy of the next row's chunk into it starts.
 __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, int cols) {
     extern __shared__ __align__(128) unsigned char smem[];
     StagedHeader &h = *reinterpret_cast<StagedHeader *>(smem);
@@ -179,66 +184,66 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
     const int c0 = static_cast<int>(rank) * cols;
     const int n = max(0, min(a.vocab, c0 + cols) - c0);
     const float scale = a.scale;
+    const int W = ((cols + 9) / 4 + kChunks - 1) / kChunks;  // vectors per range (covers any off)
+    const int64_t G = cluster_count_x();
+
+    // the bulk copy of chunk c (the body of range c) of `row`
+    auto issue = [&](int64_t row, int c, uint64_t policy) {
+        const float *p = a.logits + row * a.stride + c0;
+        const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+        const int head = min(n, (4 - off) & 3);
+        const int nvec = (n - head) >> 2;
+        const int qa = (off + head) >> 2;
+        const int q0 = max(qa, c * W), q1 = min(qa + nvec, (c + 1) * W);
+        const uint32_t bytes = q1 > q0 ? static_cast<uint32_t>(q1 - q0) * 16u : 0u;
+        mbar_arrive_expect_tx(&h.bar[c], bytes);
+        if (bytes) bulk_copy_g2s(buf4 + q0, p - off + 4 * q0, bytes, &h.bar[c], policy);
+    };
 
     uint64_t policy = 0;
     if (tid == 0) {
         for (int c = 0; c < kChunks; ++c) mbar_init(&h.bar[c], 1);
         fence_mbar_init();
         policy = l2_policy_evict_first();
+        if (static_cast<int64_t>(cluster_id_x()) < a.rows)
+            for (int c = 0; c < kChunks; ++c) issue(cluster_id_x(), c, policy);
     }
     __syncthreads();
 
     bool failed = false;
     bool pending = false;
     uint32_t parity = 0;
-    for (int64_t row = cluster_id_x(); row < a.rows; row += cluster_count_x(), parity ^= 1u) {
+    for (int64_t row = cluster_id_x(); row < a.rows; row += G, parity ^= 1u) {
         const float *p = a.logits + row * a.stride + c0;
         const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
         const int head = min(n, (4 - off) & 3);
         const int nvec = (n - head) >> 2;       // whole body vectors
         const int qa = (off + head) >> 2;       // first body vector (0 or 1)
         const int nq = (off + n + 3) >> 2;      // vectors covering the slice
-        const int vpc = (nvec + kChunks - 1) / kChunks;
         const int jbase = c0 - off;             // column of float 0 of buf
+        const bool more = row + G < a.rows;
 
-        // 1. bulk copies of the body
-        if (tid == 0) {
-            fence_proxy_async_smem();
-            for (int c = 0; c < kChunks; ++c) {
-                const int v0 = min(nvec, c * vpc), v1 = min(nvec, v0 + vpc);
-                const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
-                mbar_arrive_expect_tx(&h.bar[c], bytes);
-                if (bytes) bulk_copy_g2s(buf4 + qa + v0, p - off + 4 * (qa + v0), bytes, &h.bar[c], policy);
-            }
-        }
-        // 2. the partial end vectors (at most two) are loaded by the threads
-        //    that own them, lanes outside the slice being -inf; the label
-        const int qe0 = qa == 1 ? 0 : -1;                      // leading partial vector
-        const int qe1 = qa + nvec < nq ? qa + nvec : -1;       // trailing partial vector
+        // the partial end vectors (at most two), loaded by their owners
+        const int qe0 = qa == 1 ? 0 : -1;
+        const int qe1 = qa + nvec < nq ? qa + nvec : -1;
+        auto owner = [&](int q) { return (q - (q / W) * W) % T; };
         float4 edge0 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), edge1 = edge0;
-        if (qe0 >= 0 && qe0 % T == tid) edge0 = load_edge(p, off, n, qe0);
-        if (qe1 >= 0 && qe1 % T == tid) edge1 = load_edge(p, off, n, qe1);
+        if (qe0 >= 0 && owner(qe0) == tid) edge0 = load_edge(p, off, n, qe0);
+        if (qe1 >= 0 && owner(qe1) == tid) edge1 = load_edge(p, off, n, qe1);
         const int64_t label = a.labels[row];
         const bool lab_ok = label_valid(label, a.vocab);
         const int lab_local = (lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
         const int lab_f = lab_local >= 0 ? off + lab_local : -1;  // float index of the label
         const int lab_q = lab_f >> 2;
 
-        // 3. sweep 1: max and its first vector
+        // sweep 1: max and its first vector
         float m = -INFINITY;
         int qm = -1;
-        {
-            int ready = qa, c = 0;
-            for (int q = tid; q < nq; q += T) {
-                if (q >= qa && q < qa + nvec) {
-                    while (q >= ready) {
-                        if (!failed) failed = !mbar_wait_bounded(&h.bar[c], parity);
-                        ready += vpc;
-                        ++c;
-                    }
-                } else {
-                    buf4[q] = q == qe0 ? edge0 : edge1;
-                }
+        for (int c = 0; c < kChunks; ++c) {
+            const int qend = min(nq, (c + 1) * W);
+            if (c * W + tid < qend && !failed) failed = !mbar_wait_bounded(&h.bar[c], parity);
+            for (int q = c * W + tid; q < qend; q += T) {
+                if (q == qe0 || q == qe1) buf4[q] = q == qe0 ? edge0 : edge1;
                 const float mv = max4(buf4[q]);
                 if (mv > m) {
                     m = mv;
@@ -246,24 +251,26 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                 }
             }
         }
-        // x[label]: read by the thread that owns its vector, before it masks
-        // anything below (only that thread writes that vector)
-        if (lab_q >= 0 && lab_q % T == tid) h.bc[2] = buf[lab_f];
+        // x[label]: read by the thread that owns its vector, before it
+        // overwrites anything below (only that thread touches that vector)
+        if (lab_q >= 0 && owner(lab_q) == tid) h.bc[2] = buf[lab_f];
 
-        // 4. sweep 2: e = exp(x - m) over this thread's vectors, kept in shared
-        //    memory for the write; t sums all of them but the first element
-        //    holding m (masked to -inf for the sweep, then given e = 1).
+        // sweep 2: e = exp(x - m) in place; t sums all but the first element
+        // holding m (masked to -inf for the sweep, then given e = 1)
         RowState st;
         if (m != -INFINITY) {
             const float4 vm = buf4[qm];
             const int lm = vm.x == m ? 0 : vm.y == m ? 1 : vm.z == m ? 2 : 3;
             buf[4 * qm + lm] = -INFINITY;
             float t = 0.0f;
-            for (int q = tid; q < nq; q += T) {
-                const float4 v = buf4[q];
-                const float4 e = make_float4(exp_le0(v.x - m), exp_le0(v.y - m), exp_le0(v.z - m), exp_le0(v.w - m));
-                t += (e.x + e.y) + (e.z + e.w);
-                buf4[q] = e;
+            for (int c = 0; c < kChunks; ++c) {
+                const int qend = min(nq, (c + 1) * W);
+                for (int q = c * W + tid; q < qend; q += T) {
+                    const float4 v = buf4[q];
+                    const float4 e = make_float4(exp_le0(v.x - m), exp_le0(v.y - m), exp_le0(v.z - m), exp_le0(v.w - m));
+                    t += (e.x + e.y) + (e.z + e.w);
+                    buf4[q] = e;
+                }
             }
             buf[4 * qm + lm] = 1.0f;
             st = RowState{m, t, jbase + 4 * qm + lm};
@@ -271,18 +278,21 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
             // no value above -inf among this thread's columns: the exact
             // update; e is 0 for -inf and NaN for NaN
             st = empty_state();
-            for (int q = tid; q < nq; q += T) {
-                for (int l = 0; l < 4; ++l) {
-                    const int i = 4 * q + l;
-                    const float x = buf[i];
-                    if (i >= off && i - off < n) push<true>(st, x, jbase + i);
-                    buf[i] = x != x ? x : 0.0f;
+            for (int c = 0; c < kChunks; ++c) {
+                const int qend = min(nq, (c + 1) * W);
+                for (int q = c * W + tid; q < qend; q += T) {
+                    for (int l = 0; l < 4; ++l) {
+                        const int i = 4 * q + l;
+                        const float x = buf[i];
+                        if (i >= off && i - off < n) push<true>(st, x, jbase + i);
+                        buf[i] = x != x ? x : 0.0f;
+                    }
                 }
             }
         }
         st = block_reduce_w0<true>(st, h.red);
 
-        // 5. exchange over the cluster
+        // exchange over the cluster
         if (pending) cluster_wait();
         if (tid == 0) {
             h.xchg = Xchg{st.m, st.t, st.idx, lab_local >= 0 ? h.bc[2] : 0.0f};
@@ -292,8 +302,8 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         cluster_wait();
         if (tid < 32) {
             float xl;
-            const uint32_t owner = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
-            const RowState g = cluster_merge_w0<true>(&h.xchg, C, owner, &xl);
+            const uint32_t own = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
+            const RowState g = cluster_merge_w0<true>(&h.xchg, C, own, &xl);
             if (tid == 0) {
                 const bool bad = !isfinite(g.m) || isnan(g.t);
                 h.bc[0] = g.m;
@@ -310,32 +320,42 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         cluster_arrive();
         pending = true;
 
-        // 6. the gradient, from shared memory to HBM:
-        //    softmax = e * exp(m - M) * r, grad = softmax * scale (- scale at the label)
+        // the gradient, range by range; each freed range takes the next
+        // row's chunk
         const float M = h.bc[0], rcp = h.bc[1];
         const float shift = (m != -INFINITY && M != m) ? exp_le0(m - M) : 1.0f;
         const float sr = shift * rcp;
-        const float c = sr * scale;
+        const float cm = sr * scale;
         float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;  // column c0
-        const int goff = static_cast<int>((reinterpret_cast<uintptr_t>(gp) >> 2) & 3);
-        const bool vec_store = goff == off;
-        for (int q = tid; q < nq; q += T) {
-            const float4 e = buf4[q];
-            const float4 g = make_float4(e.x * c, e.y * c, e.z * c, e.w * c);
-            if (vec_store && static_cast<unsigned>(q - qa) < static_cast<unsigned>(nvec)) {
-                __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
-            } else {
-                const int i = 4 * q - off;  // column - c0 of lane 0
-                if (i >= 0 && i < n) __stcs(gp + i, g.x);
-                if (i + 1 >= 0 && i + 1 < n) __stcs(gp + i + 1, g.y);
-                if (i + 2 >= 0 && i + 2 < n) __stcs(gp + i + 2, g.z);
-                if (i + 3 >= 0 && i + 3 < n) __stcs(gp + i + 3, g.w);
+        const bool vec_store = ((reinterpret_cast<uintptr_t>(gp) >> 2) & 3) == static_cast<uintptr_t>(off);
+        for (int c = 0; c < kChunks; ++c) {
+            const int qend = min(nq, (c + 1) * W);
+            for (int q = c * W + tid; q < qend; q += T) {
+                const float4 e = buf4[q];
+                const float4 g = make_float4(e.x * cm, e.y * cm, e.z * cm, e.w * cm);
+                if (vec_store && static_cast<unsigned>(q - qa) < static_cast<unsigned>(nvec)) {
+                    __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
+                } else {
+                    const int i = 4 * q - off;  // column - c0 of lane 0
+                    if (i >= 0 && i < n) __stcs(gp + i, g.x);
+                    if (i + 1 >= 0 && i + 1 < n) __stcs(gp + i + 1, g.y);
+                    if (i + 2 >= 0 && i + 2 < n) __stcs(gp + i + 2, g.z);
+                    if (i + 3 >= 0 && i + 3 < n) __stcs(gp + i + 3, g.w);
+                }
+            }
+            // the label column: its owner stored e * c there above; this
+            // later store by the same thread replaces it
+            if (lab_q >= c * W && lab_q < qend && owner(lab_q) == tid)
+                __stcs(gp + lab_local, (buf[lab_f] * sr - 1.0f) * scale);
+            if (more) {
+                __syncthreads();  // range c is free
+                if (tid == 0) {
+                    fence_proxy_async_smem();
+                    issue(row + G, c, policy);
+                }
             }
         }
-        // the label column: its owner stored e * c there above; this later
-        // store by the same thread replaces it
-        if (lab_q >= 0 && lab_q % T == tid) __stcs(gp + lab_local, (buf[lab_f] * sr - 1.0f) * scale);
-        __syncthreads();  // buf is free for the next row's copies
+        __syncthreads();  // edge vectors and bc are rewritten for the next row
     }
     if (pending) cluster_wait();
     if (__syncthreads_or(failed) && tid == 0) {
@@ -407,6 +427,343 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
 }
 
 // ---------------------------------------------------------------------------
+// k_grad_ring: fused loss + gradient (+ token), persistent, on a ring of bulk
+// copies.
+//
+// One CTA per SM: 8 consumer warps and 1 producer warp. A cluster of C CTAs
+// shares each row (CTA `rank` owns columns [rank * cols, rank * cols + cols));
+// cluster `cid` of G takes rows cid, cid + G, ... The producer keeps a ring of
+// kSlots chunks (16 KB: 4 vectors per consumer thread) in shared memory full
+// with bulk copies, in the order the consumers take them:
+//   P1(row 0), then for k = 0, 1, ...: P1(row k+1), P2(row k).
+// A consumer warp frees a slot by arriving on its "empty" mbarrier; nothing
+// synchronises the whole CTA per chunk.
+// P1 streams the row slice from HBM into each thread's online state (max,
+// first index, exp-sum), block by block. The CTA's state is then pushed to
+// every CTA of the cluster (st.async into their shared memory, completing
+// bytes on their mbarrier): no cluster barrier per row. P2 streams the slice
+// again -- from L2, as only one slice per SM has been read in between -- and
+// writes the gradient. Doing P1 of the next row before P2 of this one hides
+// the exchange. Four exchange slots: a peer can run at most three row states
+// ahead of a CTA that has not yet read a slot.
+namespace ring {
+
+constexpr int kConsumers = kRingThreads - 32;  // 8 warps
+constexpr int kWarps = kConsumers / 32;
+constexpr int kRingUnroll = 4;
+constexpr int kVpc = kConsumers * kRingUnroll;  // 16-byte vectors per chunk
+constexpr int kSlots = kRingSlots;
+constexpr int kXSlots = 4;
+
+struct alignas(16) Header {
+    Xchg xchg[kXSlots][kMaxCluster];  // row states pushed by the cluster's CTAs
+    uint64_t full[kSlots];
+    uint64_t empty[kSlots];
+    uint64_t xbar[kXSlots];
+    RowState red[kWarps];
+    float bc[2][2];  // per row parity: M, f32(1/sum)
+    float xl;        // x[label], found in this CTA's slice during P1
+};
+static_assert(sizeof(Header) <= kRingHeaderBytes, "ring header too large");
+static_assert(kRingHeaderBytes % 128 == 0, "ring data must stay 128-byte aligned");
+static_assert(kRingSmemBytes == kRingHeaderBytes + kSlots * kVpc * 16, "ring size");
+
+// A CTA's slice of one row: p -> column c0; `head` scalar columns up to the
+// first 16-byte boundary, `nvec` whole vectors, then `tail` scalar columns.
+struct Geo {
+    const float *p;
+    int head, nvec, tail, nch;
+};
+
+__device__ __forceinline__ Geo geo(const Args &a, int64_t row, int c0, int n) {
+    Geo g;
+    g.p = a.logits + row * a.stride + c0;
+    const int off = static_cast<int>((reinterpret_cast<uintptr_t>(g.p) >> 2) & 3);
+    g.head = min(n, (4 - off) & 3);
+    g.nvec = (n - g.head) >> 2;
+    g.tail = n - g.head - 4 * g.nvec;
+    g.nch = (g.nvec + kVpc - 1) / kVpc;
+    return g;
+}
+
+__device__ __forceinline__ float lane_of(float4 v, int l) {
+    return l == 0 ? v.x : l == 1 ? v.y : l == 2 ? v.z : v.w;
+}
+
+// barrier among the consumer warps only
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+}  // namespace ring
+
+__global__ void __launch_bounds__(kRingThreads, 1) k_grad_ring(Args a, int cols) {
+    using namespace ring;
+    extern __shared__ __align__(128) unsigned char smem[];
+    Header &h = *reinterpret_cast<Header *>(smem);
+    float4 *ringv = reinterpret_cast<float4 *>(smem + kRingHeaderBytes);
+    const uint32_t rank = cluster_rank(), C = cluster_size();
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int c0 = static_cast<int>(rank) * cols;
+    const int n = max(0, min(a.vocab, c0 + cols) - c0);
+    const int64_t cid = cluster_id_x(), G = cluster_count_x();
+    const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;  // rows of this cluster
+    const float scale = a.scale;
+    bool failed = false;
+
+    if (tid == 0) {
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&h.full[i], 1);
+            mbar_init(&h.empty[i], kWarps);
+        }
+        for (int i = 0; i < kXSlots; ++i) mbar_init(&h.xbar[i], 1);
+        fence_mbar_init();
+        // each exchange slot expects C row states for its first row
+        for (int i = 0; i < kXSlots; ++i)
+            if (i < K) mbar_arrive_expect_tx(&h.xbar[i], 16u * C);
+    }
+    __syncthreads();
+    cluster_arrive();  // every CTA's barriers exist before a peer pushes to them
+    cluster_wait();
+
+    if (warp == kWarps) {
+        // ---------------- producer warp (lane 0 issues) ----------------
+        if (lane == 0) {
+            const uint64_t pol_keep = l2_policy_evict_last();
+            const uint64_t pol_stream = l2_policy_evict_first();
+            uint32_t issued = 0;
+            // segment 0: P1(0); 2k+1: P1(k+1); 2k+2: P2(k)
+            for (int64_t seg = 0; seg <= 2 * K; ++seg) {
+                const bool p1 = seg == 0 || (seg & 1);
+                const int64_t rk = seg == 0 ? 0 : (p1 ? (seg + 1) / 2 : (seg - 2) / 2);
+                if (rk >= K) continue;
+                const Geo g = geo(a, cid + rk * G, c0, n);
+                for (int c = 0; c < g.nch; ++c, ++issued) {
+                    const int slot = static_cast<int>(issued % kSlots);
+                    if (issued >= static_cast<uint32_t>(kSlots) && !failed)
+                        failed = !mbar_wait_bounded(&h.empty[slot], ((issued / kSlots) - 1) & 1u);
+                    const int v0 = c * kVpc;
+                    const uint32_t bytes = static_cast<uint32_t>(min(kVpc, g.nvec - v0)) * 16u;
+                    mbar_arrive_expect_tx(&h.full[slot], bytes);
+                    bulk_copy_g2s(ringv + slot * kVpc, g.p + g.head + 4 * v0, bytes, &h.full[slot],
+                                  p1 ? pol_keep : pol_stream);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- consumer warps ----------------
+        uint32_t s = 0;  // chunks consumed
+        auto wait_chunk = [&]() -> const float4 * {
+            const int slot = static_cast<int>(s % kSlots);
+            if (!failed) failed = !mbar_wait_bounded(&h.full[slot], (s / kSlots) & 1u);
+            return ringv + slot * kVpc;
+        };
+        auto release_chunk = [&]() {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&h.empty[s % kSlots]);
+            ++s;
+        };
+        auto label_at = [&](int64_t row, const Geo &g, int *ll, int *lab_v, bool *lab_ok) {
+            const int64_t label = a.labels[row];
+            *lab_ok = label_valid(label, a.vocab);
+            *ll = (*lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
+            *lab_v = (*ll >= g.head && *ll < g.head + 4 * g.nvec) ? (*ll - g.head) >> 2 : -1;
+        };
+
+        // P1: this CTA's state of row k
+        auto pass1 = [&](int64_t k) -> RowState {
+            const int64_t row = cid + k * G;
+            const Geo g = geo(a, row, c0, n);
+            int ll, lab_v;
+            bool lab_ok;
+            label_at(row, g, &ll, &lab_v, &lab_ok);
+            const int jv = c0 + g.head;
+            float hx[3], tx[3];  // the unaligned end columns, loaded early by thread 0
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                hx[i] = (tid == 0 && i < g.head) ? g.p[i] : 0.0f;
+                tx[i] = (tid == 0 && i < g.tail) ? g.p[g.head + 4 * g.nvec + i] : 0.0f;
+            }
+            RowState st = empty_state();
+            for (int c = 0; c < g.nch; ++c) {
+                const float4 *buf = wait_chunk();
+                float4 x[kRingUnroll];
+                int j[kRingUnroll];
+                bool ok[kRingUnroll];
+#pragma unroll
+                for (int u = 0; u < kRingUnroll; ++u) {
+                    const int v = c * kVpc + tid + kConsumers * u;
+                    ok[u] = v < g.nvec;
+                    x[u] = ok[u] ? buf[v - c * kVpc] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    j[u] = jv + 4 * v;
+                    if (v == lab_v) h.xl = lane_of(x[u], (ll - g.head) & 3);
+                }
+                release_chunk();
+                push_block<kRingUnroll>(st, x, j, ok);
+            }
+            if (tid == 0) {
+                RowState se = empty_state();
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    if (i < g.head) {
+                        push<true>(se, hx[i], c0 + i);
+                        if (ll == i) h.xl = hx[i];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    if (i < g.tail) {
+                        const int col = g.head + 4 * g.nvec + i;
+                        push<true>(se, tx[i], c0 + col);
+                        if (ll == col) h.xl = tx[i];
+                    }
+                }
+                st = merge<true>(st, se);
+            }
+            return st;
+        };
+
+        // push this CTA's state of row k into exchange slot k % 4 of every CTA
+        auto publish = [&](int64_t k, RowState st) {
+            st = warp_reduce<true>(st);
+            if (lane == 0) h.red[warp] = st;
+            consumers_sync();
+            if (warp == 0) {
+                RowState r = lane < kWarps ? h.red[lane] : empty_state();
+                r = warp_reduce<true>(r);
+                if (lane == 0) {
+                    const int64_t label = a.labels[cid + k * G];
+                    const bool mine = label_valid(label, a.vocab) && label >= c0 && label < c0 + n;
+                    const int xs = static_cast<int>(k & (kXSlots - 1));
+                    const float4 v = make_float4(r.m, r.t, __int_as_float(r.idx), mine ? h.xl : 0.0f);
+                    for (uint32_t q = 0; q < C; ++q)
+                        st_async_peer(peer_smem(&h.xchg[xs][rank], q), v, peer_smem(&h.xbar[xs], q));
+                }
+            }
+        };
+
+        // merge the cluster's states of row k; write its loss and token
+        auto finish = [&](int64_t k) {
+            const int xs = static_cast<int>(k & (kXSlots - 1));
+            if (warp == 0) {
+                if (!failed) failed = !mbar_wait_bounded(&h.xbar[xs], static_cast<uint32_t>(k >> 2) & 1u);
+                const int64_t row = cid + k * G;
+                const int64_t label = a.labels[row];
+                const bool lab_ok = label_valid(label, a.vocab);
+                const uint32_t owner = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
+                RowState q = empty_state();
+                float v = 0.0f;
+                if (lane < static_cast<int>(C)) {
+                    const Xchg x = h.xchg[xs][lane];
+                    q = RowState{x.m, x.t, x.idx};
+                    v = x.xl;
+                }
+                const float xl = __shfl_sync(kFullMask, v, static_cast<int>(owner));
+                const RowState g = warp_reduce<true>(q);
+                if (lane == 0) {
+                    const bool bad = !isfinite(g.m) || isnan(g.t);
+                    h.bc[k & 1][0] = g.m;
+                    h.bc[k & 1][1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);  // f32(1/sum)
+                    if (rank == 0) {
+                        if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
+                        if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+                        if (a.top) a.top[row] = row_token(g);
+                    }
+                    if (k + kXSlots < K) mbar_arrive_expect_tx(&h.xbar[xs], 16u * C);  // re-arm for row k + 4
+                }
+            }
+            consumers_sync();
+        };
+
+        // P2: the gradient of row k
+        auto pass2 = [&](int64_t k) {
+            const int64_t row = cid + k * G;
+            const Geo g = geo(a, row, c0, n);
+            int ll, lab_v;
+            bool lab_ok;
+            label_at(row, g, &ll, &lab_v, &lab_ok);
+            const float M = h.bc[k & 1][0], rcp = h.bc[k & 1][1];
+            const float cm = rcp * scale;
+            float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;
+            float *gb = gp + g.head;
+            const bool vec = (reinterpret_cast<uintptr_t>(gb) & 15) == 0;
+            float hx[3], tx[3];
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                hx[i] = (tid == 0 && i < g.head) ? g.p[i] : 0.0f;
+                tx[i] = (tid == 0 && i < g.tail) ? g.p[g.head + 4 * g.nvec + i] : 0.0f;
+            }
+            for (int c = 0; c < g.nch; ++c) {
+                const float4 *buf = wait_chunk();
+                float4 x[kRingUnroll];
+#pragma unroll
+                for (int u = 0; u < kRingUnroll; ++u) {
+                    const int v = c * kVpc + tid + kConsumers * u;
+                    x[u] = v < g.nvec ? buf[v - c * kVpc] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                release_chunk();
+#pragma unroll
+                for (int u = 0; u < kRingUnroll; ++u) {
+                    const int v = c * kVpc + tid + kConsumers * u;
+                    if (v < g.nvec) {
+                        const float4 e = make_float4(exp_le0(x[u].x - M), exp_le0(x[u].y - M),
+                                                     exp_le0(x[u].z - M), exp_le0(x[u].w - M));
+                        float4 o = make_float4(e.x * cm, e.y * cm, e.z * cm, e.w * cm);
+                        if (v == lab_v) {
+                            const int l = (ll - g.head) & 3;
+                            const float gl = (lane_of(e, l) * rcp - 1.0f) * scale;
+                            o.x = l == 0 ? gl : o.x;
+                            o.y = l == 1 ? gl : o.y;
+                            o.z = l == 2 ? gl : o.z;
+                            o.w = l == 3 ? gl : o.w;
+                        }
+                        if (vec) {
+                            __stcs(reinterpret_cast<float4 *>(gb) + v, o);
+                        } else {
+                            __stcs(gb + 4 * v, o.x);
+                            __stcs(gb + 4 * v + 1, o.y);
+                            __stcs(gb + 4 * v + 2, o.z);
+                            __stcs(gb + 4 * v + 3, o.w);
+                        }
+                    }
+                }
+            }
+            if (tid == 0) {
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    if (i < g.head) {
+                        const float e = exp_le0(hx[i] - M);
+                        __stcs(gp + i, ll == i ? (e * rcp - 1.0f) * scale : e * cm);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    if (i < g.tail) {
+                        const int col = g.head + 4 * g.nvec + i;
+                        const float e = exp_le0(tx[i] - M);
+                        __stcs(gp + col, ll == col ? (e * rcp - 1.0f) * scale : e * cm);
+                    }
+                }
+            }
+        };
+
+        if (K > 0) publish(0, pass1(0));
+        for (int64_t k = 0; k < K; ++k) {
+            if (k + 1 < K) publish(k + 1, pass1(k + 1));
+            finish(k);
+            pass2(k);
+        }
+    }
+    cluster_arrive();  // no CTA leaves while a peer may still push to it
+    cluster_wait();
+    if (__syncthreads_or(failed) && tid == 0) atomicAdd(&g_status[1], 1ull);
+}
+
+// ---------------------------------------------------------------------------
 // k_mean: one CTA. Thread k sums rows k, k + T, ... in f64; a butterfly over
 // each warp, then over the warps' sums. Fixed shape: same bits every run.
 __global__ void __launch_bounds__(1024) k_mean(const float *__restrict__ loss, int64_t rows,
@@ -444,9 +801,11 @@ cudaError_t launch_clustered(const void *fn, const Plan &p, void **args, cudaStr
 }
 
 const void *kernel_of(const Plan &p, Op op) {
-    if (op == kOpGrad)
+    if (op == kOpGrad) {
+        if (p.path == kPathRing) return reinterpret_cast<const void *>(&k_grad_ring);
         return p.path == kPathStaged ? reinterpret_cast<const void *>(&k_grad_staged)
                                      : reinterpret_cast<const void *>(&k_grad_stream);
+    }
     if (op == kOpRows) return reinterpret_cast<const void *>(&k_rows_stream<true>);
     return reinterpret_cast<const void *>(&k_rows_stream<false>);
 }
@@ -457,13 +816,17 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
     const void *fns[] = {reinterpret_cast<const void *>(&k_rows_stream<true>),
                          reinterpret_cast<const void *>(&k_rows_stream<false>),
                          reinterpret_cast<const void *>(&k_grad_staged),
-                         reinterpret_cast<const void *>(&k_grad_stream)};
+                         reinterpret_cast<const void *>(&k_grad_stream),
+                         reinterpret_cast<const void *>(&k_grad_ring)};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    return cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_grad_staged),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_grad_staged),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_grad_ring),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
 }
 
 cudaError_t max_active_clusters(const Plan &p, Op op, int *n) {
@@ -493,6 +856,13 @@ cudaError_t launch_grad_staged(const Plan &p, const Args &a, cudaStream_t s) {
     int cols = p.cols;
     void *args[] = {&aa, &cols};
     return launch_clustered(reinterpret_cast<const void *>(&k_grad_staged), p, args, s);
+}
+
+cudaError_t launch_grad_ring(const Plan &p, const Args &a, cudaStream_t s) {
+    Args aa = a;
+    int cols = p.cols;
+    void *args[] = {&aa, &cols};
+    return launch_clustered(reinterpret_cast<const void *>(&k_grad_ring), p, args, s);
 }
 
 cudaError_t launch_grad_stream(const Plan &p, const Args &a, cudaStream_t s) {
