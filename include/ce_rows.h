@@ -148,11 +148,12 @@ CE_API int ce_device_error_reset(ce_stream_t stream);
 
 /*
  * Launch-plan override, for tests and tuning: forces the kernel family
- * (path: 0 automatic, 1 shared-memory-staged, 2 streaming from global,
- * 3 persistent ring of bulk copies -- 256 threads only), the
+ * (path: 0 automatic, 1 shared-memory-staged (persistent), 2 streaming from
+ * global, 3 persistent ring of bulk copies, 4 shared-memory-staged with one
+ * row per cluster), the
  * CTAs that share one row (cluster: 0 automatic, else 1..16) and the
- * threads of a CTA (threads: 0 automatic, else 128, 256 or 512; the
- * streaming kernels take at most 256, the staged one at most 512).
+ * threads of a CTA (threads: 0 automatic, else 128 or 256; 512 is
+ * rejected by every kernel family).
  * Applies to every later call in the process. A forced plan that cannot
  * launch on this device makes the calls return CE_EINVAL.
  */

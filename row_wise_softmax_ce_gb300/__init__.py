@@ -37,7 +37,7 @@ LIB_PATH = os.path.join(_PKG, "libcerows.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "ce_rows.h")
 
 CE_OK, CE_EINVAL, CE_EALIGN, CE_ECUDA, CE_EDEVICE = 0, -1, -2, -3, -4
-PATH_AUTO, PATH_STAGED, PATH_STREAM, PATH_RING = 0, 1, 2, 3
+PATH_AUTO, PATH_STAGED, PATH_STREAM, PATH_RING, PATH_STAGED_PER_ROW = 0, 1, 2, 3, 4
 OP_ROWS, OP_GRAD, OP_ARGMAX = 0, 1, 2
 
 _lock = threading.Lock()

@@ -100,7 +100,8 @@ void plan_stream(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
 
 // Launch shape of the staged fused kernel: the fewest CTAs per row whose
 // slices are at most kStagedTargetCols columns (at most 16 CTAs).
-bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster) {
+bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster,
+                 bool per_row = false) {
     p.path = kPathStaged;
     p.threads = threads ? threads : 256;
     if (p.threads > kStagedMaxThreads) return false;
@@ -118,7 +119,14 @@ bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
         return false;
     }
     if (active < 1) return false;
-    p.clusters = std::min<int64_t>(rows, active);  // persistent: every cluster resident at once
+    // persistent (every cluster resident at once, looping over rows), or one
+    // row per cluster with the hardware scheduling clusters as others finish.
+    // Measured on GB300: persistent is ahead when each cluster loops over
+    // many rows (8192 x 128256: 160 rows per cluster, 93% vs 89% of copy
+    // bandwidth), one row per cluster when it would loop over few (4096 x
+    // 32000: 18 rows per cluster, 93% vs 89%).
+    if (!per_row && cluster == 0 && rows < 32 * static_cast<int64_t>(active)) per_row = true;
+    p.clusters = per_row ? std::min<int64_t>(rows, kMaxClusters) : std::min<int64_t>(rows, active);
     return true;
 }
 
@@ -154,8 +162,9 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
         if (f.path == kPathRing) {
             if (f.threads && f.threads != kRingThreads) return CE_EINVAL;
             if (!plan_ring(p, rows, vocab, f.cluster)) return CE_EINVAL;
-        } else if (f.path == kPathStaged) {
-            if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster)) return CE_EINVAL;
+        } else if (f.path == kPathStaged || f.path == kPathStagedPerRow) {
+            if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster, f.path == kPathStagedPerRow))
+                return CE_EINVAL;
         } else if (f.path == kPathStream) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
         } else if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster)) {
@@ -313,7 +322,7 @@ int ce_device_error_reset(ce_stream_t stream) {
 }
 
 int ce_debug_force(int path, int cluster, int threads) {
-    if (path < 0 || path > 3 || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
+    if (path < 0 || path > 4 || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
     if (threads != 0 && threads != 128 && threads != 256 && threads != 512) return CE_EINVAL;
     std::lock_guard<std::mutex> lock(g_mu);
     g_force.path = path;

@@ -227,10 +227,27 @@ __device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), 
 // Rounding the product d * log2(e) adds a relative error of about
 // |d| * 2^-24 to the result -- at most 2.2e-8 absolute, since |d| * exp(d)
 // <= 1/e for d <= 0.
-__device__ __forceinline__ float exp_le0(float d) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d * 1.4426950408889634f));
-    return y;
+__device__ __forceinline__ float ex2_ftz(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+__device__ __forceinline__ float exp_le0(float d) { return ex2_ftz(d * 1.4426950408889634f); }
+
+// exp(v - m) lane by lane (every lane <= m), the subtraction and the scaling
+// by log2(e) done two lanes per instruction (Blackwell paired f32 ops).
+__device__ __forceinline__ float4 exp4_sub(float4 v, float m) {
+    const float2 nm = make_float2(-m, -m), l2e = make_float2(1.4426950408889634f, 1.4426950408889634f);
+    const float2 a = __fmul2_rn(__fadd2_rn(make_float2(v.x, v.y), nm), l2e);
+    const float2 b = __fmul2_rn(__fadd2_rn(make_float2(v.z, v.w), nm), l2e);
+    return make_float4(ex2_ftz(a.x), ex2_ftz(a.y), ex2_ftz(b.x), ex2_ftz(b.y));
+}
+
+__device__ __forceinline__ float4 mul4(float4 v, float c) {
+    const float2 cc = make_float2(c, c);
+    const float2 a = __fmul2_rn(make_float2(v.x, v.y), cc);
+    const float2 b = __fmul2_rn(make_float2(v.z, v.w), cc);
+    return make_float4(a.x, a.y, b.x, b.y);
 }
 
 // Push four consecutive columns j..j+3. Common case: none of them exceeds the

@@ -7,14 +7,14 @@
 
 namespace cerows {
 
-enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2, kPathRing = 3 };
+enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2, kPathRing = 3, kPathStagedPerRow = 4 };
 enum Op : int { kOpRows = 0, kOpGrad = 1, kOpArgmax = 2 };
 
 // Per-CTA shared bytes the staged kernel reserves before its row buffer.
-constexpr int kStagedHeaderBytes = 1024;
+constexpr int kStagedHeaderBytes = 2048;
 constexpr int kMaxCluster = 16;
 // Largest CTA each kernel family is compiled for (its __launch_bounds__).
-constexpr int kStagedMaxThreads = 512;
+constexpr int kStagedMaxThreads = 256;
 constexpr int kStreamMaxThreads = 256;
 // The persistent ring kernel: CTA size (8 consumer warps + 1 producer warp),
 // chunks in flight (16 KB each), and its dynamic shared memory (header + ring).

@@ -42,8 +42,9 @@ constexpr int kChunks = 4;  // bulk copies (and mbarriers) per staged slice
 constexpr int kUnroll = 4;  // 16-byte loads in flight per thread (streaming)
 
 struct alignas(16) StagedHeader {
+    Xchg xchg[2][kMaxCluster];  // row states pushed by the cluster's CTAs, by row parity
     uint64_t bar[kChunks];
-    Xchg xchg;
+    uint64_t xbar[2];
     RowState red[32];
     float bc[4];
 };
@@ -169,8 +170,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
 //            holding it;
 //   sweep 2  e = exp(x - m), kept in place; t = their sum but for the first
 //            element holding m;
-//   merge    over the CTA, then over the cluster through DSMEM in rank order,
-//            so every CTA holds the same row state;
+//   merge    over the CTA; then each CTA pushes its state into every CTA of
+//            the cluster (st.async, completing bytes on their mbarrier) and
+//            merges the C states in rank order, so every CTA holds the same
+//            row state -- no cluster barrier per row;
 //   write    grad = e * exp(m - M) * f32(1/(1 + T)) * scale (the label column
 //            less scale) range by range; as soon as a range is written the
 //            bulk copy of the next row's chunk into it starts.
@@ -200,20 +203,28 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         if (bytes) bulk_copy_g2s(buf4 + q0, p - off + 4 * q0, bytes, &h.bar[c], policy);
     };
 
+    const int64_t cid = cluster_id_x();
+    const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;  // rows of this cluster
     uint64_t policy = 0;
     if (tid == 0) {
         for (int c = 0; c < kChunks; ++c) mbar_init(&h.bar[c], 1);
+        for (int i = 0; i < 2; ++i) mbar_init(&h.xbar[i], 1);
         fence_mbar_init();
+        // each exchange slot expects C row states for its first row
+        for (int i = 0; i < 2; ++i)
+            if (i < K) mbar_arrive_expect_tx(&h.xbar[i], 16u * C);
         policy = l2_policy_evict_first();
-        if (static_cast<int64_t>(cluster_id_x()) < a.rows)
-            for (int c = 0; c < kChunks; ++c) issue(cluster_id_x(), c, policy);
+        if (K > 0)
+            for (int c = 0; c < kChunks; ++c) issue(cid, c, policy);
     }
     __syncthreads();
+    cluster_arrive();  // every CTA's barriers exist before a peer pushes to them
+    cluster_wait();
 
     bool failed = false;
-    bool pending = false;
     uint32_t parity = 0;
-    for (int64_t row = cluster_id_x(); row < a.rows; row += G, parity ^= 1u) {
+    int64_t k = 0;  // this cluster's row count so far
+    for (int64_t row = cid; row < a.rows; row += G, parity ^= 1u, ++k) {
         const float *p = a.logits + row * a.stride + c0;
         const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
         const int head = min(n, (4 - off) & 3);
@@ -262,16 +273,16 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
             const float4 vm = buf4[qm];
             const int lm = vm.x == m ? 0 : vm.y == m ? 1 : vm.z == m ? 2 : 3;
             buf[4 * qm + lm] = -INFINITY;
-            float t = 0.0f;
+            float2 acc = make_float2(0.0f, 0.0f);
             for (int c = 0; c < kChunks; ++c) {
                 const int qend = min(nq, (c + 1) * W);
                 for (int q = c * W + tid; q < qend; q += T) {
-                    const float4 v = buf4[q];
-                    const float4 e = make_float4(exp_le0(v.x - m), exp_le0(v.y - m), exp_le0(v.z - m), exp_le0(v.w - m));
-                    t += (e.x + e.y) + (e.z + e.w);
+                    const float4 e = exp4_sub(buf4[q], m);
+                    acc = __fadd2_rn(acc, __fadd2_rn(make_float2(e.x, e.y), make_float2(e.z, e.w)));
                     buf4[q] = e;
                 }
             }
+            const float t = acc.x + acc.y;
             buf[4 * qm + lm] = 1.0f;
             st = RowState{m, t, jbase + 4 * qm + lm};
         } else {
@@ -292,18 +303,27 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         }
         st = block_reduce_w0<true>(st, h.red);
 
-        // exchange over the cluster
-        if (pending) cluster_wait();
+        // exchange over the cluster: push this CTA's state into slot k % 2 of
+        // every CTA (st.async, completing bytes on their slot barrier); warp 0
+        // waits for the C states of its own slot and merges them in rank order
+        const int xs = static_cast<int>(k & 1);
         if (tid == 0) {
-            h.xchg = Xchg{st.m, st.t, st.idx, lab_local >= 0 ? h.bc[2] : 0.0f};
-            fence_cluster();
+            const float4 v = make_float4(st.m, st.t, __int_as_float(st.idx), lab_local >= 0 ? h.bc[2] : 0.0f);
+            for (uint32_t r = 0; r < C; ++r)
+                st_async_peer(peer_smem(&h.xchg[xs][rank], r), v, peer_smem(&h.xbar[xs], r));
         }
-        cluster_arrive();
-        cluster_wait();
         if (tid < 32) {
-            float xl;
+            if (!failed) failed = !mbar_wait_bounded(&h.xbar[xs], static_cast<uint32_t>(k >> 1) & 1u);
             const uint32_t own = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
-            const RowState g = cluster_merge_w0<true>(&h.xchg, C, own, &xl);
+            RowState q = empty_state();
+            float v = 0.0f;
+            if (tid < static_cast<int>(C)) {
+                const Xchg x = h.xchg[xs][tid];
+                q = RowState{x.m, x.t, x.idx};
+                v = x.xl;
+            }
+            const float xl = __shfl_sync(kFullMask, v, static_cast<int>(own));
+            const RowState g = warp_reduce<true>(q);
             if (tid == 0) {
                 const bool bad = !isfinite(g.m) || isnan(g.t);
                 h.bc[0] = g.m;
@@ -313,12 +333,10 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                     if (!lab_ok) atomicAdd(&g_status[0], 1ull);
                     if (a.top) a.top[row] = row_token(g);
                 }
+                if (k + 2 < K) mbar_arrive_expect_tx(&h.xbar[xs], 16u * C);  // re-arm for row k + 2
             }
-            fence_cluster();
         }
         __syncthreads();
-        cluster_arrive();
-        pending = true;
 
         // the gradient, range by range; each freed range takes the next
         // row's chunk
@@ -331,8 +349,7 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         for (int c = 0; c < kChunks; ++c) {
             const int qend = min(nq, (c + 1) * W);
             for (int q = c * W + tid; q < qend; q += T) {
-                const float4 e = buf4[q];
-                const float4 g = make_float4(e.x * cm, e.y * cm, e.z * cm, e.w * cm);
+                const float4 g = mul4(buf4[q], cm);
                 if (vec_store && static_cast<unsigned>(q - qa) < static_cast<unsigned>(nvec)) {
                     __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
                 } else {
@@ -357,7 +374,8 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         }
         __syncthreads();  // edge vectors and bc are rewritten for the next row
     }
-    if (pending) cluster_wait();
+    cluster_arrive();  // no CTA leaves while a peer may still push to it
+    cluster_wait();
     if (__syncthreads_or(failed) && tid == 0) {
         atomicAdd(&g_status[1], 1ull);
         // give copies still in flight a last bounded chance to land
