@@ -101,7 +101,7 @@ void plan_stream(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
 // Launch shape of the staged fused kernel: the fewest CTAs per row whose
 // slices are at most kStagedTargetCols columns (at most 16 CTAs).
 bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster,
-                 bool per_row = false) {
+                 bool per_row, bool auto_form) {
     p.path = kPathStaged;
     p.threads = threads ? threads : 256;
     if (p.threads > kStagedMaxThreads) return false;
@@ -125,7 +125,7 @@ bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
     // many rows (8192 x 128256: 160 rows per cluster, 93% vs 89% of copy
     // bandwidth), one row per cluster when it would loop over few (4096 x
     // 32000: 18 rows per cluster, 93% vs 89%).
-    if (!per_row && cluster == 0 && rows < 32 * static_cast<int64_t>(active)) per_row = true;
+    if (auto_form) per_row = rows < 32 * static_cast<int64_t>(active);
     p.clusters = per_row ? std::min<int64_t>(rows, kMaxClusters) : std::min<int64_t>(rows, active);
     return true;
 }
@@ -163,11 +163,11 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
             if (f.threads && f.threads != kRingThreads) return CE_EINVAL;
             if (!plan_ring(p, rows, vocab, f.cluster)) return CE_EINVAL;
         } else if (f.path == kPathStaged || f.path == kPathStagedPerRow) {
-            if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster, f.path == kPathStagedPerRow))
+            if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster, f.path == kPathStagedPerRow, false))
                 return CE_EINVAL;
         } else if (f.path == kPathStream) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
-        } else if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster)) {
+        } else if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster, false, true)) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
         }
     } else {
