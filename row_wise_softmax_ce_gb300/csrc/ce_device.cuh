@@ -398,4 +398,56 @@ __device__ __forceinline__ RowState cluster_merge_w0(const Xchg *x, uint32_t C, 
     return warp_reduce<kStats>(s);
 }
 
+// Row-state exchange among the C CTAs of a cluster by pushes: for row k of
+// the cluster, thread 0 of every CTA stores its state into slot k % 2 of
+// every CTA (st.async, completing 16 bytes on that CTA's slot barrier), and
+// warp 0 of every CTA waits for the C states of its own slot and merges them
+// in rank order -- the same bits in every CTA, and no cluster barrier per
+// row. Two slots suffice: a CTA pushes row k + 2 only after it has merged
+// row k + 1, which needs this CTA's push of row k + 1, which this CTA makes
+// only after it has read slot k % 2 for row k. The cluster must pass one
+// cluster barrier between push_xchg_init and the first push (so that every
+// slot barrier exists), and one before any CTA exits.
+struct PushXchg {
+    Xchg slot[2][16];
+    uint64_t bar[2];
+};
+
+// thread 0; K = rows this cluster will exchange
+__device__ __forceinline__ void push_xchg_init(PushXchg &x, int64_t K, uint32_t C) {
+    for (int i = 0; i < 2; ++i) mbar_init(&x.bar[i], 1);
+    fence_mbar_init();
+    for (int i = 0; i < 2; ++i)
+        if (i < K) mbar_arrive_expect_tx(&x.bar[i], 16u * C);
+}
+
+// thread 0
+__device__ __forceinline__ void push_xchg_publish(PushXchg &x, int64_t k, uint32_t rank, uint32_t C,
+                                                  const RowState &st, float xl) {
+    const int xs = static_cast<int>(k & 1);
+    const float4 v = make_float4(st.m, st.t, __int_as_float(st.idx), xl);
+    for (uint32_t r = 0; r < C; ++r) st_async_peer(peer_smem(&x.slot[xs][rank], r), v, peer_smem(&x.bar[xs], r));
+}
+
+// all of warp 0: the merged row state (every lane); *xl = the x[label]
+// published by CTA `owner`. Re-arms the slot for row k + 2.
+template <bool kStats>
+__device__ __forceinline__ RowState push_xchg_merge(PushXchg &x, int64_t k, int64_t K, uint32_t C, uint32_t owner,
+                                                    float *xl, bool *failed) {
+    const int lane = threadIdx.x & 31;
+    const int xs = static_cast<int>(k & 1);
+    if (!*failed) *failed = !mbar_wait_bounded(&x.bar[xs], static_cast<uint32_t>(k >> 1) & 1u);
+    RowState q = empty_state();
+    float v = 0.0f;
+    if (lane < static_cast<int>(C)) {
+        const Xchg e = x.slot[xs][lane];
+        q = RowState{e.m, e.t, e.idx};
+        v = e.xl;
+    }
+    *xl = __shfl_sync(kFullMask, v, static_cast<int>(owner));
+    const RowState g = warp_reduce<kStats>(q);
+    if (lane == 0 && k + 2 < K) mbar_arrive_expect_tx(&x.bar[xs], 16u * C);
+    return g;
+}
+
 }  // namespace cerows

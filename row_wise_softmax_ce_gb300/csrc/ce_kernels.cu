@@ -42,9 +42,8 @@ constexpr int kChunks = 4;  // bulk copies (and mbarriers) per staged slice
 constexpr int kUnroll = 4;  // 16-byte loads in flight per thread (streaming)
 
 struct alignas(16) StagedHeader {
-    Xchg xchg[2][kMaxCluster];  // row states pushed by the cluster's CTAs, by row parity
+    PushXchg xg;  // row states pushed by the cluster's CTAs
     uint64_t bar[kChunks];
-    uint64_t xbar[2];
     RowState red[32];
     float bc[4];
 };
@@ -105,17 +104,25 @@ __device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int
 
 // ---------------------------------------------------------------------------
 // k_rows_stream: row loss (kStats) and/or argmax token; one read per logit.
+// The C CTAs of a cluster split a row; their states meet by pushes.
 template <bool kStats>
 __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, int cols) {
     __shared__ RowState red[32];
-    __shared__ Xchg xchg;
+    __shared__ PushXchg xg;
     const uint32_t rank = cluster_rank(), C = cluster_size();
     const int tid = threadIdx.x;
     const int c0 = static_cast<int>(rank) * cols;
     const int n = max(0, min(a.vocab, c0 + cols) - c0);
-    bool pending = false;  // a cluster arrive without its wait
-    for (int64_t row = cluster_id_x(); row < a.rows; row += cluster_count_x()) {
-        // the label and x[label], fetched early by the CTA that writes the loss
+    const int64_t cid = cluster_id_x(), G = cluster_count_x();
+    const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;  // rows of this cluster
+    if (tid == 0) push_xchg_init(xg, K, C);
+    __syncthreads();
+    cluster_arrive();  // every CTA's slot barriers exist before a peer pushes to them
+    cluster_wait();
+    bool failed = false;
+    int64_t k = 0;
+    for (int64_t row = cid; row < a.rows; row += G, ++k) {
+        // the label and x[label], fetched early by the thread that writes the loss
         int64_t label = 0;
         float xl = 0.0f;
         bool lab_ok = true;
@@ -127,29 +134,23 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
         RowState st = empty_state();
         if (n > 0) st = scan_global<kStats>(a.logits + row * a.stride + c0, c0, n);
         st = block_reduce_w0<kStats>(st, red);
-        if (pending) cluster_wait();  // peers finished reading the previous row's xchg
-        if (tid == 0) {
-            xchg = Xchg{st.m, st.t, st.idx, 0.0f};
-            fence_cluster();
-        }
-        cluster_arrive();
-        cluster_wait();
-        if (rank == 0 && tid < 32) {
+        if (tid == 0) push_xchg_publish(xg, k, rank, C, st, 0.0f);
+        if (tid < 32) {
             float unused;
-            const RowState g = cluster_merge_w0<kStats>(&xchg, C, 0u, &unused);
-            if (tid == 0) {
+            const RowState g = push_xchg_merge<kStats>(xg, k, K, C, 0u, &unused, &failed);
+            if (rank == 0 && tid == 0) {
                 if (kStats && a.loss) {
                     a.loss[row] = row_loss(g, xl, lab_ok);
                     if (!lab_ok) atomicAdd(&g_status[0], 1ull);
                 }
                 if (a.top) a.top[row] = row_token(g);
             }
-            fence_cluster();
         }
-        cluster_arrive();
-        pending = true;
+        __syncthreads();  // red is rewritten for the next row
     }
-    if (pending) cluster_wait();  // no CTA leaves while a peer may still read its xchg
+    cluster_arrive();  // no CTA leaves while a peer may still push to it
+    cluster_wait();
+    if (__syncthreads_or(failed) && tid == 0) atomicAdd(&g_status[1], 1ull);
 }
 
 // ---------------------------------------------------------------------------
@@ -208,11 +209,8 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
     uint64_t policy = 0;
     if (tid == 0) {
         for (int c = 0; c < kChunks; ++c) mbar_init(&h.bar[c], 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&h.xbar[i], 1);
         fence_mbar_init();
-        // each exchange slot expects C row states for its first row
-        for (int i = 0; i < 2; ++i)
-            if (i < K) mbar_arrive_expect_tx(&h.xbar[i], 16u * C);
+        push_xchg_init(h.xg, K, C);
         policy = l2_policy_evict_first();
         if (K > 0)
             for (int c = 0; c < kChunks; ++c) issue(cid, c, policy);
@@ -306,24 +304,11 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         // exchange over the cluster: push this CTA's state into slot k % 2 of
         // every CTA (st.async, completing bytes on their slot barrier); warp 0
         // waits for the C states of its own slot and merges them in rank order
-        const int xs = static_cast<int>(k & 1);
-        if (tid == 0) {
-            const float4 v = make_float4(st.m, st.t, __int_as_float(st.idx), lab_local >= 0 ? h.bc[2] : 0.0f);
-            for (uint32_t r = 0; r < C; ++r)
-                st_async_peer(peer_smem(&h.xchg[xs][rank], r), v, peer_smem(&h.xbar[xs], r));
-        }
+        if (tid == 0) push_xchg_publish(h.xg, k, rank, C, st, lab_local >= 0 ? h.bc[2] : 0.0f);
         if (tid < 32) {
-            if (!failed) failed = !mbar_wait_bounded(&h.xbar[xs], static_cast<uint32_t>(k >> 1) & 1u);
+            float xl;
             const uint32_t own = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
-            RowState q = empty_state();
-            float v = 0.0f;
-            if (tid < static_cast<int>(C)) {
-                const Xchg x = h.xchg[xs][tid];
-                q = RowState{x.m, x.t, x.idx};
-                v = x.xl;
-            }
-            const float xl = __shfl_sync(kFullMask, v, static_cast<int>(own));
-            const RowState g = warp_reduce<true>(q);
+            const RowState g = push_xchg_merge<true>(h.xg, k, K, C, own, &xl, &failed);
             if (tid == 0) {
                 const bool bad = !isfinite(g.m) || isnan(g.t);
                 h.bc[0] = g.m;
@@ -333,7 +318,6 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                     if (!lab_ok) atomicAdd(&g_status[0], 1ull);
                     if (a.top) a.top[row] = row_token(g);
                 }
-                if (k + 2 < K) mbar_arrive_expect_tx(&h.xbar[xs], 16u * C);  // re-arm for row k + 2
             }
         }
         __syncthreads();
@@ -385,18 +369,26 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
 
 // ---------------------------------------------------------------------------
 // k_grad_stream: fused loss + gradient for rows too long to stage; the
-// cluster's CTAs read their slices twice (state, then gradient).
+// cluster's CTAs read their slices twice (state, then gradient) and meet by
+// pushes.
 __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, int cols) {
     __shared__ RowState red[32];
-    __shared__ Xchg xchg;
+    __shared__ PushXchg xg;
     __shared__ float bc[2];
     const uint32_t rank = cluster_rank(), C = cluster_size();
     const int tid = threadIdx.x, T = blockDim.x;
     const int c0 = static_cast<int>(rank) * cols;
     const int n = max(0, min(a.vocab, c0 + cols) - c0);
     const float scale = a.scale;
-    bool pending = false;
-    for (int64_t row = cluster_id_x(); row < a.rows; row += cluster_count_x()) {
+    const int64_t cid = cluster_id_x(), G = cluster_count_x();
+    const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;  // rows of this cluster
+    if (tid == 0) push_xchg_init(xg, K, C);
+    __syncthreads();
+    cluster_arrive();  // every CTA's slot barriers exist before a peer pushes to them
+    cluster_wait();
+    bool failed = false;
+    int64_t k = 0;
+    for (int64_t row = cid; row < a.rows; row += G, ++k) {
         const float *p = a.logits + row * a.stride + c0;
         const int64_t label = a.labels[row];
         const bool lab_ok = label_valid(label, a.vocab);
@@ -406,17 +398,11 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
         RowState st = empty_state();
         if (n > 0) st = scan_global<true>(p, c0, n);
         st = block_reduce_w0<true>(st, red);
-        if (pending) cluster_wait();
-        if (tid == 0) {
-            xchg = Xchg{st.m, st.t, st.idx, xl_own};
-            fence_cluster();
-        }
-        cluster_arrive();
-        cluster_wait();
+        if (tid == 0) push_xchg_publish(xg, k, rank, C, st, xl_own);
         if (tid < 32) {
             float xl;
             const uint32_t owner = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
-            const RowState g = cluster_merge_w0<true>(&xchg, C, owner, &xl);
+            const RowState g = push_xchg_merge<true>(xg, k, K, C, owner, &xl, &failed);
             if (tid == 0) {
                 const bool bad = !isfinite(g.m) || isnan(g.t);
                 bc[0] = g.m;
@@ -427,21 +413,20 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
                     if (a.top) a.top[row] = row_token(g);
                 }
             }
-            fence_cluster();
         }
         __syncthreads();
-        cluster_arrive();
-        pending = true;
         const float M = bc[0], rcp = bc[1];
         float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;
         // coherent loads: with grad == logits this thread writes what it read
-        for (int k = tid; k < n; k += T) {
-            const float pr = exp_le0(__ldcs(p + k) - M) * rcp;
-            __stcs(gp + k, (k == lab_local ? pr - 1.0f : pr) * scale);
+        for (int kk = tid; kk < n; kk += T) {
+            const float pr = exp_le0(__ldcs(p + kk) - M) * rcp;
+            __stcs(gp + kk, (kk == lab_local ? pr - 1.0f : pr) * scale);
         }
-        __syncthreads();  // bc is rewritten for the next row
+        __syncthreads();  // bc and red are rewritten for the next row
     }
-    if (pending) cluster_wait();
+    cluster_arrive();  // no CTA leaves while a peer may still push to it
+    cluster_wait();
+    if (__syncthreads_or(failed) && tid == 0) atomicAdd(&g_status[1], 1ull);
 }
 
 // ---------------------------------------------------------------------------
