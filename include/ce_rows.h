@@ -121,10 +121,22 @@ CE_API int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t str
  * no non-NaN entry gives 0 -- written as f32 (exact, since vocab <= 2^24)
  * into top[rows]. Only the direct form (rows at logits + i * stride); the
  * page's indirect form over head blocks is not provided.
- *   logits: [rows, stride] f32, read only.   top: [rows] f32, written.
+ *   logits:    [rows, stride] f32, read only.   top: [rows] f32, written.
+ *   workspace: NULL, or workspace_bytes of device memory (8-byte aligned,
+ *              any contents, owned by the caller, not read by the host) that
+ *              lets few long rows be split evenly over the whole GPU: a call
+ *              given at least argmax_workspace_bytes(rows, vocab, stride)
+ *              bytes may use it; with less it runs without. Two calls that
+ *              may run at once on the GPU need separate workspaces.
  */
 CE_API int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top,
-                ce_stream_t stream);
+                       void *workspace, int64_t workspace_bytes, ce_stream_t stream);
+
+/*
+ * Bytes of workspace argmax_rows can use for this shape on the current
+ * device (0: none would be used). Host only; launches nothing.
+ */
+CE_API int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t stride);
 
 /* Human-readable text of a status code (a static string). */
 CE_API const char *ce_status_string(int status);
@@ -150,7 +162,8 @@ CE_API int ce_device_error_reset(ce_stream_t stream);
  * Launch-plan override, for tests and tuning: forces the kernel family
  * (path: 0 automatic, 1 shared-memory-staged (persistent), 2 streaming from
  * global, 3 persistent ring of bulk copies, 4 shared-memory-staged with one
- * row per cluster), the
+ * row per cluster, 5 argmax split evenly over the GPU -- needs a workspace),
+ * the
  * CTAs that share one row (cluster: 0 automatic, else 1..16) and the
  * threads of a CTA (threads: 0 automatic, else 128 or 256; 512 is
  * rejected by every kernel family).

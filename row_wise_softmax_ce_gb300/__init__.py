@@ -37,7 +37,7 @@ LIB_PATH = os.path.join(_PKG, "libcerows.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "ce_rows.h")
 
 CE_OK, CE_EINVAL, CE_EALIGN, CE_ECUDA, CE_EDEVICE = 0, -1, -2, -3, -4
-PATH_AUTO, PATH_STAGED, PATH_STREAM, PATH_RING, PATH_STAGED_PER_ROW = 0, 1, 2, 3, 4
+PATH_AUTO, PATH_STAGED, PATH_STREAM, PATH_RING, PATH_STAGED_PER_ROW, PATH_FLAT = 0, 1, 2, 3, 4, 5
 OP_ROWS, OP_GRAD, OP_ARGMAX = 0, 1, 2
 
 _lock = threading.Lock()
@@ -62,7 +62,8 @@ def _bind(lib):
         "ce_mean": [vp, i64, vp, vp],
         "ce_loss": [vp, i64, i64, i64, vp, vp, vp, vp],
         "ce_grad": [vp, i64, i64, i64, vp, ctypes.c_double, vp, vp, vp, vp],
-        "argmax_rows": [vp, i64, i64, i64, vp, vp],
+        "argmax_rows": [vp, i64, i64, i64, vp, vp, i64, vp],
+        "argmax_workspace_bytes": [i64, i64, i64],
         "ce_version": [],
         "ce_last_cuda_error": [],
         "ce_device_error_count": [vp, ctypes.POINTER(ctypes.c_uint64)],
@@ -73,7 +74,7 @@ def _bind(lib):
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
-        fn.restype = i32
+        fn.restype = i64 if name == "argmax_workspace_bytes" else i32
     lib.ce_status_string.argtypes = [i32]
     lib.ce_status_string.restype = ctypes.c_char_p
     return lib
@@ -212,13 +213,21 @@ def ce_grad(logits: torch.Tensor, labels: torch.Tensor, scale: float, vocab: int
 
 def argmax_rows(logits: torch.Tensor, vocab: int | None = None,
                 out: torch.Tensor | None = None) -> torch.Tensor:
-    """argmaxInto: each row's token as f32 ``[rows]`` (first of equals; NaN never wins)."""
+    """argmaxInto: each row's token as f32 ``[rows]`` (first of equals; NaN never wins).
+
+    When the library can split few long rows over the whole GPU it asks for a
+    small workspace, allocated here from PyTorch's allocator on the current
+    stream."""
     rows, vocab, stride = _logits_view(logits, vocab)
     dev = logits.device
     out = _out(out, (rows,), torch.float32, dev, "out")
     with torch.cuda.device(dev):
-        _check("argmax_rows", lib().argmax_rows(logits.data_ptr(), rows, vocab, stride, out.data_ptr(),
-                                                 _stream(dev)))
+        L = lib()
+        ws_bytes = int(L.argmax_workspace_bytes(rows, vocab, stride)) if rows > 0 else 0
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes > 0 else None
+        _check("argmax_rows", L.argmax_rows(logits.data_ptr(), rows, vocab, stride, out.data_ptr(),
+                                            ws.data_ptr() if ws is not None else None, ws_bytes,
+                                            _stream(dev)))
     return out
 
 

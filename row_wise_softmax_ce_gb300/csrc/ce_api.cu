@@ -152,6 +152,18 @@ bool plan_ring(Plan &p, int64_t rows, int64_t vocab, int cluster) {
     return true;
 }
 
+// The even split of few long rows (argmax only): two 512-thread CTAs per SM,
+// each CTA at least 8192 elements. Chosen automatically when there are fewer
+// rows than 2 CTAs per SM and rows of at least 16384 columns (measured on
+// GB300, 256 x 151936: the cluster split's best is 32.8 us).
+bool flat_applies(int64_t rows, int64_t vocab, const DeviceInfo &dev, bool forced) {
+    const int64_t ctas = 2 * static_cast<int64_t>(dev.sms);
+    if (rows * vocab < ctas * 8192) return false;
+    return forced || (rows < ctas && vocab >= 16384);
+}
+
+int64_t flat_workspace_bytes(int64_t rows, const DeviceInfo &dev) { return 8 * (2 * static_cast<int64_t>(dev.sms) + rows); }
+
 int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *out) {
     Force f;
     {
@@ -171,6 +183,14 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
         } else if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster, false, true)) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
         }
+    } else if (op == kOpArgmax && (f.path == kPathFlat || (f.path == kPathAuto && f.cluster == 0 && f.threads == 0)) &&
+               flat_applies(rows, vocab, dev, f.path == kPathFlat)) {
+        p.path = kPathFlat;
+        p.cluster = 1;
+        p.threads = 512;
+        p.smem = 0;
+        p.cols = static_cast<int>(vocab);
+        p.clusters = 2 * static_cast<int64_t>(dev.sms);
     } else {
         plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
     }
@@ -272,12 +292,22 @@ int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t stride, co
     return cuda_status(launch_grad_stream(p, a, stream));
 }
 
-int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top,
-                ce_stream_t stream) {
+int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t stride) {
+    if (rows < 1 || vocab < 1 || vocab > kMaxVocab || stride < vocab) return 0;
+    DeviceInfo dev;
+    if (current_device(&dev)) return 0;
+    Plan p;
+    if (make_plan(kOpArgmax, rows, vocab, dev, &p) || p.path != kPathFlat) return 0;
+    return flat_workspace_bytes(rows, dev);
+}
+
+int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top, void *workspace,
+                int64_t workspace_bytes, ce_stream_t stream) {
     int st = check_logits(logits, rows, vocab, stride);
     if (st) return st;
     if (rows > 0 && top == nullptr) return CE_EINVAL;
-    if (misaligned(top, 4)) return CE_EALIGN;
+    if (workspace_bytes < 0 || (workspace_bytes > 0 && workspace == nullptr)) return CE_EINVAL;
+    if (misaligned(top, 4) || misaligned(workspace, 8)) return CE_EALIGN;
     if (rows == 0) return CE_OK;
     DeviceInfo dev;
     if ((st = current_device(&dev))) return st;
@@ -285,6 +315,17 @@ int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride
     if ((st = make_plan(kOpArgmax, rows, vocab, dev, &p))) return st;
     Args a = make_args(logits, rows, vocab, stride, nullptr);
     a.top = top;
+    if (p.path == kPathFlat) {
+        if (workspace != nullptr && workspace_bytes >= flat_workspace_bytes(rows, dev))
+            return cuda_status(launch_argmax_flat(a, static_cast<int>(p.clusters), workspace, stream));
+        Force f;
+        {
+            std::lock_guard<std::mutex> lock(g_mu);
+            f = g_force;
+        }
+        if (f.path == kPathFlat) return CE_EINVAL;  // forced, but no room for it
+        plan_stream(p, rows, vocab, dev, 0, 0);
+    }
     return cuda_status(launch_rows_stream(p, a, false, stream));
 }
 
@@ -323,7 +364,7 @@ int ce_device_error_reset(ce_stream_t stream) {
 }
 
 int ce_debug_force(int path, int cluster, int threads) {
-    if (path < 0 || path > 4 || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
+    if (path < 0 || path > 5 || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
     if (threads != 0 && threads != 128 && threads != 256 && threads != 512) return CE_EINVAL;
     std::lock_guard<std::mutex> lock(g_mu);
     g_force.path = path;

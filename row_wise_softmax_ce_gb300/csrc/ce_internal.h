@@ -7,7 +7,7 @@
 
 namespace cerows {
 
-enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2, kPathRing = 3, kPathStagedPerRow = 4 };
+enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2, kPathRing = 3, kPathStagedPerRow = 4, kPathFlat = 5 };
 enum Op : int { kOpRows = 0, kOpGrad = 1, kOpArgmax = 2 };
 
 // Per-CTA shared bytes the staged kernel reserves before its row buffer.
@@ -60,6 +60,8 @@ cudaError_t launch_grad_staged(const Plan &p, const Args &a, cudaStream_t s);
 cudaError_t launch_grad_stream(const Plan &p, const Args &a, cudaStream_t s);
 cudaError_t launch_grad_ring(const Plan &p, const Args &a, cudaStream_t s);
 cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s);
+// argmax of few long rows split evenly over `ctas` CTAs; ws: 8 * (ctas + rows) bytes
+cudaError_t launch_argmax_flat(const Args &a, int ctas, void *ws, cudaStream_t s);
 
 cudaError_t read_status(unsigned long long out[2], cudaStream_t s);
 cudaError_t reset_status(cudaStream_t s);

@@ -78,7 +78,7 @@ __device__ __forceinline__ float row_token(const RowState &g) {
 // Push the columns [j0, j0 + n) of one row, read from global memory at p
 // (p -> column j0): a scalar head up to the first 16-byte boundary, 16-byte
 // vectors, a scalar tail. Each thread sees its columns in increasing order.
-template <bool kStats>
+template <bool kStats, int kU = kUnroll>
 __device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int j0, int n) {
     RowState st = empty_state();
     const int tid = threadIdx.x, T = blockDim.x;
@@ -90,12 +90,12 @@ __device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int
     const int jv = j0 + head;
     if (tid < head) push<kStats>(st, ld_stream_f1(p + tid), j0 + tid);
     int k = tid;
-    for (; k + (kUnroll - 1) * T < nvec; k += kUnroll * T) {
-        float4 v[kUnroll];
+    for (; k + (kU - 1) * T < nvec; k += kU * T) {
+        float4 v[kU];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) v[u] = ld_stream_f4(pv + k + u * T);
+        for (int u = 0; u < kU; ++u) v[u] = ld_stream_f4(pv + k + u * T);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) push_vec<kStats>(st, v[u], jv + 4 * (k + u * T));
+        for (int u = 0; u < kU; ++u) push_vec<kStats>(st, v[u], jv + 4 * (k + u * T));
     }
     for (; k < nvec; k += T) push_vec<kStats>(st, ld_stream_f4(pv + k), jv + 4 * k);
     if (tid < tail) push<kStats>(st, ld_stream_f1(p + head + 4 * nvec + tid), jv + 4 * nvec + tid);
@@ -767,6 +767,64 @@ __global__ void __launch_bounds__(kRingThreads, 1) k_grad_ring(Args a, int cols)
 }
 
 // ---------------------------------------------------------------------------
+// Argmax of few long rows, split evenly over one wave of CTAs.
+//
+// k_argmax_flat: CTA j of P scans elements [e_j, e_{j+1}), e_j = floor(j E / P),
+// of the rows read as one sequence of E = rows * vocab elements (the first
+// vocab columns of each row). For each row r its range meets, it writes the
+// segment's key into ws[j + r] -- segments are ordered by position, so before
+// (j, r) come exactly j range starts and r row starts: the index is unique.
+// A key orders (value, then lower column first): the value's bits made
+// monotone above, the column's complement below; a segment without a
+// non-NaN value keys as value 0 (below -inf), column first.
+// k_argmax_combine: each row's token is the largest key among the CTAs that
+// met the row.
+constexpr int kFlatThreads = 512;
+constexpr int kFlatUnroll = 8;
+
+__device__ __forceinline__ uint64_t argmax_key(const RowState &st, int first_col) {
+    if (st.idx == kNoIndex) return 0xFFFFFFFFull - static_cast<uint32_t>(first_col);
+    const uint32_t u = __float_as_uint(st.m + 0.0f);  // -0 -> +0
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<uint64_t>(ord) << 32) | (0xFFFFFFFFull - static_cast<uint32_t>(st.idx));
+}
+
+__device__ __forceinline__ int64_t flat_split(int64_t E, int64_t P, int64_t j) { return (E * j) / P; }
+
+__global__ void __launch_bounds__(kFlatThreads, 2) k_argmax_flat(Args a, uint64_t *__restrict__ ws) {
+    __shared__ RowState red[32];
+    const int64_t E = a.rows * static_cast<int64_t>(a.vocab), P = gridDim.x, j = blockIdx.x;
+    const int64_t e0 = flat_split(E, P, j), e1 = flat_split(E, P, j + 1);
+    for (int64_t r = e0 / a.vocab; r < a.rows && r * a.vocab < e1; ++r) {
+        const int64_t ra = max(e0, r * a.vocab), rb = min(e1, (r + 1) * a.vocab);
+        const int ca = static_cast<int>(ra - r * a.vocab);
+        RowState st = scan_global<false, kFlatUnroll>(a.logits + r * a.stride + ca, ca, static_cast<int>(rb - ra));
+        st = block_reduce_w0<false>(st, red);
+        if (threadIdx.x == 0) ws[j + r] = argmax_key(st, ca);
+        __syncthreads();  // red is rewritten for the next segment
+    }
+}
+
+__global__ void k_argmax_combine(Args a, const uint64_t *__restrict__ ws, int P) {
+    const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (r >= a.rows) return;
+    const int64_t E = a.rows * static_cast<int64_t>(a.vocab);
+    // the CTA holding element x: the largest j with e_j <= x
+    auto cta_of = [&](int64_t x) {
+        int lo = 0, hi = P - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            if (flat_split(E, P, mid) <= x) lo = mid; else hi = mid - 1;
+        }
+        return lo;
+    };
+    const int jf = cta_of(r * a.vocab), jl = cta_of((r + 1) * a.vocab - 1);
+    uint64_t key = 0;
+    for (int jj = jf; jj <= jl; ++jj) key = max(key, ws[jj + r]);
+    a.top[r] = static_cast<float>(0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull));
+}
+
+// ---------------------------------------------------------------------------
 // k_mean: one CTA. Thread k sums rows k, k + T, ... in f64; a butterfly over
 // each warp, then over the warps' sums. Fixed shape: same bits every run.
 __global__ void __launch_bounds__(1024) k_mean(const float *__restrict__ loss, int64_t rows,
@@ -873,6 +931,16 @@ cudaError_t launch_grad_stream(const Plan &p, const Args &a, cudaStream_t s) {
     int cols = p.cols;
     void *args[] = {&aa, &cols};
     return launch_clustered(reinterpret_cast<const void *>(&k_grad_stream), p, args, s);
+}
+
+cudaError_t launch_argmax_flat(const Args &a, int ctas, void *ws, cudaStream_t s) {
+    k_argmax_flat<<<ctas, kFlatThreads, 0, s>>>(a, static_cast<uint64_t *>(ws));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int threads = 256;
+    const unsigned blocks = static_cast<unsigned>((a.rows + threads - 1) / threads);
+    k_argmax_combine<<<blocks, threads, 0, s>>>(a, static_cast<const uint64_t *>(ws), ctas);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s) {

@@ -17,7 +17,8 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = ce.declared_functions()
-    assert set(names) >= {"ce_rows", "ce_mean", "ce_loss", "ce_grad", "argmax_rows", "ce_status_string",
+    assert set(names) >= {"ce_rows", "ce_mean", "ce_loss", "ce_grad", "argmax_rows", "argmax_workspace_bytes",
+                          "ce_status_string",
                           "ce_version", "ce_last_cuda_error", "ce_device_error_count",
                           "ce_device_error_reset", "ce_debug_force", "ce_plan"}
     missing = [n for n in names if not hasattr(lib, n)]
@@ -51,21 +52,24 @@ V = ctypes.c_void_p
 def test_bad_sizes_rejected_before_launch(lib, args):
     logits, rows, vocab, stride = args
     assert lib.ce_rows(logits, rows, vocab, stride, V(512), V(1024), None) == ce.CE_EINVAL
-    assert lib.argmax_rows(logits, rows, vocab, stride, V(1024), None) == ce.CE_EINVAL
+    assert lib.argmax_rows(logits, rows, vocab, stride, V(1024), None, 0, None) == ce.CE_EINVAL
     assert lib.ce_grad(logits, rows, vocab, stride, V(512), 1.0, V(4096), None, None, None) == ce.CE_EINVAL
 
 
 def test_misaligned_pointers_rejected(lib):
     assert lib.ce_rows(V(258), 4, 10, 10, V(512), V(1024), None) == ce.CE_EALIGN
     assert lib.ce_rows(V(256), 4, 10, 10, V(516), V(1024), None) == ce.CE_EALIGN     # labels need 8 B
-    assert lib.argmax_rows(V(256), 4, 10, 10, V(1026), None) == ce.CE_EALIGN
+    assert lib.argmax_rows(V(256), 4, 10, 10, V(1026), None, 0, None) == ce.CE_EALIGN
+    assert lib.argmax_rows(V(256), 4, 10, 10, V(1024), V(2052), 64, None) == ce.CE_EALIGN   # workspace 8 B
     assert lib.ce_mean(V(256), 4, V(260), None) == ce.CE_EALIGN                       # double out
 
 
 def test_null_outputs_and_bad_scale_rejected(lib):
     assert lib.ce_rows(V(256), 4, 10, 10, None, V(1024), None) == ce.CE_EINVAL
     assert lib.ce_rows(V(256), 4, 10, 10, V(512), None, None) == ce.CE_EINVAL
-    assert lib.argmax_rows(V(256), 4, 10, 10, None, None) == ce.CE_EINVAL
+    assert lib.argmax_rows(V(256), 4, 10, 10, None, None, 0, None) == ce.CE_EINVAL
+    assert lib.argmax_rows(V(256), 4, 10, 10, V(1024), None, 64, None) == ce.CE_EINVAL    # bytes, no buffer
+    assert lib.argmax_rows(V(256), 4, 10, 10, V(1024), V(2048), -8, None) == ce.CE_EINVAL
     assert lib.ce_mean(V(256), 4, None, None) == ce.CE_EINVAL
     assert lib.ce_loss(V(256), 4, 10, 10, V(512), V(1024), None, None) == ce.CE_EINVAL
     for s in (float("nan"), float("inf")):
@@ -82,12 +86,13 @@ def test_grad_overlap_rules(lib):
 def test_zero_rows_is_a_no_op_without_device(lib):
     # nothing is launched, so no device is needed
     assert lib.ce_rows(None, 0, 10, 10, None, None, None) == ce.CE_OK
-    assert lib.argmax_rows(None, 0, 10, 10, None, None) == ce.CE_OK
+    assert lib.argmax_rows(None, 0, 10, 10, None, None, 0, None) == ce.CE_OK
+    assert lib.argmax_workspace_bytes(0, 10, 10) == 0
     assert lib.ce_grad(None, 0, 10, 10, None, 1.0, None, None, None, None) == ce.CE_OK
 
 
 def test_debug_force_validation(lib):
-    assert lib.ce_debug_force(5, 0, 0) == ce.CE_EINVAL
+    assert lib.ce_debug_force(6, 0, 0) == ce.CE_EINVAL
     assert lib.ce_debug_force(0, 17, 0) == ce.CE_EINVAL
     assert lib.ce_debug_force(0, 0, 1024) == ce.CE_EINVAL
     assert lib.ce_debug_force(0, 0, 96) == ce.CE_EINVAL

@@ -376,3 +376,47 @@ def test_scales_and_side_stream(orc):
             assert_grad(g / 1e3, g_ref / 1e3, "scale 1e3 (divided back)")
         else:
             assert_grad(g, g_ref, f"scale {sc}")
+
+
+@pytest.mark.parametrize("shape", [(256, 151936, 152064), (3, 1 << 20, 1 << 20), (300, 16384, 16384),
+                                   (17, 100003, 100007)], ids=str)
+def test_argmax_even_split(orc, shape):
+    """Few long rows split evenly over the GPU (a workspace given): exact ties
+    planted across the split points resolve to the lower column; NaN segments,
+    all-NaN and all -inf rows follow the argmax rule."""
+    rows, vocab, stride = shape
+    x, _ = W.random_logits(rows, vocab, stride=stride, sigma=1.0, seed=rows + vocab, pad_value=1e30)
+    P = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    E = rows * vocab
+    for j in range(1, P, 7):
+        r, c = divmod(E * j // P, vocab)
+        if c >= 1:
+            x[r, c - 1] = x[r, c] = 50.0 + j   # a tie straddling the split of CTAs j-1 and j
+    if rows >= 3:
+        x[1, : vocab // 2] = float("nan")      # a long NaN run, several whole CTA segments
+        x[2, :vocab] = float("nan")            # all NaN: token 0
+        x[rows - 1, :vocab] = -float("inf")    # all -inf: token 0
+    ce.debug_force(5, 0, 0)
+    try:
+        p = ce.plan(ce.OP_ARGMAX, rows, vocab, stride)
+        assert p["path"] == ce.PATH_FLAT, p
+        top = ce.argmax_rows(x.to(DEV), vocab=vocab)
+        torch.cuda.synchronize()
+    finally:
+        ce.debug_force(0, 0, 0)
+    assert_tokens(top, orc.argmax(x.numpy(), vocab, threads=THREADS), f"even split {shape}")
+
+
+def test_argmax_without_workspace_falls_back(orc):
+    """The C entry point without a workspace runs the cluster path: same tokens."""
+    rows, vocab = 256, 151936
+    x, _ = W.random_logits(rows, vocab, seed=77)
+    xd = x.to(DEV)
+    top = torch.empty(rows, device=DEV)
+    L = ce.lib()
+    assert L.argmax_workspace_bytes(rows, vocab, vocab) > 0
+    st = L.argmax_rows(xd.data_ptr(), rows, vocab, vocab, top.data_ptr(), None, 0,
+                       torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert_tokens(top, orc.argmax(x.numpy(), vocab, threads=THREADS), "no workspace")
