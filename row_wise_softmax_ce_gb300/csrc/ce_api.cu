@@ -153,13 +153,13 @@ bool plan_ring(Plan &p, int64_t rows, int64_t vocab, int cluster) {
 }
 
 // The even split of few long rows (argmax only): two 512-thread CTAs per SM,
-// each CTA at least 8192 elements. Chosen automatically when there are fewer
-// rows than 2 CTAs per SM and rows of at least 16384 columns (measured on
-// GB300, 256 x 151936: the cluster split's best is 32.8 us).
+// each CTA at least 8192 elements. Taken only when forced (path 5): measured
+// on GB300 it is not yet ahead of the cluster split (256 x 151936, L2
+// flushed: 42.0 us with its combine launch, against 32.8 us).
 bool flat_applies(int64_t rows, int64_t vocab, const DeviceInfo &dev, bool forced) {
     const int64_t ctas = 2 * static_cast<int64_t>(dev.sms);
     if (rows * vocab < ctas * 8192) return false;
-    return forced || (rows < ctas && vocab >= 16384);
+    return forced;
 }
 
 int64_t flat_workspace_bytes(int64_t rows, const DeviceInfo &dev) { return 8 * (2 * static_cast<int64_t>(dev.sms) + rows); }

@@ -379,7 +379,7 @@ def test_scales_and_side_stream(orc):
 
 
 @pytest.mark.parametrize("shape", [(256, 151936, 152064), (3, 1 << 20, 1 << 20), (300, 16384, 16384),
-                                   (17, 100003, 100007)], ids=str)
+                                   (17, 200003, 200007)], ids=str)
 def test_argmax_even_split(orc, shape):
     """Few long rows split evenly over the GPU (a workspace given): exact ties
     planted across the split points resolve to the lower column; NaN segments,
