@@ -407,16 +407,27 @@ def test_argmax_even_split(orc, shape):
     assert_tokens(top, orc.argmax(x.numpy(), vocab, threads=THREADS), f"even split {shape}")
 
 
-def test_argmax_without_workspace_falls_back(orc):
-    """The C entry point without a workspace runs the cluster path: same tokens."""
+def test_argmax_workspace_contract(orc):
+    """Automatic plan: argmax_rows needs no workspace (the cluster split) and
+    argmax_workspace_bytes says 0. Forced even split: the bytes are reported;
+    a call without them is refused before any launch."""
     rows, vocab = 256, 151936
     x, _ = W.random_logits(rows, vocab, seed=77)
     xd = x.to(DEV)
-    top = torch.empty(rows, device=DEV)
+    top = torch.full((rows,), -1.0, device=DEV)
     L = ce.lib()
-    assert L.argmax_workspace_bytes(rows, vocab, vocab) > 0
-    st = L.argmax_rows(xd.data_ptr(), rows, vocab, vocab, top.data_ptr(), None, 0,
-                       torch.cuda.current_stream().cuda_stream)
-    assert st == 0
+    stream = torch.cuda.current_stream().cuda_stream
+    assert L.argmax_workspace_bytes(rows, vocab, vocab) == 0
+    assert L.argmax_rows(xd.data_ptr(), rows, vocab, vocab, top.data_ptr(), None, 0, stream) == ce.CE_OK
     torch.cuda.synchronize()
     assert_tokens(top, orc.argmax(x.numpy(), vocab, threads=THREADS), "no workspace")
+    ce.debug_force(5, 0, 0)
+    try:
+        need = L.argmax_workspace_bytes(rows, vocab, vocab)
+        assert need == 8 * (2 * torch.cuda.get_device_properties(0).multi_processor_count + rows)
+        top.fill_(-1.0)
+        assert L.argmax_rows(xd.data_ptr(), rows, vocab, vocab, top.data_ptr(), None, 0, stream) == ce.CE_EINVAL
+        torch.cuda.synchronize()
+        assert (top == -1.0).all()
+    finally:
+        ce.debug_force(0, 0, 0)
