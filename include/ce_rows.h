@@ -62,6 +62,7 @@ enum ce_status {
     CE_EALIGN = -2,
     CE_ECUDA = -3,
     CE_EDEVICE = -4, /* no CUDA device, or not an sm_103 device */
+    CE_ERANGE = -5,  /* argmax_rows_noalloc: more rows than its fixed scratch holds */
 };
 
 /*
@@ -137,6 +138,34 @@ CE_API int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t
  * device (0: none would be used). Host only; launches nothing.
  */
 CE_API int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t stride);
+
+/*
+ * argmax_rows_noalloc -- the tokens of argmax_rows (same rule, same f32
+ * output) for callers that must not allocate device memory: code running
+ * inside another runtime that owns and pre-plans every byte of device memory
+ * (an inference server's memory planner, a plugin handed only its inputs
+ * and outputs), and latency-critical decode loops where a cudaMalloc -- which
+ * can synchronise the whole device -- is not acceptable. The pages have no
+ * counterpart: argmaxInto takes no workspace.
+ *
+ * It allocates nothing: its scratch is a fixed 64 KiB array in the library's
+ * own device memory (one 64-bit key per segment of the rows' even split over
+ * the GPU), held on every device that loads the library until the process
+ * exits. The caller still passes the logits and `top` as in argmax_rows.
+ *   - A call with rows + 2 * (SMs of the device) <= 8192 always fits (7888
+ *     rows on a 152-SM GB300); a call that does not fit returns CE_ERANGE
+ *     and launches nothing.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, no allocation); make that first call
+ *     before capturing any stream.
+ *   - Every call uses the same array and leaves its contents there. Nothing
+ *     in it needs to start at zero (each call reads only keys it wrote), but
+ *     two calls that run at the same time on the GPU -- on different streams,
+ *     or from different host threads -- race on it and may return wrong
+ *     tokens; order them on one stream.
+ */
+CE_API int argmax_rows_noalloc(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top,
+                               ce_stream_t stream);
 
 /* Human-readable text of a status code (a static string). */
 CE_API const char *ce_status_string(int status);

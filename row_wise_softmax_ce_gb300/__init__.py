@@ -36,7 +36,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libcerows.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "ce_rows.h")
 
-CE_OK, CE_EINVAL, CE_EALIGN, CE_ECUDA, CE_EDEVICE = 0, -1, -2, -3, -4
+CE_OK, CE_EINVAL, CE_EALIGN, CE_ECUDA, CE_EDEVICE, CE_ERANGE = 0, -1, -2, -3, -4, -5
 PATH_AUTO, PATH_STAGED, PATH_STREAM, PATH_RING, PATH_STAGED_PER_ROW, PATH_FLAT = 0, 1, 2, 3, 4, 5
 OP_ROWS, OP_GRAD, OP_ARGMAX = 0, 1, 2
 
@@ -64,6 +64,7 @@ def _bind(lib):
         "ce_grad": [vp, i64, i64, i64, vp, ctypes.c_double, vp, vp, vp, vp],
         "argmax_rows": [vp, i64, i64, i64, vp, vp, i64, vp],
         "argmax_workspace_bytes": [i64, i64, i64],
+        "argmax_rows_noalloc": [vp, i64, i64, i64, vp, vp],
         "ce_version": [],
         "ce_last_cuda_error": [],
         "ce_device_error_count": [vp, ctypes.POINTER(ctypes.c_uint64)],
@@ -228,6 +229,22 @@ def argmax_rows(logits: torch.Tensor, vocab: int | None = None,
         _check("argmax_rows", L.argmax_rows(logits.data_ptr(), rows, vocab, stride, out.data_ptr(),
                                             ws.data_ptr() if ws is not None else None, ws_bytes,
                                             _stream(dev)))
+    return out
+
+
+def argmax_rows_noalloc(logits: torch.Tensor, vocab: int | None = None,
+                        out: torch.Tensor | None = None) -> torch.Tensor:
+    """argmaxInto's tokens without any device allocation by the library: for
+    callers whose device memory is planned by someone else, or who cannot
+    afford an allocation's possible device-wide synchronisation. Uses the
+    library's fixed 64 KiB scratch; calls running at the same time on the GPU
+    race on it. ``out`` may be given to avoid this wrapper's own allocation."""
+    rows, vocab, stride = _logits_view(logits, vocab)
+    dev = logits.device
+    out = _out(out, (rows,), torch.float32, dev, "out")
+    with torch.cuda.device(dev):
+        _check("argmax_rows_noalloc", lib().argmax_rows_noalloc(logits.data_ptr(), rows, vocab, stride,
+                                                                out.data_ptr(), _stream(dev)))
     return out
 
 

@@ -29,6 +29,14 @@ constexpr int64_t kMaxClusters = 1ll << 20;
 
 thread_local int t_last_cuda_error = 0;
 
+// Scratch of argmax_rows_noalloc: one 64-bit key per (CTA, row) segment of the
+// even split, 8192 keys = 64 KiB, resident on every device that loads this
+// library until the process exits. Host code never names it directly: its
+// device address comes from cudaGetSymbolAddress (noalloc_scratch below).
+constexpr int64_t kNoAllocKeys = 8192;
+static __device__ __align__(256) uint64_t g_noalloc_keys[kNoAllocKeys];
+uint64_t *g_noalloc_ptr[kMaxDevices] = {};
+
 struct Force {
     int path = 0, cluster = 0, threads = 0;
 };
@@ -329,6 +337,42 @@ int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride
     return cuda_status(launch_rows_stream(p, a, false, stream));
 }
 
+// The device address of g_noalloc_keys on the current device, looked up once
+// per device (with that device current) and cached.
+int noalloc_scratch(const DeviceInfo &dev, uint64_t **out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_noalloc_ptr[dev.device] == nullptr) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_keys);
+        if (e != cudaSuccess || ptr == nullptr) {
+            t_last_cuda_error = static_cast<int>(e);
+            return CE_ECUDA;
+        }
+        g_noalloc_ptr[dev.device] = static_cast<uint64_t *>(ptr);
+    }
+    *out = g_noalloc_ptr[dev.device];
+    return CE_OK;
+}
+
+int argmax_rows_noalloc(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top,
+                        ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (rows > 0 && top == nullptr) return CE_EINVAL;
+    if (misaligned(top, 4)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    // the even split over at most two CTAs per SM, each at least 8192 elements
+    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(2 * dev.sms, rows * vocab / 8192));
+    if (ctas + rows > kNoAllocKeys) return CE_ERANGE;
+    uint64_t *keys = nullptr;
+    if ((st = noalloc_scratch(dev, &keys))) return st;
+    Args a = make_args(logits, rows, vocab, stride, nullptr);
+    a.top = top;
+    return cuda_status(launch_argmax_flat(a, static_cast<int>(ctas), keys, stream));
+}
+
 const char *ce_status_string(int status) {
     switch (status) {
     case CE_OK: return "ok";
@@ -336,6 +380,7 @@ const char *ce_status_string(int status) {
     case CE_EALIGN: return "pointer not aligned to its element size";
     case CE_ECUDA: return "CUDA runtime error at launch (see ce_last_cuda_error)";
     case CE_EDEVICE: return "no usable sm_103 CUDA device";
+    case CE_ERANGE: return "too many rows for argmax_rows_noalloc's fixed scratch (rows + 2 * SMs must be <= 8192)";
     default: return "unknown status";
     }
 }
