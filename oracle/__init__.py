@@ -7,9 +7,14 @@ never does, and this package imports nothing from it.
 What each function computes follows the API reference page "gizml:netops"
 (gizstack.com/docs/reference/gizml/netops.md), section Functions:
 ``crossEntropyRows`` (per-row loss), ``crossEntropyLoss`` (mean in f64 in row
-order), ``crossEntropyGrad`` ((softmax - onehot) * scale) and ``argmaxInto``;
-section Methods: ``Tensor.argmax`` (first of equals, NaN never wins). The C
-source ``ce_oracle.c`` states each definition beside its code.
+order), ``crossEntropyGrad`` ((softmax - onehot) * scale), ``argmaxInto``,
+``candidatesInto`` and ``splitSumInto``; section Methods: ``Tensor.argmax``
+(first of equals, NaN never wins); section Constants: ``TOP_EACH``,
+``CANDIDATE_ROW``. Softmax and log-softmax rows follow the same row statistics
+(the gpukit API page's ``gkd_softmax_rows``; a request's ``logprobs`` in the
+guide "Tensors, GPU kernels and AI models", Step 5). The C source
+``ce_oracle.c`` states each definition, and each reading the pages leave
+open, beside its code.
 
 Pins: every function here is checked by ``tests/test_oracle_pins.py`` against
 closed forms, brute force, library routines and invariants; no function is
@@ -75,6 +80,11 @@ class Oracle:
         lib.oracle_ce_mean.restype = ctypes.c_double
         lib.oracle_argmax.argtypes = [_vp, _i64, _i64, _i64, _vp]
         lib.oracle_argmax.restype = ctypes.c_int
+        for name in ("oracle_softmax", "oracle_log_softmax", "oracle_candidates"):
+            getattr(lib, name).argtypes = [_vp, _i64, _i64, _i64, _vp]
+            getattr(lib, name).restype = ctypes.c_int
+        lib.oracle_split_sum.argtypes = [_vp, _vp, _i64, _i64, ctypes.c_int, _vp]
+        lib.oracle_split_sum.restype = ctypes.c_int
         self.lib = lib
 
     # -- helpers ---------------------------------------------------------
@@ -162,6 +172,54 @@ class Oracle:
 
         self._run(fn, rows, threads)
         return out
+
+    # -- rows beside the loss -------------------------------------------
+    def _rows_op(self, name, logits, vocab, width, dtype, threads):
+        rows, stride = self._check(logits, vocab)
+        out = np.empty((rows, width), dtype=dtype)
+        fn_c = getattr(self.lib, name)
+
+        def fn(a, b):
+            if fn_c(logits[a:b].ctypes.data, b - a, vocab, stride, out[a:b].ctypes.data):
+                raise ValueError(f"{name} rejected its arguments")
+
+        self._run(fn, rows, threads)
+        return out
+
+    def softmax(self, logits: np.ndarray, vocab: int, threads: int = 1):
+        """Softmax rows exp(x - m) / sum, f64 [rows, vocab]."""
+        return self._rows_op("oracle_softmax", logits, vocab, vocab, np.float64, threads)
+
+    def log_softmax(self, logits: np.ndarray, vocab: int, threads: int = 1):
+        """Log-softmax rows (x - m) - log1p(t), f64 [rows, vocab]."""
+        return self._rows_op("oracle_log_softmax", logits, vocab, vocab, np.float64, threads)
+
+    def candidates(self, logits: np.ndarray, vocab: int, threads: int = 1):
+        """Sampling candidates (candidatesInto), f32 [rows, 2048]: pair 4t + k is
+        (value, column) of thread t's rank-k value; (-inf, -1) when empty."""
+        return self._rows_op("oracle_candidates", logits, vocab, CANDIDATE_ROW, np.float32, threads)
+
+    def split_sum(self, y: np.ndarray, parts: np.ndarray, add: bool):
+        """splitSumInto: (add ? y : 0) + the sum of the parts in split order, f64
+        [total]. ``parts`` is float32 [splits, total]; ``y`` float32 [total]."""
+        parts = np.ascontiguousarray(parts, dtype=np.float32)
+        if parts.ndim != 2 or parts.shape[0] < 1:
+            raise ValueError("parts must be [splits >= 1, total]")
+        splits, total = parts.shape
+        y = np.ascontiguousarray(y, dtype=np.float32)
+        if y.shape != (total,):
+            raise ValueError("y must be [total]")
+        out = np.empty(total, dtype=np.float64)
+        if self.lib.oracle_split_sum(y.ctypes.data, parts.ctypes.data, total, splits,
+                                     1 if add else 0, out.ctypes.data):
+            raise ValueError("oracle_split_sum rejected its arguments")
+        return out
+
+
+# candidatesInto's row: 256 threads x TOP_EACH = 4 (value, token) pairs.
+CANDIDATE_THREADS = 256
+TOP_EACH = 4
+CANDIDATE_ROW = 2 * CANDIDATE_THREADS * TOP_EACH
 
 
 def load(lib_path: str | None = None) -> Oracle:

@@ -1,6 +1,8 @@
 /*
  * ce_oracle.c -- the plain, slow CPU oracle of the row-wise softmax
- * cross-entropy path: per-row loss, mean loss, gradient and row argmax.
+ * cross-entropy path: per-row loss, mean loss, gradient and row argmax;
+ * beside them, the rows a language model's step reads from the same logits:
+ * softmax and log-softmax rows, sampling candidates, and split sums.
  *
  * TEST INFRASTRUCTURE. Only the tests, the smoke check and the bench's CPU
  * baseline call this file. The CUDA library shares no code, header, table
@@ -13,8 +15,11 @@
  *
  * Source of every definition: the API reference page "gizml:netops"
  * (gizstack.com/docs/reference/gizml/netops.md), section Functions:
- * crossEntropyLoss, crossEntropyRows, crossEntropyGrad, argmaxInto; and
- * section Methods: Tensor.argmax.
+ * crossEntropyLoss, crossEntropyRows, crossEntropyGrad, argmaxInto,
+ * candidatesInto, splitSumInto; section Methods: Tensor.argmax; section
+ * Constants: TOP_EACH, CANDIDATE_ROW. The softmax and log-softmax rows also
+ * cite the gpukit API page (dev.nu, gkd_softmax_rows) and the guide
+ * "Tensors, GPU kernels and AI models" (Step 5, a request's logprobs).
  *
  * Layout: row i of the logits starts at logits + i * stride; only its first
  * `vocab` columns are read. Labels are int64, one per row. The gradient is
@@ -23,7 +28,7 @@
 #include <math.h>
 #include <stdint.h>
 
-#define ORACLE_VERSION 1
+#define ORACLE_VERSION 2
 
 int oracle_version(void) { return ORACLE_VERSION; }
 
@@ -190,6 +195,136 @@ int oracle_argmax(const float *logits, int64_t rows, int64_t vocab, int64_t stri
             }
         }
         idx_out[i] = best;
+    }
+    return 0;
+}
+
+/*
+ * Softmax rows: p_j = exp(x_j - m) / s, the softmax of the crossEntropyGrad
+ * entry without its one-hot term and scale (also the "row softmax" of the
+ * ready-made device kernels, gkd_softmax_rows, on the gpukit API page,
+ * dev.nu). 1/s is taken in f64 (the mathematical softmax). A degenerate row
+ * (NaN, +inf, or all -inf) gives a NaN row. out: rows * vocab doubles, dense.
+ */
+int oracle_softmax(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+                   double *out)
+{
+    if (rows < 0 || vocab < 1 || stride < vocab)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *x = logits + i * stride;
+        double *o = out + i * vocab;
+        row_stats st = stats_of_row(x, vocab);
+        for (int64_t j = 0; j < vocab; ++j)
+            o[j] = st.degenerate ? NAN : exp((double)x[j] - st.m) / (1.0 + st.t);
+    }
+    return 0;
+}
+
+/*
+ * Log-softmax rows: log p_j = x_j - m - log(s), the log probabilities of the
+ * tokens (the `logprobs` of a request's Sampling, "Tensors, GPU kernels and
+ * AI models", Step 5). With s = 1 + t as in stats_of_row:
+ *   log p_j = (x_j - m) - log1p(t),
+ * which keeps a log probability near 0 (a dominant token) to full relative
+ * precision. A degenerate row gives a NaN row; a -inf entry of a finite row
+ * gives -inf. out: rows * vocab doubles, dense.
+ */
+int oracle_log_softmax(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+                       double *out)
+{
+    if (rows < 0 || vocab < 1 || stride < vocab)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *x = logits + i * stride;
+        double *o = out + i * vocab;
+        row_stats st = stats_of_row(x, vocab);
+        for (int64_t j = 0; j < vocab; ++j)
+            o[j] = st.degenerate ? NAN : ((double)x[j] - st.m) - log1p(st.t);
+    }
+    return 0;
+}
+
+/*
+ * candidatesInto (netops, Functions) with the constants TOP_EACH and
+ * CANDIDATE_ROW (netops, Constants): a workgroup of 256 threads reads a row;
+ * each thread keeps the TOP_EACH = 4 largest logits of the values it reads;
+ * a row's candidates are the 256 * 4 kept (value, token) pairs, 2048 floats.
+ * The entries leave open which columns a thread reads, the order of a
+ * thread's kept values and what fills a slot for which a thread read too
+ * few values. This oracle takes the plainest readings:
+ *   - thread t reads columns t, t + 256, t + 512, ... below vocab;
+ *   - values rank by value, larger first, and among equal values the lower
+ *     column first (the first of equals, as argmaxInto); NaN is never kept;
+ *   - pair 4t + k holds thread t's rank-k value: float 2(4t + k) is the value,
+ *     float 2(4t + k) + 1 the column as f32;
+ *   - a slot with no value holds (-inf, -1).
+ * cand: rows * 2048 floats (the values are copies of the logits, so nothing
+ * here is rounded).
+ */
+#define CAND_THREADS 256
+#define CAND_KEEP 4
+
+int oracle_candidates(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+                      float *cand)
+{
+    if (rows < 0 || vocab < 1 || stride < vocab)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *x = logits + i * stride;
+        float *out = cand + i * (int64_t)(2 * CAND_THREADS * CAND_KEEP);
+        for (int t = 0; t < CAND_THREADS; ++t) {
+            float kv[CAND_KEEP];
+            int64_t kc[CAND_KEEP];
+            int kept = 0;
+            for (int64_t j = t; j < vocab; j += CAND_THREADS) {
+                float v = x[j];
+                if (isnan(v))
+                    continue;
+                /* where v ranks among the kept values: below every kept value
+                   that is larger or equal (equal ones have lower columns) */
+                int pos = 0;
+                while (pos < kept && kv[pos] >= v)
+                    ++pos;
+                if (pos >= CAND_KEEP)
+                    continue;
+                int last = kept < CAND_KEEP ? kept : CAND_KEEP - 1;
+                for (int q = last; q > pos; --q) {
+                    kv[q] = kv[q - 1];
+                    kc[q] = kc[q - 1];
+                }
+                kv[pos] = v;
+                kc[pos] = j;
+                if (kept < CAND_KEEP)
+                    ++kept;
+            }
+            for (int k = 0; k < CAND_KEEP; ++k) {
+                float *slot = out + 2 * (CAND_KEEP * t + k);
+                slot[0] = k < kept ? kv[k] : -INFINITY;
+                slot[1] = k < kept ? (float)kc[k] : -1.0f;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * splitSumInto (netops, Functions): the `total` values at y and `splits`
+ * parts at p. Reading: part s is the `total` f32 values at p + s * total;
+ *   y[i] = (add ? y[i] : 0) + sum_{s = 0 .. splits-1} p[s * total + i],
+ * summed in f64 in split order. With add = 0 the old y is never read.
+ * y_out: total doubles (y_in is read only when add != 0).
+ */
+int oracle_split_sum(const float *y_in, const float *p, int64_t total, int64_t splits, int add,
+                     double *y_out)
+{
+    if (total < 0 || splits < 1)
+        return -1;
+    for (int64_t i = 0; i < total; ++i) {
+        double acc = add ? (double)y_in[i] : 0.0;
+        for (int64_t s = 0; s < splits; ++s)
+            acc += (double)p[s * total + i];
+        y_out[i] = acc;
     }
     return 0;
 }

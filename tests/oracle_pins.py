@@ -7,8 +7,10 @@ oracle; ``tests/test_oracle_mutants.py`` runs them on copies of the oracle with
 a planted mistake and requires that some pin fails for each.
 
 The definitions pinned are those of the API reference page "gizml:netops"
-(Functions: crossEntropyLoss, crossEntropyRows, crossEntropyGrad, argmaxInto;
-Methods: Tensor.argmax).
+(Functions: crossEntropyLoss, crossEntropyRows, crossEntropyGrad, argmaxInto,
+candidatesInto, splitSumInto; Methods: Tensor.argmax; Constants: TOP_EACH,
+CANDIDATE_ROW), and the softmax / log-softmax rows read from the same row
+statistics.
 """
 from __future__ import annotations
 
@@ -297,11 +299,200 @@ def pin_golden_closed_forms(orc):
         assert int(orc.argmax(x, V)[0]) == c["argmax"], f"golden argmax {c['logits']}"
 
 
+# ---------------------------------------------------------------------------
+# softmax and log-softmax rows
+
+
+def pin_softmax_closed_forms(orc):
+    """Uniform rows: p = 1/V, log p = -log V. Two classes at gap d: p = sigmoid,
+    log p = -softplus. A dominant token at a large max: log p = -log1p(e^-gap)."""
+    for V in (1, 2, 7, 1000, 50257):
+        x = np.full((2, V), 3.5, dtype=np.float32)
+        _close(orc.softmax(x, V), np.full((2, V), 1.0 / V), rel=1e-15, what=f"uniform softmax V={V}")
+        _close(orc.log_softmax(x, V), np.full((2, V), -math.log(V)), rel=1e-15, abs_=1e-300,
+               what=f"uniform log-softmax V={V}")
+    for d in (-60.0, -20.0, -1.0, 0.0, 2.0, 30.0):
+        x = np.array([[1.0, 1.0 + d]], dtype=np.float32)
+        _close(orc.softmax(x, 2), [[1.0 / (1.0 + math.exp(d)), 1.0 / (1.0 + math.exp(-d))]],
+               rel=1e-13, abs_=1e-300, what=f"two-class softmax d={d}")
+        sp = (lambda z: math.log1p(math.exp(z)) if z <= 0 else z + math.log1p(math.exp(-z)))
+        _close(orc.log_softmax(x, 2), [[-sp(d), -sp(-d)]], rel=1e-13, what=f"two-class log-softmax d={d}")
+    x = np.array([[100.0, 50.0, 40.0]], dtype=np.float32)
+    want0 = -math.log1p(math.exp(-50) + math.exp(-60))
+    got = orc.log_softmax(x, 3)
+    _close(got[0, 0], want0, rel=1e-12, what="dominant token log p")
+    _close(got[0, 1:], [-50 + want0, -60 + want0], rel=1e-14, what="other tokens log p")
+
+
+def pin_softmax_torch(orc):
+    """torch.softmax / torch.log_softmax in f64 on the CPU (library routines)."""
+    g = torch.Generator().manual_seed(31)
+    x = (4.0 * torch.randn(9, 301, generator=g)).float()
+    _close(orc.softmax(x.numpy(), 301), torch.softmax(x.double(), 1).numpy(), abs_=1e-16,
+           rel=1e-13, what="torch softmax")
+    _close(orc.log_softmax(x.numpy(), 301), torch.log_softmax(x.double(), 1).numpy(), rel=1e-13,
+           what="torch log_softmax")
+
+
+def pin_softmax_invariants(orc):
+    """Rows sum to 1; exp(log p) = p; padding past vocab is never read;
+    non-finite rows are NaN; -inf entries of a finite row get p = 0, log p = -inf."""
+    rng = np.random.default_rng(41)
+    R, V, S = 5, 77, 90
+    dense = (6 * rng.standard_normal((R, V))).astype(np.float32)
+    p = orc.softmax(dense, V)
+    _close(p.sum(axis=1), np.ones(R), abs_=1e-14, what="softmax row sums")
+    _close(np.exp(orc.log_softmax(dense, V)), p, rel=1e-13, what="exp(log p) = p")
+    for pad in (float("nan"), 1e30):
+        x = np.full((R, S), pad, dtype=np.float32)
+        x[:, :V] = dense
+        _close(orc.softmax(x, V), p, rel=0, what="padded softmax")
+        _close(orc.log_softmax(x, V), orc.log_softmax(dense, V), rel=0, what="padded log-softmax")
+    nan, inf = float("nan"), float("inf")
+    bad = np.array([[1.0, nan, 2.0], [1.0, inf, 2.0], [-inf, -inf, -inf]], dtype=np.float32)
+    assert np.isnan(orc.softmax(bad, 3)).all() and np.isnan(orc.log_softmax(bad, 3)).all()
+    x = np.array([[0.0, -inf, 0.0]], dtype=np.float32)
+    _close(orc.softmax(x, 3), [[0.5, 0.0, 0.5]], rel=1e-15, what="-inf softmax")
+    _close(orc.log_softmax(x, 3), [[-math.log(2), -inf, -math.log(2)]], rel=1e-15, what="-inf log p")
+
+
+# ---------------------------------------------------------------------------
+# sampling candidates (candidatesInto, TOP_EACH, CANDIDATE_ROW)
+
+_CT, _CK = 256, 4  # threads of a candidates workgroup, values each keeps
+
+
+def _slots(cand_row):
+    """[256, 4, 2] view of one row's candidates: (value, column) per slot."""
+    return np.asarray(cand_row, dtype=np.float32).reshape(_CT, _CK, 2)
+
+
+def _want_cols(V, t, order):
+    """The columns t, t + 256, ... below V, in `order` (first 4 kept)."""
+    cols = list(range(t, V, _CT))
+    cols = cols[::-1] if order == "desc" else cols
+    return cols[:_CK]
+
+
+def pin_candidates_closed_forms(orc):
+    """Rows whose candidates follow by hand: x_j = j keeps each thread's last
+    four columns, largest first; x_j = -j and a constant row keep its first
+    four (equal values: the lower column ranks higher); an all -inf row keeps
+    -inf values; NaN is never kept; a slot with no value is (-inf, -1)."""
+    inf, nan = float("inf"), float("nan")
+    for V in (1, 3, 255, 256, 257, 700, 1024, 1029, 2100):
+        up = np.arange(V, dtype=np.float32)[None]
+        rows = {
+            "increasing": (up, "desc"),
+            "decreasing": (-up, "asc"),
+            "constant": (np.full((1, V), 2.5, np.float32), "asc"),
+            "all -inf": (np.full((1, V), -inf, np.float32), "asc"),
+        }
+        for name, (x, order) in rows.items():
+            sl = _slots(orc.candidates(x, V)[0])
+            for t in range(_CT):
+                cols = _want_cols(V, t, order)
+                for k in range(_CK):
+                    if k < len(cols):
+                        want = (float(x[0, cols[k]]), float(cols[k]))
+                    else:
+                        want = (-inf, -1.0)
+                    got = (float(sl[t, k, 0]), float(sl[t, k, 1]))
+                    assert got == want, f"candidates {name} V={V} thread {t} slot {k}: {got} != {want}"
+        # NaN at the even columns: even threads keep nothing, odd ones as the constant row
+        x = np.full((1, V), 1.0, np.float32)
+        x[0, 0::2] = nan
+        sl = _slots(orc.candidates(x, V)[0])
+        for t in range(_CT):
+            cols = _want_cols(V, t, "asc") if t % 2 else []
+            for k in range(_CK):
+                want = (1.0, float(cols[k])) if k < len(cols) else (-inf, -1.0)
+                got = (float(sl[t, k, 0]), float(sl[t, k, 1]))
+                assert got == want, f"candidates NaN V={V} thread {t} slot {k}: {got} != {want}"
+
+
+def pin_candidates_torch_topk(orc):
+    """Rows of distinct values: each thread's slots are torch.topk (a library
+    routine) of the values at its columns, in order, with their columns."""
+    rng = np.random.default_rng(51)
+    for V, S in ((1, 1), (300, 300), (1023, 1030), (5003, 5003)):
+        x = np.full((3, S), 1e30, dtype=np.float32)
+        x[:, :V] = rng.permutation(3 * V).reshape(3, V).astype(np.float32) * 0.5 - V
+        cand = orc.candidates(x, V)
+        for i in range(3):
+            sl = _slots(cand[i])
+            for t in range(_CT):
+                vals = torch.from_numpy(x[i, t:V:_CT].copy())
+                k = min(_CK, vals.numel())
+                if k:
+                    tv, ti = torch.topk(vals, k, sorted=True)
+                    assert (sl[t, :k, 0] == tv.numpy()).all(), f"topk values V={V} t={t}"
+                    assert (sl[t, :k, 1] == (t + _CT * ti.numpy()).astype(np.float32)).all(), \
+                        f"topk columns V={V} t={t}"
+                assert (sl[t, k:, 0] == -np.inf).all() and (sl[t, k:, 1] == -1).all()
+
+
+def pin_candidates_invariants(orc):
+    """Rows full of ties (small integers) and NaN: every slot is (x[c], c) with
+    c = t mod 256; a thread's slots are ordered; it keeps min(4, its non-NaN
+    values); the row's four best (value, then the lower column) are all kept,
+    and the best is torch.argmax's first maximal index on NaN-free rows."""
+    rng = np.random.default_rng(61)
+    for V in (5, 300, 1025, 4099):
+        x = rng.integers(0, 6, size=(4, V)).astype(np.float32)
+        x[1, rng.integers(0, V, size=V // 3)] = np.nan
+        cand = orc.candidates(x, V)
+        for i in range(4):
+            sl = _slots(cand[i])
+            kept = set()
+            for t in range(_CT):
+                real = [(float(v), int(c)) for v, c in sl[t] if c >= 0]
+                nn = int(np.count_nonzero(~np.isnan(x[i, t:V:_CT])))
+                assert len(real) == min(_CK, nn), f"kept count V={V} t={t}"
+                for v, c in real:
+                    assert c % _CT == t and x[i, c] == v, f"slot ({v}, {c}) of thread {t}"
+                keys = [(-v, c) for v, c in real]
+                assert keys == sorted(keys), f"slot order V={V} t={t}"
+                kept.update(c for _, c in real)
+            order = sorted((-float(x[i, j]), j) for j in range(V) if not math.isnan(x[i, j]))
+            assert all(c in kept for _, c in order[:_CK]), f"row top-4 missing V={V}"
+            best = min((-float(v), int(c)) for v, c in sl.reshape(-1, 2) if c >= 0)
+            if not np.isnan(x[i]).any():
+                assert best[1] == int(torch.argmax(torch.from_numpy(x[i]))), "best candidate"
+
+
+# ---------------------------------------------------------------------------
+# split sums (splitSumInto)
+
+
+def pin_split_sum(orc):
+    """Small integers sum exactly in any order; random parts against math.fsum;
+    add = 0 never reads y (NaN there changes nothing); one part is a copy."""
+    rng = np.random.default_rng(71)
+    for splits, total in ((1, 5), (2, 7), (5, 1000), (13, 3)):
+        parts = rng.integers(-50, 50, size=(splits, total)).astype(np.float32)
+        y = rng.integers(-50, 50, size=total).astype(np.float32)
+        want = parts.astype(np.int64).sum(axis=0)
+        _close(orc.split_sum(y, parts, add=True), want + y.astype(np.int64), rel=0, what="add")
+        _close(orc.split_sum(np.full(total, np.nan, np.float32), parts, add=False), want, rel=0,
+               what="no add")
+        parts = rng.standard_normal((splits, total)).astype(np.float32) * 1e3
+        y = rng.standard_normal(total).astype(np.float32)
+        want = [math.fsum([float(y[i])] + [float(v) for v in parts[:, i]]) for i in range(total)]
+        _close(orc.split_sum(y, parts, add=True), want, rel=1e-12, abs_=1e-9, what="fsum")
+    one = rng.standard_normal((1, 9)).astype(np.float32)
+    _close(orc.split_sum(np.zeros(9, np.float32), one, add=False), one[0], rel=0, what="one part")
+    assert orc.split_sum(np.zeros(0, np.float32), np.zeros((3, 0), np.float32), add=True).shape == (0,)
+
+
 PINS = [
     pin_uniform_rows, pin_two_class_closed_form, pin_tiny_loss, pin_bruteforce_tiny,
     pin_torch_cross_entropy, pin_central_differences, pin_grad_invariants,
     pin_shift_invariance, pin_mean, pin_nonfinite_rows, pin_bad_label, pin_stride_padding,
     pin_argmax_bruteforce, pin_argmax_nan_rules, pin_golden_closed_forms,
+    pin_softmax_closed_forms, pin_softmax_torch, pin_softmax_invariants,
+    pin_candidates_closed_forms, pin_candidates_torch_topk, pin_candidates_invariants,
+    pin_split_sum,
 ]
 
 

@@ -30,6 +30,22 @@ MUTANTS = {
                         "            if (!seen || v > best_v || isnan(v))"),
     "nan_rows_not_flagged": ("if (any_nan || !seen || isinf(r.m))", "if (!seen)"),
     "grad_transposed": ("double *g = grad_out + i * vocab;", "double *g = grad_out + i;"),
+    "softmax_no_shift": ("o[j] = st.degenerate ? NAN : exp((double)x[j] - st.m) / (1.0 + st.t);",
+                         "o[j] = st.degenerate ? NAN : exp((double)x[j]) / (1.0 + st.t);"),
+    "softmax_sum_is_t": ("exp((double)x[j] - st.m) / (1.0 + st.t);", "exp((double)x[j] - st.m) / st.t;"),
+    "log_softmax_cancels": ("((double)x[j] - st.m) - log1p(st.t);", "(double)x[j] - (st.m + log1p(st.t));"),
+    "log_softmax_log_t": ("((double)x[j] - st.m) - log1p(st.t);", "((double)x[j] - st.m) - log(st.t);"),
+    "cand_last_of_equals": ("while (pos < kept && kv[pos] >= v)", "while (pos < kept && kv[pos] > v)"),
+    "cand_ascending": ("while (pos < kept && kv[pos] >= v)", "while (pos < kept && kv[pos] <= v)"),
+    "cand_nan_kept": ("                if (isnan(v))\n                    continue;\n                /* where", "                /* where"),
+    "cand_blocked_columns": ("for (int64_t j = t; j < vocab; j += CAND_THREADS) {",
+                             "for (int64_t j = t * 4; j < vocab && j < t * 4 + 4; ++j) {"),
+    "cand_keeps_three": ("if (pos >= CAND_KEEP)\n                    continue;", "if (pos >= CAND_KEEP - 1)\n                    continue;"),
+    "cand_empty_token_zero": ("slot[1] = k < kept ? (float)kc[k] : -1.0f;", "slot[1] = k < kept ? (float)kc[k] : 0.0f;"),
+    "cand_thread_major_swapped": ("float *slot = out + 2 * (CAND_KEEP * t + k);", "float *slot = out + 2 * (CAND_THREADS * k + t);"),
+    "split_sum_add_ignored": ("double acc = add ? (double)y_in[i] : 0.0;", "double acc = 0.0;"),
+    "split_sum_drops_last_part": ("for (int64_t s = 0; s < splits; ++s)", "for (int64_t s = 0; s + 1 < splits; ++s)"),
+    "split_sum_transposed": ("acc += (double)p[s * total + i];", "acc += (double)p[i * splits + s];"),
 }
 
 
