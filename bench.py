@@ -408,7 +408,7 @@ def run_case(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    name = args.workload or (W.DECODE if args.case == "argmax" else W.HEADLINE)
+    name = args.workload or (W.DECODE if args.case in ("argmax", "candidates") else W.HEADLINE)
     w = W.WORKLOADS[name]
     if args.rows:
         w = w.with_rows(args.rows)
@@ -422,6 +422,25 @@ def run_case(args):
     elif args.case == "rows":
         op = lambda: ce.ce_rows(b.logits, b.labels, vocab=V, out=out)
         nbytes, opn = 4 * R * V + 12 * R, ce.OP_ROWS
+    elif args.case in ("softmax", "log_softmax"):
+        dense = torch.empty((R, V), dtype=torch.float32, device=dev)
+        fn = ce.softmax_rows if args.case == "softmax" else ce.log_softmax_rows
+        op = lambda: fn(b.logits, vocab=V, out=dense)
+        nbytes, opn = 8 * R * V, ce.OP_SOFTMAX if args.case == "softmax" else ce.OP_LOG_SOFTMAX
+    elif args.case == "candidates":
+        cand = torch.empty((R, ce.CANDIDATE_ROW), dtype=torch.float32, device=dev)
+        op = lambda: ce.candidates_rows(b.logits, vocab=V, out=cand)
+        nbytes, opn = 4 * R * V + 4 * ce.CANDIDATE_ROW * R, ce.OP_CANDIDATES
+    elif args.case == "split_sum":
+        # the workload's logits as `splits` parts of R * V / splits values
+        splits = max(1, args.splits)
+        total = (R * V) // splits
+        parts = b.logits[:, :V].reshape(-1)[: splits * total].view(splits, total)
+        if not parts.is_contiguous():
+            parts = parts.contiguous()
+        y = torch.empty(total, dtype=torch.float32, device=dev)
+        op = lambda: ce.split_sum(parts, y, add=False)
+        nbytes, opn = 4 * (splits + 1) * total, None
     else:
         op = lambda: ce.argmax_rows(b.logits, vocab=V, out=out)
         nbytes, opn = argmax_bytes(R, V), ce.OP_ARGMAX
@@ -444,7 +463,7 @@ def run_case(args):
                 e1.record(stream)
                 evs.append((e0, e1))
             torch.cuda.synchronize()
-            plan = ce.plan(opn, R, V, w.stride)
+            plan = ce.plan(opn, R, V, w.stride) if opn is not None else None
         except ce.CeError as e:
             print(json.dumps({"case": args.case, "workload": w.name, "force": force, "error": str(e)}), flush=True)
             continue
@@ -454,7 +473,7 @@ def run_case(args):
         med = statistics.median(ms)
         print(json.dumps({"case": args.case, "workload": w.name, "rows": R, "vocab": V, "force": force,
                           "plan": plan, "ms_median": round(med, 5), "ms_min": round(min(ms), 5),
-                          "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1),
+                          "GB/s": round(nbytes / (med * 1e-3) / 1e9, 1), "rows/s": round(R / (med * 1e-3), 1),
                           "frac": round(nbytes / (med * 1e-3) / 1e9 / peak, 4), "peak_kind": kind,
                           "flush": bool(args.flush)}), flush=True)
     return 0
@@ -469,8 +488,10 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=8192, help="rows of the CPU-oracle sample")
     ap.add_argument("--ref-rows", type=int, default=256, help="rows per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["grad", "rows", "argmax"],
+    ap.add_argument("--case", choices=["grad", "rows", "argmax", "softmax", "log_softmax", "candidates",
+                                       "split_sum"],
                     help="time one operation only (sweeps, profiler captures)")
+    ap.add_argument("--splits", type=int, default=4, help="with --case split_sum: parts to join")
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), help="with --case: the workload")
     ap.add_argument("--rows", type=int, default=0, help="with --case: rows of the workload to use")
     ap.add_argument("--force", default="", help="with --case: path,cluster,threads (see ce_debug_force)")

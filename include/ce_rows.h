@@ -1,12 +1,15 @@
 /*
  * ce_rows.h -- C ABI of the row-wise softmax cross-entropy library for
  * NVIDIA GB300 (sm_103a): per-row loss, mean loss, fused loss + gradient,
- * and the row argmax that closes a decode step.
+ * and the row argmax that closes a decode step; beside them, the rows a
+ * language model's step reads from the same logits (softmax, log-softmax,
+ * sampling candidates) and the join of split partial sums.
  *
  * Definitions follow the API reference page "gizml:netops"
  * (gizstack.com/docs/reference/gizml/netops.md), section Functions:
- * crossEntropyRows, crossEntropyLoss, crossEntropyGrad, argmaxInto; and
- * section Methods: Tensor.argmax.
+ * crossEntropyRows, crossEntropyLoss, crossEntropyGrad, argmaxInto,
+ * candidatesInto, splitSumInto; section Methods: Tensor.argmax; section
+ * Constants: TOP_EACH, CANDIDATE_ROW.
  *
  * Common conventions of every entry point:
  *  - Logits are f32, row-major: row i starts at logits + i * stride
@@ -167,6 +170,67 @@ CE_API int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t strid
 CE_API int argmax_rows_noalloc(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top,
                                ce_stream_t stream);
 
+/*
+ * Softmax rows: out[i, j] = exp(x_ij - m_i) * f32(1 / sum_i), the softmax of
+ * crossEntropyGrad (gizml:netops, Functions) without its one-hot term and
+ * scale -- the row softmax among the gpukit API page's device kernels
+ * (dev.nu, gkd_softmax_rows). Same kernel, same single HBM read of each
+ * logit and single write of each output as ce_grad.
+ *   logits: [rows, stride] f32, read only, unless out == logits.
+ *   out:    [rows, vocab] f32 dense, written. out == logits (in place) is
+ *           allowed when stride == vocab; any other overlap is not.
+ * A row holding a NaN or +inf, or all -inf, gives a NaN row; a -inf entry of
+ * a finite row gives 0.
+ */
+CE_API int softmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *out,
+                        ce_stream_t stream);
+
+/*
+ * Log-softmax rows: out[i, j] = (x_ij - m_i) - log(sum_i), the log
+ * probabilities of the tokens (a request's `logprobs`, guide "Tensors, GPU
+ * kernels and AI models", Step 5). log(sum) is taken as log1p(t), t the sum
+ * over all columns but one holding the max, so the log probability of a
+ * dominant token keeps its relative accuracy. Layout, aliasing and
+ * non-finite rows as softmax_rows; a -inf entry of a finite row gives -inf.
+ */
+CE_API int log_softmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *out,
+                            ce_stream_t stream);
+
+/* candidatesInto's workgroup, TOP_EACH and CANDIDATE_ROW (gizml:netops, Constants). */
+#define CE_CANDIDATE_THREADS 256
+#define CE_TOP_EACH 4
+#define CE_CANDIDATE_ROW 2048
+
+/*
+ * candidatesInto (gizml:netops, Functions; Constants TOP_EACH, CANDIDATE_ROW):
+ * each row's sampling candidates. A workgroup of CE_CANDIDATE_THREADS = 256
+ * threads reads the row; thread t reads columns t, t + 256, t + 512, ...
+ * below vocab and keeps its CE_TOP_EACH = 4 largest values, ranked by value
+ * and, among equal values, by the lower column (NaN is never kept). Row i's
+ * candidates are the CE_CANDIDATE_ROW = 2048 floats at cand + 2048 * i:
+ * float 2(4t + k) is thread t's rank-k value and float 2(4t + k) + 1 its
+ * column as f32 (exact, vocab <= 2^24); a slot for which thread t read no
+ * value holds (-inf, -1). Bit-exact: the values are copies of the logits.
+ * Only the direct form (rows at logits + i * stride), as argmax_rows.
+ *   logits: [rows, stride] f32, read only.
+ *   cand:   [rows, 2048] f32, written; must not overlap the logits.
+ */
+CE_API int candidates_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *cand,
+                           ce_stream_t stream);
+
+/*
+ * splitSumInto (gizml:netops, Functions): joins `splits` partial results of
+ * `total` f32 values each (part s at parts + s * total, e.g. the partial
+ * products of a split reduction):
+ *     y[i] = (add ? y[i] : 0) + parts[0][i] + ... + parts[splits-1][i],
+ * added in f32 in split order. With add == 0 the old y is never read.
+ *   y:     [total] f32, written (read first when add != 0).
+ *   parts: [splits, total] f32, read only. y may be parts itself (part 0),
+ *          any other overlap is rejected (CE_EINVAL).
+ * total == 0 launches nothing; splits < 1 is CE_EINVAL.
+ */
+CE_API int split_sum(float *y, const float *parts, int64_t total, int64_t splits, int add, ce_stream_t stream);
+
 /* Human-readable text of a status code (a static string). */
 CE_API const char *ce_status_string(int status);
 
@@ -190,12 +254,12 @@ CE_API int ce_device_error_reset(ce_stream_t stream);
 /*
  * Launch-plan override, for tests and tuning: forces the kernel family
  * (path: 0 automatic, 1 shared-memory-staged (persistent), 2 streaming from
- * global, 3 persistent ring of bulk copies, 4 shared-memory-staged with one
- * row per cluster, 5 argmax split evenly over the GPU -- needs a workspace),
- * the
- * CTAs that share one row (cluster: 0 automatic, else 1..16) and the
- * threads of a CTA (threads: 0 automatic, else 128 or 256; 512 is
- * rejected by every kernel family).
+ * global, 3 persistent ring of bulk copies (ce_grad only), 4
+ * shared-memory-staged with one row per cluster, 5 argmax split evenly over
+ * the GPU -- needs a workspace), the CTAs that share one row (cluster: 0
+ * automatic, else 1..16; candidates_rows takes at most 8) and the threads of
+ * a CTA (threads: 0 automatic, else 128 or 256; 512 is rejected by every
+ * kernel family; candidates_rows takes 256 only).
  * Applies to every later call in the process. A forced plan that cannot
  * launch on this device makes the calls return CE_EINVAL.
  */
@@ -203,7 +267,8 @@ CE_API int ce_debug_force(int path, int cluster, int threads);
 
 /*
  * The plan the library would pick (host only, launches nothing) for
- * op (0 ce_rows, 1 ce_grad, 2 argmax_rows) on the current device:
+ * op (0 ce_rows, 1 ce_grad, 2 argmax_rows, 3 softmax_rows, 4
+ * log_softmax_rows, 5 candidates_rows) on the current device:
  * out[0] path, out[1] cluster, out[2] threads, out[3] dynamic shared bytes
  * per CTA, out[4] columns per CTA, out[5] CTAs in the grid.
  */

@@ -17,6 +17,11 @@ Functions, and section Methods for the argmax rule):
 - ``ce_grad``      crossEntropyGrad: (softmax - onehot) * scale, optionally with
                    the row losses and argmax tokens from the same read
 - ``argmax_rows``  argmaxInto: each row's token (first of equals, NaN never wins) as f32
+- ``candidates_rows``  candidatesInto: each row's 2048-float sampling candidates
+                   (256 threads x TOP_EACH = 4 (value, token) pairs)
+- ``softmax_rows`` / ``log_softmax_rows``  the softmax and the log probabilities
+                   of each row, from the same row statistics as the loss
+- ``split_sum``    splitSumInto: y (+)= the sum of split partial results
 
 Logits are a CUDA float32 tensor ``[rows, cols]`` whose rows are contiguous
 (``stride(1) == 1``); its row stride ``stride(0)`` may exceed ``vocab``
@@ -38,7 +43,9 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "ce_rows.h")
 
 CE_OK, CE_EINVAL, CE_EALIGN, CE_ECUDA, CE_EDEVICE, CE_ERANGE = 0, -1, -2, -3, -4, -5
 PATH_AUTO, PATH_STAGED, PATH_STREAM, PATH_RING, PATH_STAGED_PER_ROW, PATH_FLAT = 0, 1, 2, 3, 4, 5
-OP_ROWS, OP_GRAD, OP_ARGMAX = 0, 1, 2
+OP_ROWS, OP_GRAD, OP_ARGMAX, OP_SOFTMAX, OP_LOG_SOFTMAX, OP_CANDIDATES = 0, 1, 2, 3, 4, 5
+# candidatesInto's workgroup, TOP_EACH and CANDIDATE_ROW (gizml:netops, Constants)
+CANDIDATE_THREADS, TOP_EACH, CANDIDATE_ROW = 256, 4, 2048
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +72,10 @@ def _bind(lib):
         "argmax_rows": [vp, i64, i64, i64, vp, vp, i64, vp],
         "argmax_workspace_bytes": [i64, i64, i64],
         "argmax_rows_noalloc": [vp, i64, i64, i64, vp, vp],
+        "softmax_rows": [vp, i64, i64, i64, vp, vp],
+        "log_softmax_rows": [vp, i64, i64, i64, vp, vp],
+        "candidates_rows": [vp, i64, i64, i64, vp, vp],
+        "split_sum": [vp, vp, i64, i64, i32, vp],
         "ce_version": [],
         "ce_last_cuda_error": [],
         "ce_device_error_count": [vp, ctypes.POINTER(ctypes.c_uint64)],
@@ -248,6 +259,53 @@ def argmax_rows_noalloc(logits: torch.Tensor, vocab: int | None = None,
     return out
 
 
+def _rows_out(fn: str, logits, vocab, out, width=None):
+    rows, vocab, stride = _logits_view(logits, vocab)
+    dev = logits.device
+    out = _out(out, (rows, vocab if width is None else width), torch.float32, dev, "out")
+    with torch.cuda.device(dev):
+        _check(fn, getattr(lib(), fn)(logits.data_ptr(), rows, vocab, stride, out.data_ptr(), _stream(dev)))
+    return out
+
+
+def softmax_rows(logits: torch.Tensor, vocab: int | None = None,
+                 out: torch.Tensor | None = None) -> torch.Tensor:
+    """Each row's softmax exp(x - m) * f32(1/sum), dense f32 ``[rows, vocab]``
+    (``out`` may be ``logits`` itself when the logits are dense)."""
+    return _rows_out("softmax_rows", logits, vocab, out)
+
+
+def log_softmax_rows(logits: torch.Tensor, vocab: int | None = None,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """Each row's log probabilities (x - m) - log(sum), dense f32 ``[rows, vocab]``."""
+    return _rows_out("log_softmax_rows", logits, vocab, out)
+
+
+def candidates_rows(logits: torch.Tensor, vocab: int | None = None,
+                    out: torch.Tensor | None = None) -> torch.Tensor:
+    """candidatesInto: f32 ``[rows, 2048]``; pair 4t + k (floats 2(4t+k), +1) is
+    thread t's rank-k (value, token) of the columns t, t + 256, ...; (-inf, -1)
+    where thread t read fewer than 4 values."""
+    return _rows_out("candidates_rows", logits, vocab, out, CANDIDATE_ROW)
+
+
+def split_sum(parts: torch.Tensor, y: torch.Tensor | None = None, add: bool = False) -> torch.Tensor:
+    """splitSumInto: ``y = (y if add else 0) + parts[0] + ... + parts[-1]`` in f32
+    in split order. ``parts`` is a contiguous f32 ``[splits, total]`` tensor;
+    ``y`` f32 ``[total]`` (allocated when None; then ``add`` must be False)."""
+    if parts.dtype != torch.float32 or parts.dim() != 2 or not parts.is_contiguous() or not parts.is_cuda:
+        raise ValueError("parts must be a contiguous float32 CUDA tensor [splits, total]")
+    splits, total = parts.shape
+    dev = parts.device
+    if y is None and add:
+        raise ValueError("add=True needs y")
+    y = _out(y, (total,), torch.float32, dev, "y")
+    with torch.cuda.device(dev):
+        _check("split_sum", lib().split_sum(y.data_ptr(), parts.data_ptr(), total, splits, 1 if add else 0,
+                                            _stream(dev)))
+    return y
+
+
 # -- diagnostics and tuning ---------------------------------------------------
 
 def version() -> int:
@@ -279,7 +337,7 @@ def debug_force(path: int = 0, cluster: int = 0, threads: int = 0) -> None:
 
 
 def plan(op: int, rows: int, vocab: int, stride: int | None = None) -> dict:
-    """The launch plan the library would pick for op (OP_ROWS, OP_GRAD, OP_ARGMAX)."""
+    """The launch plan the library would pick for op (OP_ROWS ... OP_CANDIDATES)."""
     out = (ctypes.c_int64 * 6)()
     _check("ce_plan", lib().ce_plan(op, rows, vocab, vocab if stride is None else stride, out))
     keys = ("path", "cluster", "threads", "smem", "cols", "ctas")

@@ -3,7 +3,7 @@
 //
 // Conventions follow the pages this library implements: the operations of
 // "gizml:netops" (crossEntropyRows, crossEntropyLoss, crossEntropyGrad,
-// argmaxInto) run where the data is and do not wait for the GPU; and, as the
+// argmaxInto, candidatesInto, splitSumInto) run where the data is and do not wait for the GPU; and, as the
 // "gpukit" API page's device-op wrappers do, every entry point checks its
 // buffers and sizes first and fails closed -- a wrong size never reaches
 // the device.
@@ -109,7 +109,7 @@ void plan_stream(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
 
 // Launch shape of the staged fused kernel: the fewest CTAs per row whose
 // slices are at most kStagedTargetCols columns (at most 16 CTAs).
-bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster,
+bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster,
                  bool per_row, bool auto_form) {
     p.path = kPathStaged;
     p.threads = threads ? threads : 256;
@@ -123,7 +123,7 @@ bool plan_staged(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
     p.smem = kStagedHeaderBytes + 16 * 4 * w;
     if (p.smem > dev.max_smem_optin) return false;
     int active = 0;
-    if (max_active_clusters(p, kOpGrad, &active) != cudaSuccess) {
+    if (max_active_clusters(p, op, &active) != cudaSuccess) {
         (void)cudaGetLastError();
         return false;
     }
@@ -172,6 +172,23 @@ bool flat_applies(int64_t rows, int64_t vocab, const DeviceInfo &dev, bool force
 
 int64_t flat_workspace_bytes(int64_t rows, const DeviceInfo &dev) { return 8 * (2 * static_cast<int64_t>(dev.sms) + rows); }
 
+// Launch shape of the candidates kernel: 256 threads (the pages' workgroup);
+// a row split over C CTAs when there are fewer rows than about two CTAs per
+// SM, each CTA at least 2048 columns, C at most kCandMaxCluster.
+void plan_candidates(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int cluster) {
+    p.path = kPathStream;
+    p.threads = kCandThreads;
+    int64_t c = cluster;
+    if (!c) {
+        c = ceil_div(2 * static_cast<int64_t>(dev.sms), rows);
+        c = std::min<int64_t>(c, std::min<int64_t>(kCandMaxCluster, ceil_div(vocab, kStreamMinCols)));
+    }
+    p.cluster = static_cast<int>(std::max<int64_t>(1, c));
+    p.cols = round_up4(ceil_div(vocab, p.cluster));
+    p.smem = 4 * kCandListBytes + (p.cluster - 1) * kCandListBytes;
+    p.clusters = std::min<int64_t>(rows, kMaxClusters);
+}
+
 int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *out) {
     Force f;
     {
@@ -179,18 +196,26 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
         f = g_force;
     }
     Plan p;
-    if (op == kOpGrad) {
+    if (op == kOpGrad || op == kOpSoftmax || op == kOpLogSoftmax) {
         if (f.path == kPathRing) {
-            if (f.threads && f.threads != kRingThreads) return CE_EINVAL;
+            // the ring kernel writes the gradient only
+            if (op != kOpGrad || (f.threads && f.threads != kRingThreads)) return CE_EINVAL;
             if (!plan_ring(p, rows, vocab, f.cluster)) return CE_EINVAL;
         } else if (f.path == kPathStaged || f.path == kPathStagedPerRow) {
-            if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster, f.path == kPathStagedPerRow, false))
+            if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, f.path == kPathStagedPerRow, false))
                 return CE_EINVAL;
         } else if (f.path == kPathStream) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
-        } else if (!plan_staged(p, rows, vocab, dev, f.threads, f.cluster, false, true)) {
+        } else if (f.path == kPathFlat) {
+            return CE_EINVAL;
+        } else if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, false, true)) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
         }
+    } else if (op == kOpCandidates) {
+        if (f.path != kPathAuto && f.path != kPathStream) return CE_EINVAL;
+        if (f.threads && f.threads != kCandThreads) return CE_EINVAL;
+        if (f.cluster > kCandMaxCluster) return CE_EINVAL;
+        plan_candidates(p, rows, vocab, dev, f.cluster);
     } else if (op == kOpArgmax && (f.path == kPathFlat || (f.path == kPathAuto && f.cluster == 0 && f.threads == 0)) &&
                flat_applies(rows, vocab, dev, f.path == kPathFlat)) {
         p.path = kPathFlat;
@@ -295,9 +320,75 @@ int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t stride, co
     a.grad = grad;
     a.loss = loss_rows;
     a.top = top;
-    if (p.path == kPathRing) return cuda_status(launch_grad_ring(p, a, stream));
-    if (p.path == kPathStaged) return cuda_status(launch_grad_staged(p, a, stream));
-    return cuda_status(launch_grad_stream(p, a, stream));
+    return cuda_status(launch_fused(p, kOpGrad, a, stream));
+}
+
+// softmax_rows and log_softmax_rows: the fused kernels without labels.
+int normalised_rows(Op op, const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *out,
+                    ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (rows > 0 && out == nullptr) return CE_EINVAL;
+    if (misaligned(out, 4)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    const int64_t in_bytes = ((rows - 1) * stride + vocab) * 4;
+    const int64_t out_bytes = rows * vocab * 4;
+    if (out == logits) {
+        if (stride != vocab) return CE_EINVAL;  // in place needs the same layout
+    } else if (ranges_overlap(out, out_bytes, logits, in_bytes)) {
+        return CE_EINVAL;
+    }
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(op, rows, vocab, dev, &p))) return st;
+    Args a = make_args(logits, rows, vocab, stride, nullptr);
+    a.scale = 1.0f;
+    a.grad = out;
+    return cuda_status(launch_fused(p, op, a, stream));
+}
+
+int softmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *out, ce_stream_t stream) {
+    return normalised_rows(kOpSoftmax, logits, rows, vocab, stride, out, stream);
+}
+
+int log_softmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *out,
+                     ce_stream_t stream) {
+    return normalised_rows(kOpLogSoftmax, logits, rows, vocab, stride, out, stream);
+}
+
+int candidates_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *cand,
+                    ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (rows > 0 && cand == nullptr) return CE_EINVAL;
+    if (misaligned(cand, 4)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    if (ranges_overlap(cand, rows * int64_t(kCandRow) * 4, logits, ((rows - 1) * stride + vocab) * 4))
+        return CE_EINVAL;
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(kOpCandidates, rows, vocab, dev, &p))) return st;
+    Args a = make_args(logits, rows, vocab, stride, nullptr);
+    return cuda_status(launch_candidates(p, a, cand, stream));
+}
+
+int split_sum(float *y, const float *parts, int64_t total, int64_t splits, int add, ce_stream_t stream) {
+    if (total < 0 || splits < 1) return CE_EINVAL;
+    if (total > 0 && (y == nullptr || parts == nullptr)) return CE_EINVAL;
+    if (total > 0 && splits > (INT64_MAX / 4) / total) return CE_EINVAL;  // byte offsets fit int64
+    if (misaligned(y, 4) || misaligned(parts, 4)) return CE_EALIGN;
+    if (total == 0) return CE_OK;
+    // y may be part 0 itself (each element is read before it is written, by
+    // the same thread); any other overlap is rejected
+    if (y != parts && ranges_overlap(y, total * 4, parts, splits * total * 4)) return CE_EINVAL;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    const int64_t units = (total % 4 == 0) ? total / 4 : total;
+    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(ceil_div(units, kSplitThreads), 8 * int64_t(dev.sms)));
+    return cuda_status(launch_split_sum(y, parts, total, splits, add != 0, static_cast<int>(ctas), stream));
 }
 
 int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t stride) {
@@ -419,7 +510,7 @@ int ce_debug_force(int path, int cluster, int threads) {
 }
 
 int ce_plan(int op, int64_t rows, int64_t vocab, int64_t stride, int64_t out[6]) {
-    if (out == nullptr || op < 0 || op > 2) return CE_EINVAL;
+    if (out == nullptr || op < 0 || op > kOpCandidates) return CE_EINVAL;
     if (rows < 1 || vocab < 1 || vocab > kMaxVocab || stride < vocab) return CE_EINVAL;
     DeviceInfo dev;
     int st = current_device(&dev);

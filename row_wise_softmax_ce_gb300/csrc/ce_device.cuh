@@ -250,6 +250,15 @@ __device__ __forceinline__ float4 mul4(float4 v, float c) {
     return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// (v - m) - l lane by lane, two lanes per instruction: a log-softmax row
+// from its max m and l = log(sum).
+__device__ __forceinline__ float4 sub2_4(float4 v, float m, float l) {
+    const float2 nm = make_float2(-m, -m), nl = make_float2(-l, -l);
+    const float2 a = __fadd2_rn(__fadd2_rn(make_float2(v.x, v.y), nm), nl);
+    const float2 b = __fadd2_rn(__fadd2_rn(make_float2(v.z, v.w), nm), nl);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
 // Push four consecutive columns j..j+3. Common case: none of them exceeds the
 // running max m (and m is above -inf), so each adds exp(x - m) -- a tie adds
 // exactly 1 and keeps the first index, a NaN makes t NaN. Otherwise (a new

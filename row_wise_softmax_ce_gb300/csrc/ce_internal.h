@@ -8,7 +8,21 @@
 namespace cerows {
 
 enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2, kPathRing = 3, kPathStagedPerRow = 4, kPathFlat = 5 };
-enum Op : int { kOpRows = 0, kOpGrad = 1, kOpArgmax = 2 };
+enum Op : int { kOpRows = 0, kOpGrad = 1, kOpArgmax = 2, kOpSoftmax = 3, kOpLogSoftmax = 4, kOpCandidates = 5 };
+// What the fused two-pass kernels write from a row's (max, exp-sum) state.
+enum Mode : int { kModeGrad = 0, kModeSoftmax = 1, kModeLogSoftmax = 2 };
+
+// candidatesInto: a workgroup of 256 threads, each keeping its TOP_EACH = 4
+// largest values; a row's candidates are 2048 floats (value, token pairs).
+constexpr int kCandThreads = 256;
+constexpr int kTopEach = 4;
+constexpr int kCandRow = 2 * kCandThreads * kTopEach;
+constexpr int kCandMaxCluster = 8;
+// shared memory of the candidates kernel: the 4 thread groups' lists, and
+// (split rows) the lists the cluster's other CTAs send to CTA 0
+constexpr int kCandListBytes = kCandThreads * kTopEach * 8;  // one (value, column) list set
+constexpr int kCandMaxSmemBytes = 4 * kCandListBytes + kCandMaxCluster * kCandListBytes;
+constexpr int kSplitThreads = 256;
 
 // Per-CTA shared bytes the staged kernel reserves before its row buffer.
 constexpr int kStagedHeaderBytes = 2048;
@@ -56,9 +70,13 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev);
 cudaError_t max_active_clusters(const Plan &p, Op op, int *n);
 
 cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStream_t s);
-cudaError_t launch_grad_staged(const Plan &p, const Args &a, cudaStream_t s);
-cudaError_t launch_grad_stream(const Plan &p, const Args &a, cudaStream_t s);
-cudaError_t launch_grad_ring(const Plan &p, const Args &a, cudaStream_t s);
+// the two-pass kernels (staged, stream or ring, as p.path says) for kOpGrad,
+// kOpSoftmax or kOpLogSoftmax; the output row goes to a.grad
+cudaError_t launch_fused(const Plan &p, Op op, const Args &a, cudaStream_t s);
+// cand: rows * kCandRow floats
+cudaError_t launch_candidates(const Plan &p, const Args &a, float *cand, cudaStream_t s);
+cudaError_t launch_split_sum(float *y, const float *parts, int64_t total, int64_t splits, bool add, int ctas,
+                             cudaStream_t s);
 cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s);
 // argmax of few long rows split evenly over `ctas` CTAs; ws: 8 * (ctas + rows) bytes
 cudaError_t launch_argmax_flat(const Args &a, int ctas, void *ws, cudaStream_t s);

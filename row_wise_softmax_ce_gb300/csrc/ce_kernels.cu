@@ -178,7 +178,15 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
 //   write    grad = e * exp(m - M) * f32(1/(1 + T)) * scale (the label column
 //            less scale) range by range; as soon as a range is written the
 //            bulk copy of the next row's chunk into it starts.
+//
+// The same kernel writes two other rows of the same statistics (kMode):
+//   kModeSoftmax     out = e * exp(m - M) * f32(1/(1 + T)): no label, no scale;
+//   kModeLogSoftmax  out = (x - M) - log1p(T): sweep 2 sums e without storing
+//                    it, so the write reads x back from shared memory.
+template <int kMode>
 __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, int cols) {
+    constexpr bool kCE = kMode == kModeGrad;
+    constexpr bool kLog = kMode == kModeLogSoftmax;
     extern __shared__ __align__(128) unsigned char smem[];
     StagedHeader &h = *reinterpret_cast<StagedHeader *>(smem);
     float *buf = reinterpret_cast<float *>(smem + kStagedHeaderBytes);
@@ -239,9 +247,9 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         float4 edge0 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), edge1 = edge0;
         if (qe0 >= 0 && owner(qe0) == tid) edge0 = load_edge(p, off, n, qe0);
         if (qe1 >= 0 && owner(qe1) == tid) edge1 = load_edge(p, off, n, qe1);
-        const int64_t label = a.labels[row];
-        const bool lab_ok = label_valid(label, a.vocab);
-        const int lab_local = (lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
+        const int64_t label = kCE ? a.labels[row] : 0;
+        const bool lab_ok = !kCE || label_valid(label, a.vocab);
+        const int lab_local = (kCE && lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
         const int lab_f = lab_local >= 0 ? off + lab_local : -1;  // float index of the label
         const int lab_q = lab_f >> 2;
 
@@ -277,11 +285,11 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                 for (int q = c * W + tid; q < qend; q += T) {
                     const float4 e = exp4_sub(buf4[q], m);
                     acc = __fadd2_rn(acc, __fadd2_rn(make_float2(e.x, e.y), make_float2(e.z, e.w)));
-                    buf4[q] = e;
+                    if (!kLog) buf4[q] = e;
                 }
             }
             const float t = acc.x + acc.y;
-            buf[4 * qm + lm] = 1.0f;
+            buf[4 * qm + lm] = kLog ? m : 1.0f;
             st = RowState{m, t, jbase + 4 * qm + lm};
         } else {
             // no value above -inf among this thread's columns: the exact
@@ -294,7 +302,7 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                         const int i = 4 * q + l;
                         const float x = buf[i];
                         if (i >= off && i - off < n) push<true>(st, x, jbase + i);
-                        buf[i] = x != x ? x : 0.0f;
+                        if (!kLog) buf[i] = x != x ? x : 0.0f;
                     }
                 }
             }
@@ -312,8 +320,9 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
             if (tid == 0) {
                 const bool bad = !isfinite(g.m) || isnan(g.t);
                 h.bc[0] = g.m;
-                h.bc[1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);  // f32(1/sum)
-                if (rank == 0) {
+                // f32(1/sum), or for log-softmax log(sum) = log1p(T)
+                h.bc[1] = bad ? __int_as_float(0x7fffffff) : kLog ? log1pf(g.t) : 1.0f / (1.0f + g.t);
+                if (kCE && rank == 0) {
                     if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
                     if (!lab_ok) atomicAdd(&g_status[0], 1ull);
                     if (a.top) a.top[row] = row_token(g);
@@ -322,7 +331,7 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         }
         __syncthreads();
 
-        // the gradient, range by range; each freed range takes the next
+        // the output, range by range; each freed range takes the next
         // row's chunk
         const float M = h.bc[0], rcp = h.bc[1];
         const float shift = (m != -INFINITY && M != m) ? exp_le0(m - M) : 1.0f;
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         for (int c = 0; c < kChunks; ++c) {
             const int qend = min(nq, (c + 1) * W);
             for (int q = c * W + tid; q < qend; q += T) {
-                const float4 g = mul4(buf4[q], cm);
+                const float4 g = kLog ? sub2_4(buf4[q], M, rcp) : mul4(buf4[q], cm);
                 if (vec_store && static_cast<unsigned>(q - qa) < static_cast<unsigned>(nvec)) {
                     __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
                 } else {
@@ -371,7 +380,10 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
 // k_grad_stream: fused loss + gradient for rows too long to stage; the
 // cluster's CTAs read their slices twice (state, then gradient) and meet by
 // pushes.
+template <int kMode>
 __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, int cols) {
+    constexpr bool kCE = kMode == kModeGrad;
+    constexpr bool kLog = kMode == kModeLogSoftmax;
     __shared__ RowState red[32];
     __shared__ PushXchg xg;
     __shared__ float bc[2];
@@ -390,9 +402,9 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
     int64_t k = 0;
     for (int64_t row = cid; row < a.rows; row += G, ++k) {
         const float *p = a.logits + row * a.stride + c0;
-        const int64_t label = a.labels[row];
-        const bool lab_ok = label_valid(label, a.vocab);
-        const int lab_local = (lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
+        const int64_t label = kCE ? a.labels[row] : 0;
+        const bool lab_ok = !kCE || label_valid(label, a.vocab);
+        const int lab_local = (kCE && lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
         // x[label] is read before any CTA of the cluster writes (grad may alias logits)
         const float xl_own = (tid == 0 && lab_local >= 0) ? p[lab_local] : 0.0f;
         RowState st = empty_state();
@@ -406,8 +418,8 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
             if (tid == 0) {
                 const bool bad = !isfinite(g.m) || isnan(g.t);
                 bc[0] = g.m;
-                bc[1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);
-                if (rank == 0) {
+                bc[1] = bad ? __int_as_float(0x7fffffff) : kLog ? log1pf(g.t) : 1.0f / (1.0f + g.t);
+                if (kCE && rank == 0) {
                     if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
                     if (!lab_ok) atomicAdd(&g_status[0], 1ull);
                     if (a.top) a.top[row] = row_token(g);
@@ -419,8 +431,13 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
         float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;
         // coherent loads: with grad == logits this thread writes what it read
         for (int kk = tid; kk < n; kk += T) {
-            const float pr = exp_le0(__ldcs(p + kk) - M) * rcp;
-            __stcs(gp + kk, (kk == lab_local ? pr - 1.0f : pr) * scale);
+            const float x = __ldcs(p + kk);
+            if (kLog) {
+                __stcs(gp + kk, (x - M) - rcp);
+            } else {
+                const float pr = exp_le0(x - M) * rcp;
+                __stcs(gp + kk, (kk == lab_local ? pr - 1.0f : pr) * scale);
+            }
         }
         __syncthreads();  // bc and red are rewritten for the next row
     }
@@ -825,6 +842,255 @@ __global__ void k_argmax_combine(Args a, const uint64_t *__restrict__ ws, int P)
 }
 
 // ---------------------------------------------------------------------------
+// Sampling candidates (candidatesInto; constants TOP_EACH and CANDIDATE_ROW).
+//
+// What is computed: a workgroup of 256 threads reads each row; thread t reads
+// columns t, t + 256, t + 512, ... and keeps its 4 largest values, ranked by
+// value and then by the lower column (NaN is never kept). Row i's output is
+// 2048 floats at cand + 2048 i: pair 4t + k is thread t's rank-k (value,
+// column as f32), (-inf, -1) where the thread read fewer than 4 values.
+//
+// How: a CTA of 256 threads is 4 groups of 64, and a cluster of C CTAs shares
+// a row. The row is read as 16-byte vectors from the 16-byte boundary at or
+// below its start (off = the start's offset in floats): vector q holds
+// columns 4q - off ... 4q - off + 3. As 256 columns are 64 vectors, vector
+// q = 64 n + u always holds columns of the logical threads (4u + k - off) mod
+// 256, k = 0..3, so physical thread u of group G (of the cluster's 4C) reads
+// the blocks n = G, G + 4C, ... and keeps one list per lane k. The lists then
+// meet: the CTA's 4 groups through shared memory, the cluster's CTAs in CTA 0
+// through distributed shared memory; CTA 0 writes the row.
+namespace cand {
+
+constexpr int kUnrollC = 4;                 // 16-byte loads in flight per thread
+constexpr int kEmptyCol = 0x7fffffff;       // a slot without a value ranks last
+constexpr int kGroups = kCandThreads / 64;  // groups of 64 threads in a CTA
+
+struct TopList {
+    float v[kTopEach];
+    int c[kTopEach];
+};
+
+__device__ __forceinline__ void top_init(TopList &L) {
+#pragma unroll
+    for (int k = 0; k < kTopEach; ++k) {
+        L.v[k] = -INFINITY;
+        L.c[k] = kEmptyCol;
+    }
+}
+
+// (v1, c1) ranks above (v2, c2): a larger value, or an equal one at a lower
+// column. Any comparison with a NaN value is false.
+__device__ __forceinline__ bool ranks_above(float v1, int c1, float v2, int c2) {
+    return v1 > v2 || (v1 == v2 && c1 < c2);
+}
+
+// Keep (x, col) if it ranks above the list's last slot; the list stays sorted.
+__device__ __forceinline__ void top_push(TopList &L, float x, int col) {
+    if (!ranks_above(x, col, L.v[3], L.c[3])) return;
+    const bool a0 = ranks_above(L.v[0], L.c[0], x, col);
+    const bool a1 = ranks_above(L.v[1], L.c[1], x, col);
+    const bool a2 = ranks_above(L.v[2], L.c[2], x, col);
+    const float v0 = L.v[0], v1 = L.v[1], v2 = L.v[2];
+    const int c0 = L.c[0], c1 = L.c[1], c2 = L.c[2];
+    L.v[3] = a2 ? x : v2;
+    L.c[3] = a2 ? col : c2;
+    L.v[2] = a2 ? v2 : (a1 ? x : v1);
+    L.c[2] = a2 ? c2 : (a1 ? col : c1);
+    L.v[1] = a1 ? v1 : (a0 ? x : v0);
+    L.c[1] = a1 ? c1 : (a0 ? col : c0);
+    L.v[0] = a0 ? v0 : x;
+    L.c[0] = a0 ? c0 : col;
+}
+
+__device__ __forceinline__ float2 slot_of(const TopList &L, int k) {
+    return make_float2(L.v[k], __int_as_float(L.c[k]));
+}
+
+__device__ __forceinline__ void push_slot(TopList &L, float2 e) { top_push(L, e.x, __float_as_int(e.y)); }
+
+// 16-byte vector q of a row (p -> column 0, off = p's offset in floats within
+// 16 bytes): columns 4q - off ... +3, NaN (never kept) outside [0, vocab).
+__device__ __forceinline__ float4 load_vec(const float *p, int off, int vocab, int q, int qlo, int qhi) {
+    if (q >= qlo && q < qhi) return ld_stream_f4(reinterpret_cast<const float4 *>(p - off) + q);
+    float v[4];
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+        const int col = 4 * q - off + l;
+        v[l] = (col >= 0 && col < vocab) ? ld_stream_f1(p + col) : __int_as_float(0x7fffffff);
+    }
+    return make_float4(v[0], v[1], v[2], v[3]);
+}
+
+__device__ __forceinline__ float lane4(float4 v, int l) { return l == 0 ? v.x : l == 1 ? v.y : l == 2 ? v.z : v.w; }
+
+__device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float2 v) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+}  // namespace cand
+
+// Dynamic shared memory: S, 4 groups x 4 ranks x 256 logical threads of
+// (value, column) float2; then X, the merged lists of CTAs 1..C-1 of the
+// cluster (in CTA 0 only), C - 1 x 4 x 256 float2.
+__global__ void __launch_bounds__(kCandThreads, 3) k_candidates(Args a, float *__restrict__ out) {
+    using namespace cand;
+    extern __shared__ __align__(16) unsigned char smem[];
+    float2 *S = reinterpret_cast<float2 *>(smem);
+    float2 *X = S + kGroups * kTopEach * kCandThreads;
+    const uint32_t rank = cluster_rank(), C = cluster_size();
+    const int tid = threadIdx.x, u = tid & 63, grp = tid >> 6;
+    const int G = static_cast<int>(rank) * kGroups + grp, NG = static_cast<int>(C) * kGroups;
+    const int64_t cid = cluster_id_x(), GC = cluster_count_x();
+    const bool vec_out = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+    if (C > 1) cluster_arrive();  // matched before the first write to CTA 0
+    for (int64_t row = cid; row < a.rows; row += GC) {
+        const float *p = a.logits + row * a.stride;
+        const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+        const int nq = (a.vocab + off + 3) >> 2;  // vectors covering the row
+        const int qlo = off ? 1 : 0, qhi = (a.vocab + off) >> 2;  // whole vectors: [qlo, qhi)
+        const int nb = (nq + 63) >> 6;            // blocks of 64 vectors (256 columns)
+        TopList L[4];
+#pragma unroll
+        for (int l = 0; l < 4; ++l) top_init(L[l]);
+        for (int n0 = G; n0 < nb; n0 += NG * kUnrollC) {
+            float4 v[kUnrollC];
+#pragma unroll
+            for (int i = 0; i < kUnrollC; ++i) {
+                const int q = 64 * (n0 + i * NG) + u;
+                v[i] = q < nq ? load_vec(p, off, a.vocab, q, qlo, qhi)
+                              : make_float4(__int_as_float(0x7fffffff), 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < kUnrollC; ++i) {
+                const int q = 64 * (n0 + i * NG) + u;
+                if (q < nq) {
+#pragma unroll
+                    for (int l = 0; l < 4; ++l) top_push(L[l], lane4(v[i], l), 4 * q - off + l);
+                }
+            }
+        }
+        // the CTA's 4 groups: S[grp][k][t], t the logical thread of the list
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            const int t = (4 * u + l - off) & (kCandThreads - 1);
+#pragma unroll
+            for (int k = 0; k < kTopEach; ++k) S[(grp * kTopEach + k) * kCandThreads + t] = slot_of(L[l], k);
+        }
+        __syncthreads();
+        TopList M;
+        const int t = tid;  // from here on, thread t merges logical thread t's lists
+#pragma unroll
+        for (int k = 0; k < kTopEach; ++k) {
+            const float2 e = S[k * kCandThreads + t];
+            M.v[k] = e.x;
+            M.c[k] = __float_as_int(e.y);
+        }
+#pragma unroll
+        for (int g = 1; g < kGroups; ++g)
+#pragma unroll
+            for (int k = 0; k < kTopEach; ++k) push_slot(M, S[(g * kTopEach + k) * kCandThreads + t]);
+        if (C > 1) {
+            cluster_wait();  // CTA 0 is running, and (later rows) done with X
+            if (rank != 0) {
+                const uint32_t x0 = peer_smem(X, 0u);
+#pragma unroll
+                for (int k = 0; k < kTopEach; ++k)
+                    st_dsmem_f2(x0 + 8u * static_cast<uint32_t>(((rank - 1) * kTopEach + k) * kCandThreads + t),
+                                slot_of(M, k));
+            }
+            cluster_arrive_release();
+            cluster_wait();
+            if (rank == 0)
+                for (uint32_t r = 1; r < C; ++r)
+#pragma unroll
+                    for (int k = 0; k < kTopEach; ++k) push_slot(M, X[((r - 1) * kTopEach + k) * kCandThreads + t]);
+            cluster_arrive_release();  // X and S may be rewritten once every CTA is past here
+        } else {
+            __syncthreads();  // S is rewritten for the next row
+        }
+        if (rank == 0) {
+            float o[8];
+#pragma unroll
+            for (int k = 0; k < kTopEach; ++k) {
+                const bool empty = M.c[k] == kEmptyCol;
+                o[2 * k] = empty ? -INFINITY : M.v[k];
+                o[2 * k + 1] = empty ? -1.0f : static_cast<float>(M.c[k]);
+            }
+            float *dst = out + row * static_cast<int64_t>(kCandRow) + 8 * t;
+            if (vec_out) {
+                __stcs(reinterpret_cast<float4 *>(dst), make_float4(o[0], o[1], o[2], o[3]));
+                __stcs(reinterpret_cast<float4 *>(dst) + 1, make_float4(o[4], o[5], o[6], o[7]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) __stcs(dst + i, o[i]);
+            }
+        }
+    }
+    if (C > 1) cluster_wait();  // the last arrive's match: no CTA leaves before its peers
+}
+
+// ---------------------------------------------------------------------------
+// Split sums (splitSumInto): y[i] = (add ? y[i] : 0) + parts[0][i] + ... +
+// parts[splits - 1][i], part s at parts + s * total, added in f32 in split
+// order. A grid-stride loop over 16-byte vectors (kVec) or single floats;
+// each thread keeps several parts' loads in flight. Loads and stores are
+// coherent: y may be parts[0] itself.
+constexpr int kSplitUnroll = 4;
+
+template <bool kVec>
+__global__ void __launch_bounds__(kSplitThreads) k_split_sum(float *__restrict__ y, const float *parts, int64_t total,
+                                                            int64_t splits, bool add) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (kVec) {
+        const int64_t nv = total / 4;
+        float4 *yv = reinterpret_cast<float4 *>(y);
+        const float4 *pv = reinterpret_cast<const float4 *>(parts);
+        for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nv; i += stride) {
+            float4 acc = add ? __ldcs(yv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            int64_t sp = 0;
+            for (; sp + kSplitUnroll <= splits; sp += kSplitUnroll) {
+                float4 v[kSplitUnroll];
+#pragma unroll
+                for (int k = 0; k < kSplitUnroll; ++k) v[k] = __ldcs(pv + (sp + k) * nv + i);
+#pragma unroll
+                for (int k = 0; k < kSplitUnroll; ++k) {
+                    acc.x += v[k].x;
+                    acc.y += v[k].y;
+                    acc.z += v[k].z;
+                    acc.w += v[k].w;
+                }
+            }
+            for (; sp < splits; ++sp) {
+                const float4 v = __ldcs(pv + sp * nv + i);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            __stcs(yv + i, acc);
+        }
+    } else {
+        for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total; i += stride) {
+            float acc = add ? __ldcs(y + i) : 0.0f;
+            int64_t sp = 0;
+            for (; sp + kSplitUnroll <= splits; sp += kSplitUnroll) {
+                float v[kSplitUnroll];
+#pragma unroll
+                for (int k = 0; k < kSplitUnroll; ++k) v[k] = __ldcs(parts + (sp + k) * total + i);
+#pragma unroll
+                for (int k = 0; k < kSplitUnroll; ++k) acc += v[k];
+            }
+            for (; sp < splits; ++sp) acc += __ldcs(parts + sp * total + i);
+            __stcs(y + i, acc);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // k_mean: one CTA. Thread k sums rows k, k + T, ... in f64; a butterfly over
 // each warp, then over the warps' sums. Fixed shape: same bits every run.
 __global__ void __launch_bounds__(1024) k_mean(const float *__restrict__ loss, int64_t rows,
@@ -861,12 +1127,20 @@ cudaError_t launch_clustered(const void *fn, const Plan &p, void **args, cudaStr
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+template <int kMode>
+const void *fused_kernel(int path) {
+    return path == kPathStaged ? reinterpret_cast<const void *>(&k_grad_staged<kMode>)
+                               : reinterpret_cast<const void *>(&k_grad_stream<kMode>);
+}
+
 const void *kernel_of(const Plan &p, Op op) {
     if (op == kOpGrad) {
         if (p.path == kPathRing) return reinterpret_cast<const void *>(&k_grad_ring);
-        return p.path == kPathStaged ? reinterpret_cast<const void *>(&k_grad_staged)
-                                     : reinterpret_cast<const void *>(&k_grad_stream);
+        return fused_kernel<kModeGrad>(p.path);
     }
+    if (op == kOpSoftmax) return fused_kernel<kModeSoftmax>(p.path);
+    if (op == kOpLogSoftmax) return fused_kernel<kModeLogSoftmax>(p.path);
+    if (op == kOpCandidates) return reinterpret_cast<const void *>(&k_candidates);
     if (op == kOpRows) return reinterpret_cast<const void *>(&k_rows_stream<true>);
     return reinterpret_cast<const void *>(&k_rows_stream<false>);
 }
@@ -876,15 +1150,27 @@ const void *kernel_of(const Plan &p, Op op) {
 cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
     const void *fns[] = {reinterpret_cast<const void *>(&k_rows_stream<true>),
                          reinterpret_cast<const void *>(&k_rows_stream<false>),
-                         reinterpret_cast<const void *>(&k_grad_staged),
-                         reinterpret_cast<const void *>(&k_grad_stream),
-                         reinterpret_cast<const void *>(&k_grad_ring)};
+                         reinterpret_cast<const void *>(&k_grad_staged<kModeGrad>),
+                         reinterpret_cast<const void *>(&k_grad_staged<kModeSoftmax>),
+                         reinterpret_cast<const void *>(&k_grad_staged<kModeLogSoftmax>),
+                         reinterpret_cast<const void *>(&k_grad_stream<kModeGrad>),
+                         reinterpret_cast<const void *>(&k_grad_stream<kModeSoftmax>),
+                         reinterpret_cast<const void *>(&k_grad_stream<kModeLogSoftmax>),
+                         reinterpret_cast<const void *>(&k_grad_ring),
+                         reinterpret_cast<const void *>(&k_candidates)};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_grad_staged),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
+    const void *staged[] = {reinterpret_cast<const void *>(&k_grad_staged<kModeGrad>),
+                            reinterpret_cast<const void *>(&k_grad_staged<kModeSoftmax>),
+                            reinterpret_cast<const void *>(&k_grad_staged<kModeLogSoftmax>)};
+    for (const void *f : staged) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
+        if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_candidates),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kCandMaxSmemBytes);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_grad_ring),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
@@ -912,25 +1198,29 @@ cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStr
     return launch_clustered(kernel_of(p, stats ? kOpRows : kOpArgmax), p, args, s);
 }
 
-cudaError_t launch_grad_staged(const Plan &p, const Args &a, cudaStream_t s) {
+cudaError_t launch_fused(const Plan &p, Op op, const Args &a, cudaStream_t s) {
     Args aa = a;
     int cols = p.cols;
     void *args[] = {&aa, &cols};
-    return launch_clustered(reinterpret_cast<const void *>(&k_grad_staged), p, args, s);
+    return launch_clustered(kernel_of(p, op), p, args, s);
 }
 
-cudaError_t launch_grad_ring(const Plan &p, const Args &a, cudaStream_t s) {
+cudaError_t launch_candidates(const Plan &p, const Args &a, float *cand, cudaStream_t s) {
     Args aa = a;
-    int cols = p.cols;
-    void *args[] = {&aa, &cols};
-    return launch_clustered(reinterpret_cast<const void *>(&k_grad_ring), p, args, s);
+    float *cc = cand;
+    void *args[] = {&aa, &cc};
+    return launch_clustered(reinterpret_cast<const void *>(&k_candidates), p, args, s);
 }
 
-cudaError_t launch_grad_stream(const Plan &p, const Args &a, cudaStream_t s) {
-    Args aa = a;
-    int cols = p.cols;
-    void *args[] = {&aa, &cols};
-    return launch_clustered(reinterpret_cast<const void *>(&k_grad_stream), p, args, s);
+cudaError_t launch_split_sum(float *y, const float *parts, int64_t total, int64_t splits, bool add, int ctas,
+                             cudaStream_t s) {
+    const bool vec = total % 4 == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0 &&
+                     (reinterpret_cast<uintptr_t>(parts) & 15) == 0;
+    if (vec)
+        k_split_sum<true><<<ctas, kSplitThreads, 0, s>>>(y, parts, total, splits, add);
+    else
+        k_split_sum<false><<<ctas, kSplitThreads, 0, s>>>(y, parts, total, splits, add);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_argmax_flat(const Args &a, int ctas, void *ws, cudaStream_t s) {

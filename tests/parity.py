@@ -6,6 +6,12 @@ Tolerances (element by element, CUDA path vs the f64 CPU oracle):
   mean loss      relative 1e-6
   gradient       absolute 1e-6
   argmax token   exact
+  softmax row    absolute 1e-6 (the gradient's: the same kernel and arithmetic)
+  log-softmax    relative 2e-5 (the loss's: it shares one log1pf of the same
+                 sum and one rounded subtraction per element)
+  candidates     exact, bit for bit (values are copies of the logits)
+  split sums     the f32 recursive-summation bound, per element:
+                 (terms - 1) * 2^-24 * sum of |terms| (and 2^-149, one denormal)
 A NaN must meet a NaN, and an infinity the same infinity.
 """
 from __future__ import annotations
@@ -77,3 +83,49 @@ def assert_tokens(got, ref, what="argmax"):
     if bad.any():
         k = int(np.argmax(bad))
         raise AssertionError(f"{what}: row {k}: got {int(got[k])}, ref {ref[k]} ({int(bad.sum())} rows differ)")
+
+
+LOGP_REL = LOSS_REL
+SOFTMAX_ABS = GRAD_ABS
+
+
+def assert_softmax(got, ref, what="softmax"):
+    """Softmax rows: the gradient's absolute tolerance."""
+    assert_grad(got, ref, what)
+
+
+def assert_log_softmax(got, ref, what="log-softmax"):
+    """Log-softmax rows: the loss's relative tolerance."""
+    assert_loss(got, ref, what)
+
+
+def assert_candidates(got, ref, what="candidates"):
+    """Candidate rows: equal bit for bit."""
+    g = np.ascontiguousarray(got.detach().cpu().numpy() if isinstance(got, torch.Tensor) else got,
+                             dtype=np.float32)
+    r = np.ascontiguousarray(ref, dtype=np.float32)
+    assert g.shape == r.shape, f"{what}: shape {g.shape} != {r.shape}"
+    bad = g.view(np.int32) != r.view(np.int32)
+    if bad.any():
+        k = int(np.argmax(bad.ravel()))
+        row, f = divmod(k, g.shape[-1])
+        t, rest = divmod(f, 8)
+        raise AssertionError(f"{what}: row {row} thread {t} float {rest}: got {g.ravel()[k]!r}, "
+                             f"ref {r.ravel()[k]!r} ({int(bad.sum())} floats differ)")
+
+
+def assert_split_sum(got, ref, y, parts, add, what="split_sum"):
+    """Split sums against the f64 oracle, within the f32 summation bound."""
+    got, ref = _np(got), _np(ref)
+    p = np.asarray(parts, dtype=np.float64)
+    mag = np.abs(p).sum(axis=0)
+    terms = p.shape[0]
+    if add:
+        mag = mag + np.abs(np.asarray(y, dtype=np.float64))
+        terms += 1
+    fin = _same_specials(got, ref, what)
+    tol = max(terms - 1, 1) * 2.0 ** -24 * mag + 2.0 ** -149
+    err = np.abs(got - ref)
+    if (err[fin] > tol[fin]).any():
+        k = int(np.argmax(np.where(fin, err / tol, 0)))
+        raise AssertionError(f"{what}: element {k}: got {got[k]!r}, ref {ref[k]!r}, bound {tol[k]:.3e}")

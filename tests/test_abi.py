@@ -20,7 +20,8 @@ def test_exports_every_declared_function(lib):
     assert set(names) >= {"ce_rows", "ce_mean", "ce_loss", "ce_grad", "argmax_rows", "argmax_workspace_bytes",
                           "ce_status_string",
                           "ce_version", "ce_last_cuda_error", "ce_device_error_count",
-                          "ce_device_error_reset", "ce_debug_force", "ce_plan"}
+                          "ce_device_error_reset", "ce_debug_force", "ce_plan", "softmax_rows",
+                          "log_softmax_rows", "candidates_rows", "split_sum", "argmax_rows_noalloc"}
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, f"declared but not exported: {missing}"
 
@@ -29,8 +30,7 @@ def test_only_declared_functions_are_exported(lib):
     import subprocess
     out = subprocess.run(["nm", "-D", "--defined-only", ce.LIB_PATH], capture_output=True, text=True).stdout
     exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
-    ours = {n for n in exported if n.startswith(("ce_", "argmax_"))}
-    assert ours == set(ce.declared_functions()), ours ^ set(ce.declared_functions())
+    assert exported == set(ce.declared_functions()), exported ^ set(ce.declared_functions())
 
 
 def test_version_and_status_strings(lib):
@@ -54,6 +54,8 @@ def test_bad_sizes_rejected_before_launch(lib, args):
     assert lib.ce_rows(logits, rows, vocab, stride, V(512), V(1024), None) == ce.CE_EINVAL
     assert lib.argmax_rows(logits, rows, vocab, stride, V(1024), None, 0, None) == ce.CE_EINVAL
     assert lib.ce_grad(logits, rows, vocab, stride, V(512), 1.0, V(4096), None, None, None) == ce.CE_EINVAL
+    for fn in (lib.softmax_rows, lib.log_softmax_rows, lib.candidates_rows):
+        assert fn(logits, rows, vocab, stride, V(1 << 20), None) == ce.CE_EINVAL
 
 
 def test_misaligned_pointers_rejected(lib):
@@ -81,6 +83,31 @@ def test_grad_overlap_rules(lib):
     # in place needs stride == vocab; a partial overlap is rejected
     assert lib.ce_grad(V(4096), 4, 10, 12, V(512), 1.0, V(4096), None, None, None) == ce.CE_EINVAL
     assert lib.ce_grad(V(4096), 4, 10, 10, V(512), 1.0, V(4100), None, None, None) == ce.CE_EINVAL
+
+
+def test_rows_beside_the_loss_validation(lib):
+    for fn in (lib.softmax_rows, lib.log_softmax_rows, lib.candidates_rows):
+        assert fn(V(256), 4, 10, 10, None, None) == ce.CE_EINVAL          # no output
+        assert fn(V(256), 4, 10, 10, V(1 << 20 | 2), None) == ce.CE_EALIGN
+        assert fn(None, 0, 10, 10, None, None) == ce.CE_OK                # nothing launched
+    # in place needs stride == vocab; any partial overlap is rejected
+    assert lib.softmax_rows(V(4096), 4, 10, 12, V(4096), None) == ce.CE_EINVAL
+    assert lib.log_softmax_rows(V(4096), 4, 10, 10, V(4100), None) == ce.CE_EINVAL
+    # candidates never alias the logits
+    assert lib.candidates_rows(V(4096), 4, 10, 10, V(4096), None) == ce.CE_EINVAL
+    assert lib.candidates_rows(V(1 << 20), 2, 10, 10, V((1 << 20) - 2 * 8192 + 16), None) == ce.CE_EINVAL
+
+
+def test_split_sum_validation(lib):
+    assert lib.split_sum(V(256), V(1 << 20), 10, 0, 0, None) == ce.CE_EINVAL     # splits < 1
+    assert lib.split_sum(V(256), V(1 << 20), -1, 2, 0, None) == ce.CE_EINVAL     # total < 0
+    assert lib.split_sum(None, V(1 << 20), 10, 2, 0, None) == ce.CE_EINVAL
+    assert lib.split_sum(V(256), None, 10, 2, 1, None) == ce.CE_EINVAL
+    assert lib.split_sum(V(258), V(1 << 20), 10, 2, 0, None) == ce.CE_EALIGN
+    assert lib.split_sum(V(256), V(1 << 20), (1 << 62), 4, 0, None) == ce.CE_EINVAL  # bytes overflow
+    # y inside the parts but not part 0 itself
+    assert lib.split_sum(V(4096 + 40), V(4096), 10, 2, 0, None) == ce.CE_EINVAL
+    assert lib.split_sum(None, None, 0, 3, 1, None) == ce.CE_OK                    # nothing launched
 
 
 def test_zero_rows_is_a_no_op_without_device(lib):
