@@ -386,9 +386,7 @@ int split_sum(float *y, const float *parts, int64_t total, int64_t splits, int a
     DeviceInfo dev;
     int st = current_device(&dev);
     if (st) return st;
-    const int64_t units = (total % 4 == 0) ? total / 4 : total;
-    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>(ceil_div(units, kSplitThreads), 8 * int64_t(dev.sms)));
-    return cuda_status(launch_split_sum(y, parts, total, splits, add != 0, static_cast<int>(ctas), stream));
+    return cuda_status(launch_split_sum(y, parts, total, splits, add != 0, dev.sms, stream));
 }
 
 int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t stride) {

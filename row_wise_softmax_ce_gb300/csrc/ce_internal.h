@@ -75,7 +75,8 @@ cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStr
 cudaError_t launch_fused(const Plan &p, Op op, const Args &a, cudaStream_t s);
 // cand: rows * kCandRow floats
 cudaError_t launch_candidates(const Plan &p, const Args &a, float *cand, cudaStream_t s);
-cudaError_t launch_split_sum(float *y, const float *parts, int64_t total, int64_t splits, bool add, int ctas,
+// one resident wave on a device of `sms` SMs
+cudaError_t launch_split_sum(float *y, const float *parts, int64_t total, int64_t splits, bool add, int sms,
                              cudaStream_t s);
 cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s);
 // argmax of few long rows split evenly over `ctas` CTAs; ws: 8 * (ctas + rows) bytes

@@ -25,6 +25,7 @@
 //
 // Every kernel loops over rows (row = cluster id, + number of clusters), so
 // any row count fits one launch.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -902,6 +903,26 @@ __device__ __forceinline__ void top_push(TopList &L, float x, int col) {
     L.c[0] = a0 ? c0 : col;
 }
 
+// The scan's insertion: x at column col, later than every column the list
+// holds, so an equal value never displaces a kept one. Branch-free (four
+// compares, fourteen selects): with 128 lists per warp some lane almost
+// always inserts, so a branch would not skip. Strict compares keep out NaN,
+// and also -inf (it ties an empty slot's -inf): a list left with empty slots
+// takes its -inf columns after the scan.
+__device__ __forceinline__ void stream_push(TopList &L, float x, int col) {
+    const bool p0 = x > L.v[0], p1 = x > L.v[1], p2 = x > L.v[2], p3 = x > L.v[3];
+    const float v0 = L.v[0], v1 = L.v[1], v2 = L.v[2];
+    const int c0 = L.c[0], c1 = L.c[1], c2 = L.c[2];
+    L.v[3] = p2 ? v2 : (p3 ? x : L.v[3]);
+    L.c[3] = p2 ? c2 : (p3 ? col : L.c[3]);
+    L.v[2] = p1 ? v1 : (p2 ? x : v2);
+    L.c[2] = p1 ? c1 : (p2 ? col : c2);
+    L.v[1] = p0 ? v0 : (p1 ? x : v1);
+    L.c[1] = p0 ? c0 : (p1 ? col : c1);
+    L.v[0] = p0 ? x : v0;
+    L.c[0] = p0 ? col : c0;
+}
+
 __device__ __forceinline__ float2 slot_of(const TopList &L, int k) {
     return make_float2(L.v[k], __int_as_float(L.c[k]));
 }
@@ -969,8 +990,25 @@ __global__ void __launch_bounds__(kCandThreads, 3) k_candidates(Args a, float *_
                 const int q = 64 * (n0 + i * NG) + u;
                 if (q < nq) {
 #pragma unroll
-                    for (int l = 0; l < 4; ++l) top_push(L[l], lane4(v[i], l), 4 * q - off + l);
+                    for (int l = 0; l < 4; ++l) stream_push(L[l], lane4(v[i], l), 4 * q - off + l);
                 }
+            }
+        }
+        // a list with an empty slot takes, in column order, its columns that
+        // hold -inf (the scan kept every larger value already)
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            if (L[l].c[3] != kEmptyCol) continue;
+            int r = 0;
+#pragma unroll
+            for (int k = 0; k < kTopEach; ++k) r += L[l].c[k] != kEmptyCol;
+            for (int n = G; n < nb && r < kTopEach; n += NG) {
+                const int col = 4 * (64 * n + u) - off + l;
+                if (col < 0 || col >= a.vocab || p[col] != -INFINITY) continue;
+#pragma unroll
+                for (int k = 0; k < kTopEach; ++k)
+                    if (k == r) L[l].c[k] = col;  // its value is already -inf
+                ++r;
             }
         }
         // the CTA's 4 groups: S[grp][k][t], t the logical thread of the list
@@ -1036,57 +1074,82 @@ __global__ void __launch_bounds__(kCandThreads, 3) k_candidates(Args a, float *_
 // ---------------------------------------------------------------------------
 // Split sums (splitSumInto): y[i] = (add ? y[i] : 0) + parts[0][i] + ... +
 // parts[splits - 1][i], part s at parts + s * total, added in f32 in split
-// order. A grid-stride loop over 16-byte vectors (kVec) or single floats;
-// each thread keeps several parts' loads in flight. Loads and stores are
+// order. One resident wave of CTAs in a grid-stride loop over 16-byte
+// vectors (kVec) or single floats; each thread sums two units per step, and
+// keeps their loads of several parts in flight. Loads and stores are
 // coherent: y may be parts[0] itself.
 constexpr int kSplitUnroll = 4;
+
+__device__ __forceinline__ void acc_add(float &a, float b) { a += b; }
+__device__ __forceinline__ void acc_add(float4 &a, const float4 &b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+
+template <typename T>
+__device__ __forceinline__ T zero_of() {
+    return T{};
+}
+template <>
+__device__ __forceinline__ float4 zero_of<float4>() {
+    return make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// y[i] and y[j] (j = i + blockDim, when j < n) from their `splits` parts
+template <typename T>
+__device__ __forceinline__ void split_pair(T *__restrict__ y, const T *p, int64_t n, int64_t splits, bool add,
+                                           int64_t i, int64_t j) {
+    const bool two = j < n;
+    T a = add ? __ldcs(y + i) : zero_of<T>();
+    T b = (add && two) ? __ldcs(y + j) : zero_of<T>();
+    int64_t sp = 0;
+    for (; sp + kSplitUnroll <= splits; sp += kSplitUnroll) {
+        T va[kSplitUnroll], vb[kSplitUnroll];
+#pragma unroll
+        for (int k = 0; k < kSplitUnroll; ++k) {
+            va[k] = __ldcs(p + (sp + k) * n + i);
+            vb[k] = two ? __ldcs(p + (sp + k) * n + j) : zero_of<T>();
+        }
+#pragma unroll
+        for (int k = 0; k < kSplitUnroll; ++k) {
+            acc_add(a, va[k]);
+            acc_add(b, vb[k]);
+        }
+    }
+    // the last splits % 4 parts, all loads first
+    const int rest = static_cast<int>(splits - sp);
+    T va[kSplitUnroll - 1], vb[kSplitUnroll - 1];
+#pragma unroll
+    for (int k = 0; k < kSplitUnroll - 1; ++k) {
+        va[k] = k < rest ? __ldcs(p + (sp + k) * n + i) : zero_of<T>();
+        vb[k] = (k < rest && two) ? __ldcs(p + (sp + k) * n + j) : zero_of<T>();
+    }
+#pragma unroll
+    for (int k = 0; k < kSplitUnroll - 1; ++k) {
+        if (k < rest) {
+            acc_add(a, va[k]);
+            acc_add(b, vb[k]);
+        }
+    }
+    __stcs(y + i, a);
+    if (two) __stcs(y + j, b);
+}
 
 template <bool kVec>
 __global__ void __launch_bounds__(kSplitThreads) k_split_sum(float *__restrict__ y, const float *parts, int64_t total,
                                                             int64_t splits, bool add) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    // CTA b takes units [2 T b, 2 T b + 2 T) of each grid step: i and i + T
+    const int64_t T = blockDim.x, step = 2 * T * gridDim.x;
     if (kVec) {
-        const int64_t nv = total / 4;
-        float4 *yv = reinterpret_cast<float4 *>(y);
-        const float4 *pv = reinterpret_cast<const float4 *>(parts);
-        for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < nv; i += stride) {
-            float4 acc = add ? __ldcs(yv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            int64_t sp = 0;
-            for (; sp + kSplitUnroll <= splits; sp += kSplitUnroll) {
-                float4 v[kSplitUnroll];
-#pragma unroll
-                for (int k = 0; k < kSplitUnroll; ++k) v[k] = __ldcs(pv + (sp + k) * nv + i);
-#pragma unroll
-                for (int k = 0; k < kSplitUnroll; ++k) {
-                    acc.x += v[k].x;
-                    acc.y += v[k].y;
-                    acc.z += v[k].z;
-                    acc.w += v[k].w;
-                }
-            }
-            for (; sp < splits; ++sp) {
-                const float4 v = __ldcs(pv + sp * nv + i);
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
-            }
-            __stcs(yv + i, acc);
-        }
+        const int64_t n = total / 4;
+        for (int64_t i = 2 * T * blockIdx.x + threadIdx.x; i < n; i += step)
+            split_pair(reinterpret_cast<float4 *>(y), reinterpret_cast<const float4 *>(parts), n, splits, add, i,
+                       i + T);
     } else {
-        for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total; i += stride) {
-            float acc = add ? __ldcs(y + i) : 0.0f;
-            int64_t sp = 0;
-            for (; sp + kSplitUnroll <= splits; sp += kSplitUnroll) {
-                float v[kSplitUnroll];
-#pragma unroll
-                for (int k = 0; k < kSplitUnroll; ++k) v[k] = __ldcs(parts + (sp + k) * total + i);
-#pragma unroll
-                for (int k = 0; k < kSplitUnroll; ++k) acc += v[k];
-            }
-            for (; sp < splits; ++sp) acc += __ldcs(parts + sp * total + i);
-            __stcs(y + i, acc);
-        }
+        for (int64_t i = 2 * T * blockIdx.x + threadIdx.x; i < total; i += step)
+            split_pair(y, parts, total, splits, add, i, i + T);
     }
 }
 
@@ -1212,10 +1275,19 @@ cudaError_t launch_candidates(const Plan &p, const Args &a, float *cand, cudaStr
     return launch_clustered(reinterpret_cast<const void *>(&k_candidates), p, args, s);
 }
 
-cudaError_t launch_split_sum(float *y, const float *parts, int64_t total, int64_t splits, bool add, int ctas,
+cudaError_t launch_split_sum(float *y, const float *parts, int64_t total, int64_t splits, bool add, int sms,
                              cudaStream_t s) {
     const bool vec = total % 4 == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(parts) & 15) == 0;
+    const void *fn = vec ? reinterpret_cast<const void *>(&k_split_sum<true>)
+                         : reinterpret_cast<const void *>(&k_split_sum<false>);
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kSplitThreads, 0);
+    if (e != cudaSuccess) return e;
+    // one resident wave, and no more CTAs than there are pairs of units
+    const int64_t units = vec ? total / 4 : total;
+    const int64_t pair_ctas = (units + 2 * kSplitThreads - 1) / (2 * kSplitThreads);
+    const int ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(pair_ctas, int64_t(per_sm) * sms)));
     if (vec)
         k_split_sum<true><<<ctas, kSplitThreads, 0, s>>>(y, parts, total, splits, add);
     else

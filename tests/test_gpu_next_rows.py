@@ -246,6 +246,8 @@ def test_candidates_nonfinite_rows(orc, plan):
     x[5, :] = nan
     x[5, 4] = -inf                     # one value in the whole row
     x[6, 256:] = nan                   # only the first 256 columns: one value per thread
+    x[7, :] = -inf                     # a masked row (a grammar allows three tokens)
+    x[7, 5], x[7, 300], x[7, 2999] = 1.5, -2.0, 0.25
     with forced(plan):
         cand = ce.candidates_rows(x.to(DEV))
     assert_candidates(cand, orc.candidates(x.numpy(), V), f"non-finite {plan}")
