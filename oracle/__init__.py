@@ -85,6 +85,10 @@ class Oracle:
             getattr(lib, name).restype = ctypes.c_int
         lib.oracle_split_sum.argtypes = [_vp, _vp, _i64, _i64, ctypes.c_int, _vp]
         lib.oracle_split_sum.restype = ctypes.c_int
+        lib.oracle_ce_stats.argtypes = [_vp, _i64, _i64, _i64, _i64, _vp, _vp]
+        lib.oracle_ce_stats.restype = ctypes.c_int
+        lib.oracle_ce_stats_combine.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]
+        lib.oracle_ce_stats_combine.restype = ctypes.c_int
         self.lib = lib
 
     # -- helpers ---------------------------------------------------------
@@ -214,6 +218,37 @@ class Oracle:
                                      1 if add else 0, out.ctypes.data):
             raise ValueError("oracle_split_sum rejected its arguments")
         return out
+
+    # -- vocab-sharded rows ----------------------------------------------
+    def ce_stats(self, logits: np.ndarray, col0: int, vocab: int, labels: np.ndarray):
+        """Row statistics (m, t, top, x[label] or 0) of the column slice
+        [col0, col0 + vocab) of ``logits`` [rows, stride], f64 [rows, 4]."""
+        rows, stride = self._check(logits, 1)
+        if col0 < 0 or vocab < 1 or col0 + vocab > stride:
+            raise ValueError("need 0 <= col0 and col0 + vocab <= stride")
+        labels = np.ascontiguousarray(labels, dtype=np.int64)
+        out = np.empty((rows, 4), dtype=np.float64)
+        if self.lib.oracle_ce_stats(logits.ctypes.data + 4 * col0, rows, vocab, stride, col0,
+                                    labels.ctypes.data, out.ctypes.data):
+            raise ValueError("oracle_ce_stats rejected its arguments")
+        return out
+
+    def ce_stats_combine(self, stats: np.ndarray, vocab_total: int, labels: np.ndarray):
+        """Whole-row loss, token, max M and T from slice statistics
+        ``stats`` f64 [shards, rows, 4]."""
+        stats = np.ascontiguousarray(stats, dtype=np.float64)
+        if stats.ndim != 3 or stats.shape[2] != 4 or stats.shape[0] < 1:
+            raise ValueError("stats must be [shards >= 1, rows, 4]")
+        shards, rows, _ = stats.shape
+        labels = np.ascontiguousarray(labels, dtype=np.int64)
+        loss = np.empty(rows, np.float64)
+        top = np.empty(rows, np.int64)
+        m = np.empty(rows, np.float64)
+        t = np.empty(rows, np.float64)
+        if self.lib.oracle_ce_stats_combine(stats.ctypes.data, shards, rows, vocab_total, labels.ctypes.data,
+                                            loss.ctypes.data, top.ctypes.data, m.ctypes.data, t.ctypes.data):
+            raise ValueError("oracle_ce_stats_combine rejected its arguments")
+        return dict(loss=loss, top=top, m=m, t=t)
 
 
 # candidatesInto's row: 256 threads x TOP_EACH = 4 (value, token) pairs.

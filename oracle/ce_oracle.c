@@ -28,7 +28,7 @@
 #include <math.h>
 #include <stdint.h>
 
-#define ORACLE_VERSION 2
+#define ORACLE_VERSION 3
 
 int oracle_version(void) { return ORACLE_VERSION; }
 
@@ -325,6 +325,130 @@ int oracle_split_sum(const float *y_in, const float *p, int64_t total, int64_t s
         for (int64_t s = 0; s < splits; ++s)
             acc += (double)p[s * total + i];
         y_out[i] = acc;
+    }
+    return 0;
+}
+
+/*
+ * Vocab-sharded cross-entropy: the row statistics of one column slice of the
+ * rows, and their combination over the slices. crossEntropyLoss (netops,
+ * Functions) defines the loss through the row max m and the row's exp-sum
+ * s = sum_j exp(x_j - m); both decompose over any split of the columns:
+ *   m = max_s m_s,  s = sum_s exp(m_s - m) * s_s,
+ * so a row split over slices (e.g. a language-model head whose vocabulary is
+ * split over several devices) needs only each slice's (m_s, s_s), its first
+ * max column and, from the slice that holds it, x[label].
+ *
+ * oracle_ce_stats: for the slice [col0, col0 + vocab) of each row, whose
+ * columns are at logits + i * stride (so `logits` points at column col0),
+ * four doubles per row:
+ *   [0] m   the max of the slice's non-NaN values (-inf if none);
+ *   [1] t   sum of exp(x_j - m) over the slice but its first column holding
+ *           m; NaN if the slice holds a NaN or m = +inf; 0 if m = -inf;
+ *   [2] top the global column (col0 + j) of the first element holding m, or
+ *           -1 if the slice has no non-NaN value;
+ *   [3] xl  x[label] if col0 <= label < col0 + vocab, else 0.
+ */
+int oracle_ce_stats(const float *logits, int64_t rows, int64_t vocab, int64_t stride, int64_t col0,
+                    const int64_t *labels, double *stats_out)
+{
+    if (rows < 0 || vocab < 1 || stride < vocab || col0 < 0)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *x = logits + i * stride;
+        double *o = stats_out + 4 * i;
+        double m = -INFINITY;
+        int64_t jmax = -1;
+        int any_nan = 0;
+        for (int64_t j = 0; j < vocab; ++j) {
+            double v = (double)x[j];
+            if (isnan(v)) {
+                any_nan = 1;
+                continue;
+            }
+            if (jmax < 0 || v > m) {
+                m = v;
+                jmax = j;
+            }
+        }
+        double t = 0.0;
+        if (any_nan || m == INFINITY) {
+            t = NAN;
+        } else if (m != -INFINITY) {
+            for (int64_t j = 0; j < vocab; ++j)
+                if (j != jmax)
+                    t += exp((double)x[j] - m);
+        }
+        int64_t local = labels[i] - col0;
+        o[0] = m;
+        o[1] = t;
+        o[2] = jmax < 0 ? -1.0 : (double)(col0 + jmax);
+        o[3] = (local >= 0 && local < vocab) ? (double)x[local] : 0.0;
+    }
+    return 0;
+}
+
+/*
+ * The combination of `shards` slices' statistics (stats: shards * rows * 4
+ * doubles, slice-major, as oracle_ce_stats writes them) into each whole row's
+ *   M = max_s m_s, and the first column holding it: the lowest top among the
+ *       slices with m_s = M (0 if no slice has a non-NaN value);
+ *   T = the row's exp-sum relative to M less the one term of that column:
+ *       t_s of its slice s*, plus (1 + t_s) exp(m_s - M) of every other slice
+ *       (0 for a slice with m_s = -inf);
+ *   loss = (M - x[label]) + log1p(T), x[label] the sum of the slices' xl (0
+ *       from every slice but the label's); NaN if the label is outside
+ *       [0, vocab_total), or if the row holds a NaN (some t_s is NaN) or M is
+ *       infinite, as crossEntropyRows' value on the whole row.
+ * loss_out, top_out (int64), m_out, t_out: rows each; any may be NULL.
+ */
+int oracle_ce_stats_combine(const double *stats, int64_t shards, int64_t rows, int64_t vocab_total,
+                            const int64_t *labels, double *loss_out, int64_t *top_out, double *m_out,
+                            double *t_out)
+{
+    if (shards < 1 || rows < 0 || vocab_total < 1)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        double M = -INFINITY, xl = 0.0;
+        int any_nan_t = 0;
+        for (int64_t s = 0; s < shards; ++s) {
+            const double *st = stats + 4 * (s * rows + i);
+            if (st[0] > M)
+                M = st[0];
+            if (isnan(st[1]))
+                any_nan_t = 1;
+            xl += st[3];
+        }
+        int64_t star = -1;
+        double top = -1.0;
+        for (int64_t s = 0; s < shards; ++s) {
+            const double *st = stats + 4 * (s * rows + i);
+            if (st[0] == M && st[2] >= 0.0 && (top < 0.0 || st[2] < top)) {
+                top = st[2];
+                star = s;
+            }
+        }
+        int degenerate = any_nan_t || isinf(M) || star < 0;
+        double T = NAN;
+        if (!degenerate) {
+            T = 0.0;
+            for (int64_t s = 0; s < shards; ++s) {
+                const double *st = stats + 4 * (s * rows + i);
+                if (s == star)
+                    T += st[1];
+                else if (st[0] != -INFINITY)
+                    T += (1.0 + st[1]) * exp(st[0] - M);
+            }
+        }
+        int label_ok = labels[i] >= 0 && labels[i] < vocab_total;
+        if (loss_out)
+            loss_out[i] = (degenerate || !label_ok) ? NAN : (M - xl) + log1p(T);
+        if (top_out)
+            top_out[i] = top < 0.0 ? 0 : (int64_t)top;
+        if (m_out)
+            m_out[i] = M;
+        if (t_out)
+            t_out[i] = T;
     }
     return 0;
 }

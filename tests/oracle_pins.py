@@ -485,6 +485,75 @@ def pin_split_sum(orc):
     assert orc.split_sum(np.zeros(0, np.float32), np.zeros((3, 0), np.float32), add=True).shape == (0,)
 
 
+# ---------------------------------------------------------------------------
+# vocab-sharded rows: slice statistics and their combination
+
+
+def _random_cuts(rng, V, shards):
+    cuts = sorted(rng.choice(np.arange(1, V), size=shards - 1, replace=False).tolist()) if shards > 1 else []
+    return [0] + cuts + [V]
+
+
+def pin_sharded_equals_whole_rows(orc):
+    """For any split of the columns, combining the slices' statistics gives
+    the whole row's loss (crossEntropyRows), its argmax token and its max;
+    rows with NaN, +inf, all -inf, slices all -inf or all NaN, ties across
+    slice boundaries and labels out of range included."""
+    rng = np.random.default_rng(81)
+    nan, inf = float("nan"), float("inf")
+    R, V = 14, 97
+    x = (4 * rng.standard_normal((R, V))).astype(np.float32)
+    x[0, 5] = nan
+    x[1, 60] = inf
+    x[2, :] = -inf
+    x[3, :40] = -inf                   # a slice may be all -inf (masked)
+    x[4, :50] = nan                    # a slice may be all NaN
+    x[5, :] = 1.0                      # ties everywhere
+    x[6, 10] = x[6, 70] = 30.0         # the max twice, in different slices
+    x[7, :] = -inf
+    x[7, 80] = 2.0                     # one finite value
+    x[8, 3] = 60.0                     # the label far below a dominant token
+    x[9, :] = x[9, :] - 200.0
+    labels = rng.integers(0, V, size=R).astype(np.int64)
+    labels[8] = 3                      # a tiny loss: label at the max, the rest far below
+    labels[4] = 90                     # a finite label column: only the NaN slice makes the loss NaN
+    labels[10] = -1
+    labels[11] = V
+    whole = orc.ce_rows(x, V, labels)
+    arg = orc.argmax(x, V)
+    fixed = [[0, 40, V], [0, 50, V], [0, 10, 70, V], [0, 3, 4, V]]   # slices all -inf, all NaN, the max alone
+    random_cuts = [_random_cuts(rng, V, shards) for shards in (1, 2, 3, 5, 9) for _ in range(4)]
+    for cuts in fixed + random_cuts:
+        st = np.stack([orc.ce_stats(x, a, b - a, labels) for a, b in zip(cuts, cuts[1:])])
+        comb = orc.ce_stats_combine(st, V, labels)
+        _close(comb["loss"], whole, rel=1e-12, abs_=1e-300, what=f"sharded loss {cuts}")
+        assert (comb["top"] == arg).all(), f"sharded token {cuts}: {comb['top']} != {arg}"
+        fin = ~np.isnan(whole)
+        _close(comb["m"][fin], np.nanmax(x[fin], axis=1), rel=0, what="sharded max")
+
+
+def pin_stats_closed_forms(orc):
+    """A constant slice: m = c, t = width - 1, top = its first column; x[label]
+    only from the slice that holds the label (0 elsewhere); a slice with a NaN
+    has t = NaN; an all -inf slice has m = -inf, t = 0, top = its first column;
+    an all-NaN slice has top = -1."""
+    nan, inf = float("nan"), float("inf")
+    x = np.array([[2.5] * 10, [1.0, nan, 3.0] + [0.0] * 7, [-inf] * 10, [nan] * 10], dtype=np.float32)
+    labels = np.array([7, 2, 4, 0], dtype=np.int64)
+    st = orc.ce_stats(x, 4, 5, labels)      # columns 4..8
+    _close(st[0], [2.5, 4.0, 4.0, 2.5], rel=0, what="constant slice")
+    assert st[1][0] == 0.0 and st[1][2] == 4.0 and st[1][3] == 0.0, st[1]   # label 2 is outside
+    _close(st[2], [-inf, 0.0, 4.0, -inf], rel=0, what="all -inf slice (its label column is -inf)")
+    assert np.isneginf(st[3][0]) and st[3][2] == -1.0, st[3]
+    st2 = orc.ce_stats(x, 0, 3, labels)     # columns 0..2 of the NaN row
+    assert st2[1][0] == 3.0 and np.isnan(st2[1][1]) and st2[1][2] == 2.0 and st2[1][3] == 3.0, st2[1]
+    # two slices of a constant row: T = V - 1, loss = log V
+    comb = orc.ce_stats_combine(np.stack([orc.ce_stats(x, 0, 4, labels), orc.ce_stats(x, 4, 6, labels)]), 10,
+                                labels)
+    _close(comb["t"][0], 9.0, rel=0, what="constant row T")
+    _close(comb["loss"][0], math.log(10), rel=1e-15, what="constant row loss")
+
+
 PINS = [
     pin_uniform_rows, pin_two_class_closed_form, pin_tiny_loss, pin_bruteforce_tiny,
     pin_torch_cross_entropy, pin_central_differences, pin_grad_invariants,
@@ -492,7 +561,7 @@ PINS = [
     pin_argmax_bruteforce, pin_argmax_nan_rules, pin_golden_closed_forms,
     pin_softmax_closed_forms, pin_softmax_torch, pin_softmax_invariants,
     pin_candidates_closed_forms, pin_candidates_torch_topk, pin_candidates_invariants,
-    pin_split_sum,
+    pin_split_sum, pin_sharded_equals_whole_rows, pin_stats_closed_forms,
 ]
 
 

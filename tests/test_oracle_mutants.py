@@ -46,6 +46,15 @@ MUTANTS = {
     "split_sum_add_ignored": ("double acc = add ? (double)y_in[i] : 0.0;", "double acc = 0.0;"),
     "split_sum_drops_last_part": ("for (int64_t s = 0; s < splits; ++s)", "for (int64_t s = 0; s + 1 < splits; ++s)"),
     "split_sum_transposed": ("acc += (double)p[s * total + i];", "acc += (double)p[i * splits + s];"),
+    "stats_t_counts_max": ("                if (j != jmax)\n                    t += exp((double)x[j] - m);",
+                           "                t += exp((double)x[j] - m);"),
+    "stats_top_local": ("o[2] = jmax < 0 ? -1.0 : (double)(col0 + jmax);", "o[2] = jmax < 0 ? -1.0 : (double)jmax;"),
+    "stats_xl_unowned": ("o[3] = (local >= 0 && local < vocab) ? (double)x[local] : 0.0;",
+                         "o[3] = (local >= 0 && local < vocab) ? (double)x[local] : (double)x[0];"),
+    "combine_no_rescale": ("T += (1.0 + st[1]) * exp(st[0] - M);", "T += (1.0 + st[1]);"),
+    "combine_drops_tied_max": ("T += (1.0 + st[1]) * exp(st[0] - M);", "T += st[1] * exp(st[0] - M);"),
+    "combine_last_top": ("(top < 0.0 || st[2] < top)", "(top < 0.0 || st[2] > top)"),
+    "combine_nan_ignored": ("int degenerate = any_nan_t || isinf(M) || star < 0;", "int degenerate = isinf(M) || star < 0;"),
 }
 
 
