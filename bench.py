@@ -431,6 +431,23 @@ def run_case(args):
         cand = torch.empty((R, ce.CANDIDATE_ROW), dtype=torch.float32, device=dev)
         op = lambda: ce.candidates_rows(b.logits, vocab=V, out=cand)
         nbytes, opn = 4 * R * V + 4 * ce.CANDIDATE_ROW * R, ce.OP_CANDIDATES
+    elif args.case == "sharded":
+        # the vocab split into `splits` slices: stats of each, combine, each slice's gradient
+        shards = max(1, args.splits)
+        cuts = sorted(set([min(V, k * -(-V // shards)) for k in range(shards + 1)]))
+        stats = torch.empty((len(cuts) - 1, R, 4), dtype=torch.float32, device=dev)
+        grad = torch.empty((R, V), dtype=torch.float32, device=dev)
+        lr = torch.empty(R, dtype=torch.float32, device=dev)
+        comb = torch.empty((R, 4), dtype=torch.float32, device=dev)
+
+        def op():
+            for k, (a, c) in enumerate(zip(cuts, cuts[1:])):
+                ce.ce_stats(b.logits, b.labels, col0=a, vocab=c - a, out=stats[k])
+            ce.ce_stats_combine(stats, b.labels, V, loss_rows=lr, top=out, combined=comb)
+            for a, c in zip(cuts, cuts[1:]):
+                ce.ce_grad_from_stats(b.logits[:, a:c], b.labels, a, comb, b.scale, grad=grad[:, a:c])
+        # what this split moves: each slice read twice (stats, gradient), the gradient written once
+        nbytes, opn = 12 * R * V + 32 * R * (len(cuts) - 1), None
     elif args.case == "split_sum":
         # the workload's logits as `splits` parts of R * V / splits values
         splits = max(1, args.splits)
@@ -489,9 +506,10 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=256, help="rows per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=["grad", "rows", "argmax", "softmax", "log_softmax", "candidates",
-                                       "split_sum"],
+                                       "split_sum", "sharded"],
                     help="time one operation only (sweeps, profiler captures)")
-    ap.add_argument("--splits", type=int, default=4, help="with --case split_sum: parts to join")
+    ap.add_argument("--splits", type=int, default=4,
+                    help="with --case split_sum: parts to join; with --case sharded: vocab slices")
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), help="with --case: the workload")
     ap.add_argument("--rows", type=int, default=0, help="with --case: rows of the workload to use")
     ap.add_argument("--force", default="", help="with --case: path,cluster,threads (see ce_debug_force)")

@@ -231,6 +231,60 @@ CE_API int candidates_rows(const float *logits, int64_t rows, int64_t vocab, int
  */
 CE_API int split_sum(float *y, const float *parts, int64_t total, int64_t splits, int add, ce_stream_t stream);
 
+/*
+ * Vocab-sharded cross-entropy: the loss, token and gradient of rows whose
+ * columns are split over slices (e.g. a language-model head whose vocabulary
+ * is split over devices), with one exchange of 16 bytes per row and slice.
+ * crossEntropyLoss (gizml:netops, Functions) defines the loss by the row max
+ * m and exp-sum s = sum_j exp(x_j - m); both decompose over any split of the
+ * columns (m = max_s m_s, s = sum_s exp(m_s - m) s_s), so:
+ *   1. ce_stats on each slice            -> [rows] float4 per slice;
+ *   2. gather the slices' stats in column order (the caller's exchange);
+ *   3. ce_stats_combine                  -> each row's loss, token and the
+ *                                           combined float4;
+ *   4. ce_grad_from_stats on each slice  -> the slice of crossEntropyGrad.
+ * The results equal ce_grad's on the whole rows (same rules for ties, NaN,
+ * infinities and bad labels), up to f32 rounding order.
+ *
+ * ce_stats: per row of the slice [col0, col0 + vocab) -- `logits` points at
+ * column col0 of row 0, rows `stride` apart -- the float4 (m, t, top, xl):
+ *   m   the max of the slice's non-NaN values (-inf if none);
+ *   t   sum of exp(x_j - m) over the slice but one element holding m; NaN if
+ *       the slice holds a NaN; not meaningful when m is +-inf;
+ *   top the global column of the first element holding m as f32, or -1 if
+ *       the slice has no non-NaN value;
+ *   xl  x[label] if col0 <= label < col0 + vocab, else 0.
+ *   labels: [rows] int64 GLOBAL columns.   stats: [rows] x 4 f32, 16-byte
+ *   aligned, written. col0 + vocab <= 2^24. No label is checked here.
+ */
+CE_API int ce_stats(const float *logits, int64_t rows, int64_t vocab, int64_t stride, int64_t col0,
+                    const int64_t *labels, float *stats, ce_stream_t stream);
+
+/*
+ * ce_stats_combine: merges `shards` slices' stats (stats: [shards][rows] x 4
+ * f32, slices in column order, 16-byte aligned) into each whole row's
+ *   loss_rows (f32, or NULL): crossEntropyRows of the whole row;
+ *   top       (f32, or NULL): the whole row's argmax token;
+ *   combined  ([rows] x 4 f32, 16-byte aligned, or NULL): (M, T, top, x[label])
+ *             of the whole row, the input of ce_grad_from_stats.
+ * A label outside [0, vocab_total) gives a NaN loss and increments the
+ * device counter, as ce_rows does.
+ */
+CE_API int ce_stats_combine(const float *stats, int64_t shards, int64_t rows, int64_t vocab_total,
+                            const int64_t *labels, float *loss_rows, float *top, float *combined,
+                            ce_stream_t stream);
+
+/*
+ * ce_grad_from_stats: the slice [col0, col0 + vocab) of crossEntropyGrad,
+ *     grad[i, j] = (exp(x_ij - M_i) * f32(1 / (1 + T_i)) - [col0 + j == label_i]) * scale,
+ * from the combined (M, T) of ce_stats_combine; dense [rows, vocab]. A row
+ * whose M is infinite or T is NaN gives a NaN gradient row. grad == logits is
+ * allowed when stride == vocab; any other overlap is not.
+ */
+CE_API int ce_grad_from_stats(const float *logits, int64_t rows, int64_t vocab, int64_t stride, int64_t col0,
+                              const int64_t *labels, const float *combined, double scale, float *grad,
+                              ce_stream_t stream);
+
 /* Human-readable text of a status code (a static string). */
 CE_API const char *ce_status_string(int status);
 

@@ -22,6 +22,9 @@ Functions, and section Methods for the argmax rule):
 - ``softmax_rows`` / ``log_softmax_rows``  the softmax and the log probabilities
                    of each row, from the same row statistics as the loss
 - ``split_sum``    splitSumInto: y (+)= the sum of split partial results
+- ``ce_stats`` / ``ce_stats_combine`` / ``ce_grad_from_stats``  the loss, token
+                   and gradient of rows whose vocabulary is split over slices,
+                   from one exchange of 16 bytes per row and slice
 
 Logits are a CUDA float32 tensor ``[rows, cols]`` whose rows are contiguous
 (``stride(1) == 1``); its row stride ``stride(0)`` may exceed ``vocab``
@@ -76,6 +79,9 @@ def _bind(lib):
         "log_softmax_rows": [vp, i64, i64, i64, vp, vp],
         "candidates_rows": [vp, i64, i64, i64, vp, vp],
         "split_sum": [vp, vp, i64, i64, i32, vp],
+        "ce_stats": [vp, i64, i64, i64, i64, vp, vp, vp],
+        "ce_stats_combine": [vp, i64, i64, i64, vp, vp, vp, vp, vp],
+        "ce_grad_from_stats": [vp, i64, i64, i64, i64, vp, vp, ctypes.c_double, vp, vp],
         "ce_version": [],
         "ce_last_cuda_error": [],
         "ce_device_error_count": [vp, ctypes.POINTER(ctypes.c_uint64)],
@@ -304,6 +310,84 @@ def split_sum(parts: torch.Tensor, y: torch.Tensor | None = None, add: bool = Fa
         _check("split_sum", lib().split_sum(y.data_ptr(), parts.data_ptr(), total, splits, 1 if add else 0,
                                             _stream(dev)))
     return y
+
+
+# -- vocab-sharded cross-entropy ------------------------------------------------
+
+def _slice_view(logits: torch.Tensor, col0: int, vocab: int | None):
+    rows, cols = logits.shape
+    vocab = cols - col0 if vocab is None else int(vocab)
+    if col0 < 0 or vocab < 1 or col0 + vocab > cols:
+        raise ValueError(f"need 0 <= col0 and col0 + vocab <= logits.shape[1] (col0={col0}, vocab={vocab})")
+    view = logits[:, col0: col0 + vocab]
+    r, v, stride = _logits_view(view, vocab)
+    return view, r, v, stride
+
+
+def ce_stats(logits: torch.Tensor, labels: torch.Tensor, col0: int = 0, vocab: int | None = None,
+             out: torch.Tensor | None = None) -> torch.Tensor:
+    """Row statistics (m, t, top, x[label] or 0) of the column slice
+    ``logits[:, col0:col0 + vocab]`` of whole rows, f32 ``[rows, 4]``;
+    ``labels`` are the rows' global columns. For a shard held on its own (its
+    first column being global column col0) use ``ce_stats_shard``."""
+    view, rows, vocab, stride = _slice_view(logits, col0, vocab)
+    return ce_stats_shard(view, labels, col0, out=out)
+
+
+def ce_stats_shard(shard: torch.Tensor, labels: torch.Tensor, col0: int,
+                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """Row statistics of a shard ``[rows, width]`` (row-contiguous, any row
+    stride) whose first column is global column ``col0``; f32 ``[rows, 4]``."""
+    rows, vocab, stride = _logits_view(shard, None)
+    dev = shard.device
+    labels = _labels(labels, rows, dev)
+    out = _out(out, (rows, 4), torch.float32, dev, "out")
+    with torch.cuda.device(dev):
+        _check("ce_stats", lib().ce_stats(shard.data_ptr(), rows, vocab, stride, int(col0), labels.data_ptr(),
+                                           out.data_ptr(), _stream(dev)))
+    return out
+
+
+def ce_stats_combine(stats: torch.Tensor, labels: torch.Tensor, vocab_total: int,
+                     loss_rows: bool | torch.Tensor = True, top: bool | torch.Tensor = True,
+                     combined: bool | torch.Tensor = True):
+    """Merge slices' statistics ``stats`` f32 ``[shards, rows, 4]`` (slices in
+    column order) into the whole rows' loss, token and combined (M, T, top,
+    x[label]); returns ``(loss_rows, top, combined)`` with None for what was
+    not asked."""
+    if stats.dtype != torch.float32 or stats.dim() != 3 or stats.shape[2] != 4 or not stats.is_contiguous():
+        raise ValueError("stats must be a contiguous float32 [shards, rows, 4] tensor")
+    shards, rows, _ = stats.shape
+    dev = stats.device
+    labels = _labels(labels, rows, dev)
+    lr = None if loss_rows is False else _out(None if loss_rows is True else loss_rows, (rows,), torch.float32,
+                                              dev, "loss_rows")
+    tp = None if top is False else _out(None if top is True else top, (rows,), torch.float32, dev, "top")
+    cb = None if combined is False else _out(None if combined is True else combined, (rows, 4), torch.float32,
+                                             dev, "combined")
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    with torch.cuda.device(dev):
+        _check("ce_stats_combine", lib().ce_stats_combine(stats.data_ptr(), shards, rows, int(vocab_total),
+                                                           labels.data_ptr(), ptr(lr), ptr(tp), ptr(cb),
+                                                           _stream(dev)))
+    return lr, tp, cb
+
+
+def ce_grad_from_stats(shard: torch.Tensor, labels: torch.Tensor, col0: int, combined: torch.Tensor,
+                       scale: float, grad: torch.Tensor | None = None) -> torch.Tensor:
+    """The shard's slice of crossEntropyGrad from the combined row state,
+    dense f32 ``[rows, width]`` (``grad`` may be ``shard`` itself when dense)."""
+    rows, vocab, stride = _logits_view(shard, None)
+    dev = shard.device
+    labels = _labels(labels, rows, dev)
+    if combined.dtype != torch.float32 or tuple(combined.shape) != (rows, 4) or not combined.is_contiguous():
+        raise ValueError(f"combined must be a contiguous float32 [{rows}, 4] tensor")
+    grad = _out(grad, (rows, vocab), torch.float32, dev, "grad")
+    with torch.cuda.device(dev):
+        _check("ce_grad_from_stats", lib().ce_grad_from_stats(shard.data_ptr(), rows, vocab, stride, int(col0),
+                                                               labels.data_ptr(), combined.data_ptr(),
+                                                               float(scale), grad.data_ptr(), _stream(dev)))
+    return grad
 
 
 # -- diagnostics and tuning ---------------------------------------------------

@@ -389,6 +389,66 @@ int split_sum(float *y, const float *parts, int64_t total, int64_t splits, int a
     return cuda_status(launch_split_sum(y, parts, total, splits, add != 0, dev.sms, stream));
 }
 
+int ce_stats(const float *logits, int64_t rows, int64_t vocab, int64_t stride, int64_t col0, const int64_t *labels,
+             float *stats, ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (col0 < 0 || col0 + vocab > kMaxVocab) return CE_EINVAL;  // global columns exact in f32
+    if (rows > 0 && (labels == nullptr || stats == nullptr)) return CE_EINVAL;
+    if (misaligned(labels, 8) || misaligned(stats, 16)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    if (ranges_overlap(stats, rows * 16, logits, ((rows - 1) * stride + vocab) * 4)) return CE_EINVAL;
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(kOpRows, rows, vocab, dev, &p))) return st;
+    Args a = make_args(logits, rows, vocab, stride, labels);
+    a.stats = stats;
+    a.col0 = col0;
+    return cuda_status(launch_rows_stream(p, a, true, stream));
+}
+
+int ce_stats_combine(const float *stats, int64_t shards, int64_t rows, int64_t vocab_total, const int64_t *labels,
+                     float *loss_rows, float *top, float *combined, ce_stream_t stream) {
+    if (shards < 1 || rows < 0 || vocab_total < 1 || vocab_total > kMaxVocab) return CE_EINVAL;
+    if (rows > 0 && (stats == nullptr || labels == nullptr)) return CE_EINVAL;
+    if (rows > 0 && shards > (INT64_MAX / 16) / rows) return CE_EINVAL;
+    if (misaligned(stats, 16) || misaligned(labels, 8) || misaligned(loss_rows, 4) || misaligned(top, 4) ||
+        misaligned(combined, 16))
+        return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    if (combined && ranges_overlap(combined, rows * 16, stats, shards * rows * 16)) return CE_EINVAL;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    return cuda_status(
+        launch_stats_combine(stats, shards, rows, vocab_total, labels, loss_rows, top, combined, dev.sms, stream));
+}
+
+int ce_grad_from_stats(const float *logits, int64_t rows, int64_t vocab, int64_t stride, int64_t col0,
+                       const int64_t *labels, const float *combined, double scale, float *grad, ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (col0 < 0 || col0 + vocab > kMaxVocab || !std::isfinite(scale)) return CE_EINVAL;
+    if (rows > 0 && (labels == nullptr || combined == nullptr || grad == nullptr)) return CE_EINVAL;
+    if (misaligned(labels, 8) || misaligned(combined, 16) || misaligned(grad, 4)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    const int64_t in_bytes = ((rows - 1) * stride + vocab) * 4;
+    const int64_t out_bytes = rows * vocab * 4;
+    if (grad == logits) {
+        if (stride != vocab) return CE_EINVAL;  // in place needs the same layout
+    } else if (ranges_overlap(grad, out_bytes, logits, in_bytes)) {
+        return CE_EINVAL;
+    }
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Args a = make_args(logits, rows, vocab, stride, labels);
+    a.scale = static_cast<float>(scale);
+    a.grad = grad;
+    a.col0 = col0;
+    return cuda_status(launch_grad_from_stats(a, combined, dev.sms, stream));
+}
+
 int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t stride) {
     if (rows < 1 || vocab < 1 || vocab > kMaxVocab || stride < vocab) return 0;
     DeviceInfo dev;

@@ -64,6 +64,8 @@ struct Args {
     float *grad;
     float *loss;
     float *top;
+    float *stats;   // vocab-sharded rows: [rows] float4 (m, t, top, x[label]) of the slice
+    int64_t col0;   // vocab-sharded rows: global column of the slice's first column
 };
 
 cudaError_t set_kernel_attributes(const DeviceInfo &dev);
@@ -79,6 +81,11 @@ cudaError_t launch_candidates(const Plan &p, const Args &a, float *cand, cudaStr
 cudaError_t launch_split_sum(float *y, const float *parts, int64_t total, int64_t splits, bool add, int sms,
                              cudaStream_t s);
 cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s);
+// vocab-sharded rows: combine `shards` slices' statistics; gradient of one slice
+cudaError_t launch_stats_combine(const float *stats, int64_t shards, int64_t rows, int64_t vocab_total,
+                                 const int64_t *labels, float *loss, float *top, float *combined, int sms,
+                                 cudaStream_t s);
+cudaError_t launch_grad_from_stats(const Args &a, const float *combined, int sms, cudaStream_t s);
 // argmax of few long rows split evenly over `ctas` CTAs; ws: 8 * (ctas + rows) bytes
 cudaError_t launch_argmax_flat(const Args &a, int ctas, void *ws, cudaStream_t s);
 

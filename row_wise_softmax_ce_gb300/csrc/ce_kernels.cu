@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
         float xl = 0.0f;
         bool lab_ok = true;
         if (kStats && rank == 0 && tid == 0) {
-            label = a.labels[row];
+            label = a.labels[row] - a.col0;  // col0: 0 but for a vocab slice
             lab_ok = label_valid(label, a.vocab);
             if (lab_ok) xl = a.logits[row * a.stride + label];
         }
@@ -140,7 +140,11 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
             float unused;
             const RowState g = push_xchg_merge<kStats>(xg, k, K, C, 0u, &unused, &failed);
             if (rank == 0 && tid == 0) {
-                if (kStats && a.loss) {
+                if (kStats && a.stats) {
+                    // a vocab slice's statistics; x[label] is 0 unless the slice holds the label
+                    const float top = g.idx == kNoIndex ? -1.0f : static_cast<float>(a.col0 + g.idx);
+                    reinterpret_cast<float4 *>(a.stats)[row] = make_float4(g.m, g.t, top, xl);
+                } else if (kStats && a.loss) {
                     a.loss[row] = row_loss(g, xl, lab_ok);
                     if (!lab_ok) atomicAdd(&g_status[0], 1ull);
                 }
@@ -1154,6 +1158,73 @@ __global__ void __launch_bounds__(kSplitThreads) k_split_sum(float *__restrict__
 }
 
 // ---------------------------------------------------------------------------
+// Vocab-sharded rows. A row split over column slices (k_rows_stream writes
+// each slice's float4 (m, t, top, x[label] or 0)) is put back together here:
+// k_stats_combine merges the slices' states in slice order with the same
+// symmetric merge the CTAs of a cluster use for one row, and writes the whole
+// row's loss, token and combined state (M, T, top, x[label]); then
+// k_grad_from_stats writes one slice's gradient from the combined (M, T).
+__global__ void __launch_bounds__(256) k_stats_combine(const float4 *__restrict__ stats, int64_t shards,
+                                                       int64_t rows, int64_t vocab_total,
+                                                       const int64_t *__restrict__ labels, float *__restrict__ loss,
+                                                       float *__restrict__ top, float4 *__restrict__ combined) {
+    const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; row < rows; row += step) {
+        RowState g = empty_state();
+        float xl = 0.0f;
+        for (int64_t sh = 0; sh < shards; ++sh) {
+            const float4 v = stats[sh * rows + row];
+            const RowState q{v.x, v.y, v.z < 0.0f ? kNoIndex : static_cast<int>(v.z)};
+            g = sh == 0 ? q : merge<true>(g, q);
+            xl += v.w;  // every slice but the label's adds an exact 0
+        }
+        const int64_t label = labels[row];
+        const bool lab_ok = label >= 0 && label < vocab_total;
+        if (loss) loss[row] = row_loss(g, xl, lab_ok);
+        if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+        if (top) top[row] = row_token(g);
+        if (combined)
+            combined[row] = make_float4(g.m, g.t, g.idx == kNoIndex ? -1.0f : static_cast<float>(g.idx), xl);
+    }
+}
+
+// One CTA per row (looping): grad[j] = (exp(x_j - M) * f32(1/(1 + T)) - [col0
+// + j == label]) * scale over the slice, dense [rows, vocab]; NaN rows where
+// the whole row is degenerate. Loads and stores are coherent (grad may be the
+// slice itself when the slice is dense).
+constexpr int kGradStatsUnroll = 4;
+
+__global__ void __launch_bounds__(256) k_grad_from_stats(Args a, const float4 *__restrict__ combined) {
+    const int T = blockDim.x;
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+        const float4 st = combined[row];
+        const float M = st.x;
+        const bool bad = !isfinite(M) || isnan(st.y);
+        const float rcp = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + st.y);
+        const float cm = rcp * a.scale;
+        const int64_t local = a.labels[row] - a.col0;
+        const int lab = (local >= 0 && local < a.vocab) ? static_cast<int>(local) : -1;
+        const float *p = a.logits + row * a.stride;
+        float *g = a.grad + row * static_cast<int64_t>(a.vocab);
+        int j = threadIdx.x;
+        for (; j + (kGradStatsUnroll - 1) * T < a.vocab; j += kGradStatsUnroll * T) {
+            float x[kGradStatsUnroll];
+#pragma unroll
+            for (int u = 0; u < kGradStatsUnroll; ++u) x[u] = __ldcs(p + j + u * T);
+#pragma unroll
+            for (int u = 0; u < kGradStatsUnroll; ++u) {
+                const float e = exp_le0(x[u] - M);
+                __stcs(g + j + u * T, j + u * T == lab ? (e * rcp - 1.0f) * a.scale : e * cm);
+            }
+        }
+        for (; j < a.vocab; j += T) {
+            const float e = exp_le0(__ldcs(p + j) - M);
+            __stcs(g + j, j == lab ? (e * rcp - 1.0f) * a.scale : e * cm);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // k_mean: one CTA. Thread k sums rows k, k + T, ... in f64; a butterfly over
 // each warp, then over the warps' sums. Fixed shape: same bits every run.
 __global__ void __launch_bounds__(1024) k_mean(const float *__restrict__ loss, int64_t rows,
@@ -1302,6 +1373,23 @@ cudaError_t launch_argmax_flat(const Args &a, int ctas, void *ws, cudaStream_t s
     const int threads = 256;
     const unsigned blocks = static_cast<unsigned>((a.rows + threads - 1) / threads);
     k_argmax_combine<<<blocks, threads, 0, s>>>(a, static_cast<const uint64_t *>(ws), ctas);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats_combine(const float *stats, int64_t shards, int64_t rows, int64_t vocab_total,
+                                 const int64_t *labels, float *loss, float *top, float *combined, int sms,
+                                 cudaStream_t s) {
+    const int64_t blocks = std::min<int64_t>((rows + 255) / 256, 8 * int64_t(sms));
+    k_stats_combine<<<static_cast<unsigned>(std::max<int64_t>(1, blocks)), 256, 0, s>>>(
+        reinterpret_cast<const float4 *>(stats), shards, rows, vocab_total, labels, loss, top,
+        reinterpret_cast<float4 *>(combined));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grad_from_stats(const Args &a, const float *combined, int sms, cudaStream_t s) {
+    (void)sms;
+    const int64_t blocks = std::min<int64_t>(a.rows, int64_t(1) << 20);
+    k_grad_from_stats<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a, reinterpret_cast<const float4 *>(combined));
     return cudaGetLastError();
 }
 

@@ -110,6 +110,27 @@ def test_split_sum_validation(lib):
     assert lib.split_sum(None, None, 0, 3, 1, None) == ce.CE_OK                    # nothing launched
 
 
+def test_vocab_sharded_validation(lib):
+    # ce_stats: slice bounds, 16-byte stats, no overlap with the logits
+    assert lib.ce_stats(V(256), 4, 10, 10, -1, V(512), V(4096), None) == ce.CE_EINVAL
+    assert lib.ce_stats(V(256), 4, 10, 10, (1 << 24) - 5, V(512), V(4096), None) == ce.CE_EINVAL
+    assert lib.ce_stats(V(256), 4, 10, 10, 0, None, V(4096), None) == ce.CE_EINVAL
+    assert lib.ce_stats(V(256), 4, 10, 10, 0, V(512), V(4100), None) == ce.CE_EALIGN
+    assert lib.ce_stats(V(4096), 4, 10, 10, 0, V(512), V(4096 + 16), None) == ce.CE_EINVAL
+    assert lib.ce_stats(None, 0, 10, 10, 0, None, None, None) == ce.CE_OK
+    # ce_stats_combine
+    assert lib.ce_stats_combine(V(4096), 0, 4, 100, V(512), None, None, None, None) == ce.CE_EINVAL
+    assert lib.ce_stats_combine(V(4096), 2, 4, (1 << 24) + 1, V(512), None, None, None, None) == ce.CE_EINVAL
+    assert lib.ce_stats_combine(V(4104), 2, 4, 100, V(512), None, None, None, None) == ce.CE_EALIGN
+    assert lib.ce_stats_combine(V(4096), 2, 4, 100, V(512), None, None, V(4096 + 64), None) == ce.CE_EINVAL
+    assert lib.ce_stats_combine(None, 2, 0, 100, None, None, None, None, None) == ce.CE_OK
+    # ce_grad_from_stats
+    assert lib.ce_grad_from_stats(V(256), 4, 10, 10, 0, V(512), V(1024), float("nan"), V(8192), None) == ce.CE_EINVAL
+    assert lib.ce_grad_from_stats(V(256), 4, 10, 10, 0, V(512), V(1032), 1.0, V(8192), None) == ce.CE_EALIGN
+    assert lib.ce_grad_from_stats(V(4096), 4, 10, 12, 0, V(512), V(1024), 1.0, V(4096), None) == ce.CE_EINVAL
+    assert lib.ce_grad_from_stats(V(256), 4, 10, 10, 0, V(512), None, 1.0, V(8192), None) == ce.CE_EINVAL
+
+
 def test_zero_rows_is_a_no_op_without_device(lib):
     # nothing is launched, so no device is needed
     assert lib.ce_rows(None, 0, 10, 10, None, None, None) == ce.CE_OK
