@@ -436,7 +436,7 @@ def run_case(args):
         shards = max(1, args.splits)
         cuts = sorted(set([min(V, k * -(-V // shards)) for k in range(shards + 1)]))
         stats = torch.empty((len(cuts) - 1, R, 4), dtype=torch.float32, device=dev)
-        grad = torch.empty((R, V), dtype=torch.float32, device=dev)
+        grads = [torch.empty((R, c - a), dtype=torch.float32, device=dev) for a, c in zip(cuts, cuts[1:])]
         lr = torch.empty(R, dtype=torch.float32, device=dev)
         comb = torch.empty((R, 4), dtype=torch.float32, device=dev)
 
@@ -444,8 +444,8 @@ def run_case(args):
             for k, (a, c) in enumerate(zip(cuts, cuts[1:])):
                 ce.ce_stats(b.logits, b.labels, col0=a, vocab=c - a, out=stats[k])
             ce.ce_stats_combine(stats, b.labels, V, loss_rows=lr, top=out, combined=comb)
-            for a, c in zip(cuts, cuts[1:]):
-                ce.ce_grad_from_stats(b.logits[:, a:c], b.labels, a, comb, b.scale, grad=grad[:, a:c])
+            for (a, c), g in zip(zip(cuts, cuts[1:]), grads):
+                ce.ce_grad_from_stats(b.logits[:, a:c], b.labels, a, comb, b.scale, grad=g)
         # what this split moves: each slice read twice (stats, gradient), the gradient written once
         nbytes, opn = 12 * R * V + 32 * R * (len(cuts) - 1), None
     elif args.case == "split_sum":
