@@ -310,7 +310,8 @@ CE_API int ce_device_error_reset(ce_stream_t stream);
  * (path: 0 automatic, 1 shared-memory-staged (persistent), 2 streaming from
  * global, 3 persistent ring of bulk copies (ce_grad only), 4
  * shared-memory-staged with one row per cluster, 5 argmax split evenly over
- * the GPU -- needs a workspace), the CTAs that share one row (cluster: 0
+ * the GPU -- needs a workspace, 6 one warp per row -- ce_rows, ce_loss,
+ * argmax_rows and ce_stats only), the CTAs that share one row (cluster: 0
  * automatic, else 1..16; candidates_rows takes at most 8) and the threads of
  * a CTA (threads: 0 automatic, else 128 or 256; 512 is rejected by every
  * kernel family; candidates_rows takes 256 only).

@@ -107,6 +107,25 @@ void plan_stream(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, in
     p.clusters = std::min<int64_t>(rows, kMaxClusters);
 }
 
+// Launch shape of the warp-per-row kernel: 256-thread CTAs (8 rows at a
+// time each), as many as are resident at once and no more than the rows need.
+bool plan_warp(Plan &p, Op op, int64_t rows) {
+    p.path = kPathWarp;
+    p.threads = 256;
+    p.cluster = 1;
+    p.smem = 0;
+    p.cols = 0;
+    p.clusters = 1;
+    int active = 0;
+    if (max_active_clusters(p, op, &active) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    if (active < 1) return false;
+    p.clusters = std::max<int64_t>(1, std::min<int64_t>(ceil_div(rows, 8), active));
+    return true;
+}
+
 // Launch shape of the staged fused kernel: the fewest CTAs per row whose
 // slices are at most kStagedTargetCols columns (at most 16 CTAs).
 bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster,
@@ -189,6 +208,18 @@ void plan_candidates(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev
     p.clusters = std::min<int64_t>(rows, kMaxClusters);
 }
 
+// Where one warp per row beats a CTA (or cluster) per row, measured on GB300
+// with L2 flushed: ce_rows 4096 x 32000 81% vs 66% of copy bandwidth, 16384 x
+// 50257 97% vs 83%, slices of 16032 columns x 8192 rows 2.24 vs 2.49 ms for
+// eight; argmax 4096 x 32000 96% vs 90%, but 16384 x 50257 97% vs 105%. Long
+// rows (128256) and few rows stay with the CTA per row.
+bool warp_applies(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev) {
+    if (rows < 8 * static_cast<int64_t>(dev.sms)) return false;
+    if (op == kOpRows) return vocab <= 65536;
+    if (op == kOpArgmax) return vocab <= 32768;
+    return false;
+}
+
 int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *out) {
     Force f;
     {
@@ -206,7 +237,7 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
                 return CE_EINVAL;
         } else if (f.path == kPathStream) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
-        } else if (f.path == kPathFlat) {
+        } else if (f.path == kPathFlat || f.path == kPathWarp) {
             return CE_EINVAL;
         } else if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, false, true)) {
             plan_stream(p, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
@@ -224,6 +255,11 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
         p.smem = 0;
         p.cols = static_cast<int>(vocab);
         p.clusters = 2 * static_cast<int64_t>(dev.sms);
+    } else if (f.path == kPathWarp) {
+        if ((f.threads && f.threads != 256) || f.cluster > 1 || !plan_warp(p, op, rows)) return CE_EINVAL;
+    } else if (f.path == kPathAuto && f.cluster == 0 && f.threads == 0 && warp_applies(op, rows, vocab, dev) &&
+               plan_warp(p, op, rows)) {
+        // many rows of moderate width: one warp per row
     } else {
         plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
     }
@@ -558,7 +594,7 @@ int ce_device_error_reset(ce_stream_t stream) {
 }
 
 int ce_debug_force(int path, int cluster, int threads) {
-    if (path < 0 || path > 5 || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
+    if (path < 0 || path > kPathWarp || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
     if (threads != 0 && threads != 128 && threads != 256 && threads != 512) return CE_EINVAL;
     std::lock_guard<std::mutex> lock(g_mu);
     g_force.path = path;

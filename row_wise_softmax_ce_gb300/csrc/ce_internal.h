@@ -7,7 +7,15 @@
 
 namespace cerows {
 
-enum Path : int { kPathAuto = 0, kPathStaged = 1, kPathStream = 2, kPathRing = 3, kPathStagedPerRow = 4, kPathFlat = 5 };
+enum Path : int {
+    kPathAuto = 0,
+    kPathStaged = 1,
+    kPathStream = 2,
+    kPathRing = 3,
+    kPathStagedPerRow = 4,
+    kPathFlat = 5,
+    kPathWarp = 6,  // one warp per row (ce_rows, argmax, slice statistics of many short rows)
+};
 enum Op : int { kOpRows = 0, kOpGrad = 1, kOpArgmax = 2, kOpSoftmax = 3, kOpLogSoftmax = 4, kOpCandidates = 5 };
 // What the fused two-pass kernels write from a row's (max, exp-sum) state.
 enum Mode : int { kModeGrad = 0, kModeSoftmax = 1, kModeLogSoftmax = 2 };

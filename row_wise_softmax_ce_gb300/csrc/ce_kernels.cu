@@ -80,9 +80,8 @@ __device__ __forceinline__ float row_token(const RowState &g) {
 // (p -> column j0): a scalar head up to the first 16-byte boundary, 16-byte
 // vectors, a scalar tail. Each thread sees its columns in increasing order.
 template <bool kStats, int kU = kUnroll>
-__device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int j0, int n) {
+__device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int j0, int n, int tid, int T) {
     RowState st = empty_state();
-    const int tid = threadIdx.x, T = blockDim.x;
     const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
     const int head = min(n, (4 - off) & 3);
     const int nvec = (n - head) >> 2;
@@ -101,6 +100,12 @@ __device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int
     for (; k < nvec; k += T) push_vec<kStats>(st, ld_stream_f4(pv + k), jv + 4 * k);
     if (tid < tail) push<kStats>(st, ld_stream_f1(p + head + 4 * nvec + tid), jv + 4 * nvec + tid);
     return st;
+}
+
+// the CTA's threads over one slice
+template <bool kStats, int kU = kUnroll>
+__device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int j0, int n) {
+    return scan_global<kStats, kU>(p, j0, n, static_cast<int>(threadIdx.x), static_cast<int>(blockDim.x));
 }
 
 // ---------------------------------------------------------------------------
@@ -156,6 +161,42 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
     cluster_arrive();  // no CTA leaves while a peer may still push to it
     cluster_wait();
     if (__syncthreads_or(failed) && tid == 0) atomicAdd(&g_status[1], 1ull);
+}
+
+// ---------------------------------------------------------------------------
+// k_rows_warp: the outputs of k_rows_stream (row loss, token, or a vocab
+// slice's statistics) for many short rows: one warp per row, looping over
+// rows, the state merged by shuffles alone -- no CTA barrier, no exchange.
+// Each warp keeps 2 KB of loads in flight; tens of warps per SM cover HBM's
+// latency where a CTA per row would spend most of its time starting, merging
+// and ending.
+template <bool kStats>
+__global__ void __launch_bounds__(256) k_rows_warp(Args a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < a.rows;
+         row += nwarps) {
+        int64_t label = 0;
+        float xl = 0.0f;
+        bool lab_ok = true;
+        if (kStats && lane == 0) {
+            label = a.labels[row] - a.col0;  // col0: 0 but for a vocab slice
+            lab_ok = label_valid(label, a.vocab);
+            if (lab_ok) xl = a.logits[row * a.stride + label];
+        }
+        RowState g = scan_global<kStats>(a.logits + row * a.stride, 0, a.vocab, lane, 32);
+        g = warp_reduce<kStats>(g);
+        if (lane == 0) {
+            if (kStats && a.stats) {
+                const float top = g.idx == kNoIndex ? -1.0f : static_cast<float>(a.col0 + g.idx);
+                reinterpret_cast<float4 *>(a.stats)[row] = make_float4(g.m, g.t, top, xl);
+            } else if (kStats && a.loss) {
+                a.loss[row] = row_loss(g, xl, lab_ok);
+                if (!lab_ok) atomicAdd(&g_status[0], 1ull);
+            }
+            if (a.top) a.top[row] = row_token(g);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1275,6 +1316,9 @@ const void *kernel_of(const Plan &p, Op op) {
     if (op == kOpSoftmax) return fused_kernel<kModeSoftmax>(p.path);
     if (op == kOpLogSoftmax) return fused_kernel<kModeLogSoftmax>(p.path);
     if (op == kOpCandidates) return reinterpret_cast<const void *>(&k_candidates);
+    if (p.path == kPathWarp)
+        return op == kOpRows ? reinterpret_cast<const void *>(&k_rows_warp<true>)
+                             : reinterpret_cast<const void *>(&k_rows_warp<false>);
     if (op == kOpRows) return reinterpret_cast<const void *>(&k_rows_stream<true>);
     return reinterpret_cast<const void *>(&k_rows_stream<false>);
 }
@@ -1326,6 +1370,13 @@ cudaError_t max_active_clusters(const Plan &p, Op op, int *n) {
 }
 
 cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStream_t s) {
+    if (p.path == kPathWarp) {
+        if (stats)
+            k_rows_warp<true><<<static_cast<unsigned>(p.clusters), p.threads, 0, s>>>(a);
+        else
+            k_rows_warp<false><<<static_cast<unsigned>(p.clusters), p.threads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
     Args aa = a;
     int cols = p.cols;
     void *args[] = {&aa, &cols};

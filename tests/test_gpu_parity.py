@@ -431,3 +431,39 @@ def test_argmax_workspace_contract(orc):
         assert (top == -1.0).all()
     finally:
         ce.debug_force(0, 0, 0)
+
+
+@pytest.mark.parametrize("offset", [0, 1, 3])
+def test_warp_per_row_path(orc, offset):
+    """The warp-per-row kernel (path 6): ce_rows, ce_loss and argmax_rows on
+    shapes that cross its vector loop, misaligned rows, padding never read,
+    and non-finite rows; fused calls reject the path."""
+    nan, inf = float("nan"), float("inf")
+    ce.debug_force(6, 0, 0)
+    try:
+        for rows, vocab, stride in ((1, 1, 1), (3, 5, 7), (37, 1000, 1003), (300, 4099, 4099), (2000, 129, 130)):
+            x, y = W.random_logits(rows, vocab, stride=stride, sigma=3.0, seed=rows + vocab, pad_value=nan)
+            if rows >= 37:
+                x[0, 3] = nan
+                x[1, :vocab] = -inf
+                x[2, 7] = inf
+                x[3, :vocab] = 2.0
+                y[4] = -1
+            buf = torch.full((rows * stride + offset + 8,), 1e30, device=DEV)
+            dx = buf[offset: offset + rows * stride].view(rows, stride)
+            dx.copy_(x.to(DEV))
+            yd = y.to(DEV)
+            lr = ce.ce_rows(dx, yd, vocab=vocab)
+            mean, lr2 = ce.ce_loss(dx, yd, vocab=vocab)
+            top = ce.argmax_rows(dx, vocab=vocab)
+            torch.cuda.synchronize()
+            l_ref = orc.ce_rows(x.numpy(), vocab, y.numpy())
+            assert_loss(lr, l_ref, f"warp ce_rows {rows}x{vocab}")
+            assert_loss(lr2, l_ref, f"warp ce_loss rows {rows}x{vocab}")
+            assert_mean(mean.item(), orc.ce_mean(l_ref), f"warp mean {rows}x{vocab}")
+            assert_tokens(top, orc.argmax(x.numpy(), vocab), f"warp argmax {rows}x{vocab}")
+        with pytest.raises(ce.CeError):
+            ce.ce_grad(dx, yd, 1.0, vocab=vocab)
+    finally:
+        ce.debug_force(0, 0, 0)
+        ce.device_error_reset()

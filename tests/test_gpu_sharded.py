@@ -154,3 +154,17 @@ def test_sharded_bad_labels_counter(orc):
     check(orc, x, y, [0, 2000, V], 1.0, res, "bad labels")
     assert ce.device_error_count() == (2, 0)
     ce.device_error_reset()
+
+
+@pytest.mark.parametrize("plan", [(2, 0, 0), (6, 0, 0)], ids=["cta-per-row", "warp-per-row"])
+def test_sharded_stats_on_each_row_kernel(orc, plan):
+    V, R = 20000, 700
+    x, y = W.random_logits(R, V, sigma=2.0, seed=33)
+    x[5, :8000] = -float("inf")
+    cuts = [0, 7001, 8000, 13333, V]
+    ce.debug_force(*plan)
+    try:
+        res = sharded_step(x.to(DEV), y.to(DEV), cuts, 1.0 / R)
+    finally:
+        ce.debug_force(0, 0, 0)
+    check(orc, x, y, cuts, 1.0 / R, res, f"stats via {plan}")
