@@ -276,6 +276,8 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
     bool failed = false;
     uint32_t parity = 0;
     int64_t k = 0;  // this cluster's row count so far
+    // each row's label is loaded one row ahead, off the row's critical path
+    int64_t label_next = (kCE && K > 0) ? a.labels[cid] : 0;
     for (int64_t row = cid; row < a.rows; row += G, parity ^= 1u, ++k) {
         const float *p = a.logits + row * a.stride + c0;
         const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
@@ -293,7 +295,8 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         float4 edge0 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), edge1 = edge0;
         if (qe0 >= 0 && owner(qe0) == tid) edge0 = load_edge(p, off, n, qe0);
         if (qe1 >= 0 && owner(qe1) == tid) edge1 = load_edge(p, off, n, qe1);
-        const int64_t label = kCE ? a.labels[row] : 0;
+        const int64_t label = label_next;
+        if (kCE && more) label_next = a.labels[row + G];
         const bool lab_ok = !kCE || label_valid(label, a.vocab);
         const int lab_local = (kCE && lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
         const int lab_f = lab_local >= 0 ? off + lab_local : -1;  // float index of the label
@@ -361,7 +364,8 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         if (tid == 0) push_xchg_publish(h.xg, k, rank, C, st, lab_local >= 0 ? h.bc[2] : 0.0f);
         if (tid < 32) {
             float xl;
-            const uint32_t own = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
+            // a valid label is below 2^24: a 32-bit division
+            const uint32_t own = lab_ok ? static_cast<uint32_t>(label) / static_cast<uint32_t>(cols) : 0u;
             const RowState g = push_xchg_merge<true>(h.xg, k, K, C, own, &xl, &failed);
             if (tid == 0) {
                 const bool bad = !isfinite(g.m) || isnan(g.t);
