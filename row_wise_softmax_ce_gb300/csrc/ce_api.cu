@@ -89,11 +89,19 @@ int current_device(DeviceInfo *out) {
 // Launch shape of a streaming kernel (ce_rows, argmax_rows, and the fused
 // path for rows too long to stage): split a row over C CTAs when there are
 // too few rows to give every SM several CTAs.
-void plan_stream(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster) {
+void plan_stream(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster) {
     p.path = kPathStream;
     p.threads = threads ? threads : kStreamMaxThreads;
     if (cluster) {
         p.cluster = cluster;
+    } else if (op == kOpArgmax) {
+        // argmax (branch-free scan): split rows until about four CTAs per SM;
+        // none from three rows per SM up. Measured on GB300, rows x 151936, L2
+        // flushed (us, by CTAs per row): 256 rows 36.9 / 30.8 / 28.7 / 34.8 for
+        // 1 / 2 / 3 / 4; 128 rows best at 5 (18.4); 512 rows best at 1 (51.2).
+        int64_t c = rows >= 3 * static_cast<int64_t>(dev.sms) ? 1 : ceil_div(4 * static_cast<int64_t>(dev.sms), rows);
+        c = std::min<int64_t>(c, std::min<int64_t>(kMaxCluster, ceil_div(vocab, kStreamMinCols)));
+        p.cluster = static_cast<int>(std::max<int64_t>(1, c));
     } else {
         // split a row only when there are fewer rows than about two CTAs per
         // SM (measured on GB300, 256 x 151936: 2 CTAs per row 32.8 us, 4: 38.9,
@@ -236,11 +244,11 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
             if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, f.path == kPathStagedPerRow, false))
                 return CE_EINVAL;
         } else if (f.path == kPathStream) {
-            plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
+            plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster);
         } else if (f.path == kPathFlat || f.path == kPathWarp) {
             return CE_EINVAL;
         } else if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, false, true)) {
-            plan_stream(p, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
+            plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
         }
     } else if (op == kOpCandidates) {
         if (f.path != kPathAuto && f.path != kPathStream) return CE_EINVAL;
@@ -261,7 +269,7 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
                plan_warp(p, op, rows)) {
         // many rows of moderate width: one warp per row
     } else {
-        plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
+        plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster);
     }
     if (p.cluster < 1 || p.cluster > kMaxCluster) return CE_EINVAL;
     if (p.path == kPathStream && p.threads > kStreamMaxThreads) return CE_EINVAL;
@@ -517,7 +525,7 @@ int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride
             f = g_force;
         }
         if (f.path == kPathFlat) return CE_EINVAL;  // forced, but no room for it
-        plan_stream(p, rows, vocab, dev, 0, 0);
+        plan_stream(p, kOpArgmax, rows, vocab, dev, 0, 0);
     }
     return cuda_status(launch_rows_stream(p, a, false, stream));
 }

@@ -76,11 +76,65 @@ __device__ __forceinline__ float row_token(const RowState &g) {
     return static_cast<float>(g.idx == kNoIndex ? 0 : g.idx);
 }
 
+// The argmax state (max, first column) of columns [j0, j0 + n) read from
+// global memory at p, without the exp-sum: per 16-byte vector one max4 and one
+// compare, and selects keep the best value, its vector and the vector itself
+// -- no branch, so a warp never serialises on a lane that found a new max.
+// The first lane holding the best value is found once at the end; strict
+// compares keep the first vector of equals, and NaN never wins (fmaxf drops
+// it). A thread whose vectors hold nothing above -inf rescans them exactly
+// (only rows of -inf and NaN get there).
+template <int kU>
+__device__ __forceinline__ RowState scan_argmax(const float *__restrict__ p, int j0, int n, int tid, int T) {
+    RowState st = empty_state();
+    const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+    const int head = min(n, (4 - off) & 3);
+    const int nvec = (n - head) >> 2;
+    const int tail = n - head - 4 * nvec;
+    const float4 *pv = reinterpret_cast<const float4 *>(p + head);
+    const int jv = j0 + head;
+    if (tid < head) push<false>(st, ld_stream_f1(p + tid), j0 + tid);
+    float best = -INFINITY;
+    int bk = -1;
+    float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+    int k = tid;
+    for (; k + (kU - 1) * T < nvec; k += kU * T) {
+        float4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) v[u] = ld_stream_f4(pv + k + u * T);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const float mv = max4(v[u]);
+            const bool gt = mv > best;
+            best = gt ? mv : best;
+            bk = gt ? k + u * T : bk;
+            bv = gt ? v[u] : bv;
+        }
+    }
+    for (; k < nvec; k += T) {
+        const float4 v = ld_stream_f4(pv + k);
+        const float mv = max4(v);
+        const bool gt = mv > best;
+        best = gt ? mv : best;
+        bk = gt ? k : bk;
+        bv = gt ? v : bv;
+    }
+    if (bk >= 0) {
+        const int l = bv.x == best ? 0 : bv.y == best ? 1 : bv.z == best ? 2 : 3;
+        push<false>(st, best, jv + 4 * bk + l);
+    } else {
+        for (k = tid; k < nvec; k += T) push4<false>(st, ld_stream_f4(pv + k), jv + 4 * k);
+    }
+    if (tid < tail) push<false>(st, ld_stream_f1(p + head + 4 * nvec + tid), jv + 4 * nvec + tid);
+    return st;
+}
+
 // Push the columns [j0, j0 + n) of one row, read from global memory at p
 // (p -> column j0): a scalar head up to the first 16-byte boundary, 16-byte
 // vectors, a scalar tail. Each thread sees its columns in increasing order.
 template <bool kStats, int kU = kUnroll>
 __device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int j0, int n, int tid, int T) {
+    if constexpr (!kStats) return scan_argmax<kU>(p, j0, n, tid, T);
     RowState st = empty_state();
     const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
     const int head = min(n, (4 - off) & 3);
@@ -1008,7 +1062,7 @@ __device__ __forceinline__ void cluster_arrive_release() {
 // cluster (in CTA 0 only), C - 1 x 4 x 256 float2.
 __global__ void __launch_bounds__(kCandThreads, 3) k_candidates(Args a, float *__restrict__ out) {
     using namespace cand;
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     float2 *S = reinterpret_cast<float2 *>(smem);
     float2 *X = S + kGroups * kTopEach * kCandThreads;
     const uint32_t rank = cluster_rank(), C = cluster_size();
