@@ -164,12 +164,26 @@ def dist_env():
 
 
 def max_over_ranks(x: float, ws: int) -> float:
+    """The largest of the ranks' values (the slowest rank's time): a host
+    tensor over gloo, a device tensor over NCCL."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_workload(w, rank: int):
+    """Rank r's batch: the same shape, its own seed (replicas of independent rows)."""
+    import dataclasses
+    return w if rank == 0 else dataclasses.replace(w, seed=w.seed + 1000 * rank)
+
+
+def aggregate_gbs(ws: int, bytes_per_rank_step: int, step_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank moved in a step over the slowest rank's step time."""
+    return ws * bytes_per_rank_step / (step_ms * 1e-3) / 1e9
 
 
 def barrier(ws: int):
@@ -256,10 +270,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     # ---- the training step on the headline workload
-    w = W.WORKLOADS[W.HEADLINE]
-    if ws > 1:
-        import dataclasses
-        w = dataclasses.replace(w, seed=w.seed + 1000 * rank)
+    w = replica_workload(W.WORKLOADS[W.HEADLINE], rank)
     b = W.generate(w, device=dev)
     x, y, scale = b.logits, b.labels, b.scale
     R, V = w.rows, w.vocab
@@ -295,7 +306,7 @@ def run_ours(args):
     step_ms = max_over_ranks(step_ms_local, ws)
     fused_ms = statistics.mean(a.elapsed_time(c) for a, c in ev)
     bytes_step = step_bytes(R, V)
-    value = ws * bytes_step / (step_ms * 1e-3) / 1e9
+    value = aggregate_gbs(ws, bytes_step, step_ms)
     peak, peak_kind = peaks()
     fused_bytes = 8 * R * V + 16 * R   # what one ce_grad launch moves
     achieved = fused_bytes / (fused_ms * 1e-3) / 1e9
@@ -320,7 +331,7 @@ def run_ours(args):
         e1.record(stream)
         times.append((e0, e1))
     torch.cuda.synchronize()
-    arg_ms = statistics.median(a.elapsed_time(c) for a, c in times)
+    arg_ms = max_over_ranks(statistics.median(a.elapsed_time(c) for a, c in times), ws)
     del flush, bd
 
     # ---- end to end: inputs from pinned host memory, results back to the host
@@ -352,7 +363,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K2, ws)
-    e2e_value = ws * bytes_step / (e2e_ms * 1e-3) / 1e9
+    e2e_value = aggregate_gbs(ws, bytes_step, e2e_ms)
     h2d = xh.numel() * 4 + yh.numel() * 8
     d2h = 8 + top_h.numel() * 4
     del xh, xd
@@ -382,7 +393,7 @@ def run_ours(args):
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes": fused_bytes, "ms_per_launch": round(fused_ms, 4)},
-            "argmax": {"workload": wd.name, "rows_per_s": round(wd.rows / (arg_ms * 1e-3), 1),
+            "argmax": {"workload": wd.name, "rows_per_s": round(ws * wd.rows / (arg_ms * 1e-3), 1),
                        "ms": round(arg_ms, 5),
                        "GB/s": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9, 1),
                        "frac": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9 / peak, 4),
