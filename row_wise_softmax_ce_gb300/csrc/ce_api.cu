@@ -200,19 +200,22 @@ bool flat_applies(int64_t rows, int64_t vocab, const DeviceInfo &dev, bool force
 int64_t flat_workspace_bytes(int64_t rows, const DeviceInfo &dev) { return 8 * (2 * static_cast<int64_t>(dev.sms) + rows); }
 
 // Launch shape of the candidates kernel: 256 threads (the pages' workgroup);
-// a row split over C CTAs when there are fewer rows than about two CTAs per
-// SM, each CTA at least 2048 columns, C at most kCandMaxCluster.
+// a row split over C CTAs below two rows per SM: 4, or 8 for 32 rows or fewer;
+// each CTA at least 2048 columns. Measured on GB300, rows x 151936, L2
+// flushed (us): 256 rows 56.6 / 55.4 / 57.7 / 53.7 / 78.1 for C = 1 / 2 / 3 /
+// 4 / 8; 128 rows 38.9 / 36.9 / 45.2 for C = 2 / 4 / 8; 64 rows 34.1 / 24.9 /
+// 27.4; 32 rows 33.3 / 22.8 / 21.4.
 void plan_candidates(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int cluster) {
     p.path = kPathStream;
     p.threads = kCandThreads;
     int64_t c = cluster;
     if (!c) {
-        c = ceil_div(2 * static_cast<int64_t>(dev.sms), rows);
+        c = rows >= 2 * static_cast<int64_t>(dev.sms) ? 1 : rows > 32 ? 4 : 8;
         c = std::min<int64_t>(c, std::min<int64_t>(kCandMaxCluster, ceil_div(vocab, kStreamMinCols)));
     }
     p.cluster = static_cast<int>(std::max<int64_t>(1, c));
     p.cols = round_up4(ceil_div(vocab, p.cluster));
-    p.smem = 4 * kCandListBytes + (p.cluster - 1) * kCandListBytes;
+    p.smem = (p.cluster - 1) * kCandListBytes;
     p.clusters = std::min<int64_t>(rows, kMaxClusters);
 }
 

@@ -26,10 +26,10 @@ constexpr int kCandThreads = 256;
 constexpr int kTopEach = 4;
 constexpr int kCandRow = 2 * kCandThreads * kTopEach;
 constexpr int kCandMaxCluster = 8;
-// shared memory of the candidates kernel: the 4 thread groups' lists, and
-// (split rows) the lists the cluster's other CTAs send to CTA 0
+// shared memory of the candidates kernel (split rows): the lists the cluster's
+// other CTAs send to CTA 0
 constexpr int kCandListBytes = kCandThreads * kTopEach * 8;  // one (value, column) list set
-constexpr int kCandMaxSmemBytes = 4 * kCandListBytes + kCandMaxCluster * kCandListBytes;
+constexpr int kCandMaxSmemBytes = (kCandMaxCluster - 1) * kCandListBytes;
 constexpr int kSplitThreads = 256;
 
 // Per-CTA shared bytes the staged kernel reserves before its row buffer.

@@ -954,20 +954,10 @@ __global__ void k_argmax_combine(Args a, const uint64_t *__restrict__ ws, int P)
 // 2048 floats at cand + 2048 i: pair 4t + k is thread t's rank-k (value,
 // column as f32), (-inf, -1) where the thread read fewer than 4 values.
 //
-// How: a CTA of 256 threads is 4 groups of 64, and a cluster of C CTAs shares
-// a row. The row is read as 16-byte vectors from the 16-byte boundary at or
-// below its start (off = the start's offset in floats): vector q holds
-// columns 4q - off ... 4q - off + 3. As 256 columns are 64 vectors, vector
-// q = 64 n + u always holds columns of the logical threads (4u + k - off) mod
-// 256, k = 0..3, so physical thread u of group G (of the cluster's 4C) reads
-// the blocks n = G, G + 4C, ... and keeps one list per lane k. The lists then
-// meet: the CTA's 4 groups through shared memory, the cluster's CTAs in CTA 0
-// through distributed shared memory; CTA 0 writes the row.
+// How: see k_candidates below; the helpers here keep a thread's sorted list.
 namespace cand {
 
-constexpr int kUnrollC = 4;                 // 16-byte loads in flight per thread
-constexpr int kEmptyCol = 0x7fffffff;       // a slot without a value ranks last
-constexpr int kGroups = kCandThreads / 64;  // groups of 64 threads in a CTA
+constexpr int kEmptyCol = 0x7fffffff;  // a slot without a value ranks last
 
 struct TopList {
     float v[kTopEach];
@@ -1007,11 +997,10 @@ __device__ __forceinline__ void top_push(TopList &L, float x, int col) {
 }
 
 // The scan's insertion: x at column col, later than every column the list
-// holds, so an equal value never displaces a kept one. Branch-free (four
-// compares, fourteen selects): with 128 lists per warp some lane almost
-// always inserts, so a branch would not skip. Strict compares keep out NaN,
-// and also -inf (it ties an empty slot's -inf): a list left with empty slots
-// takes its -inf columns after the scan.
+// holds, so an equal value never displaces a kept one (four compares, then
+// selects; the caller has seen x > the list's 4th value). Strict compares keep
+// out NaN, and also -inf (it ties an empty slot's -inf): a list left with
+// empty slots takes its -inf columns after the scan.
 __device__ __forceinline__ void stream_push(TopList &L, float x, int col) {
     const bool p0 = x > L.v[0], p1 = x > L.v[1], p2 = x > L.v[2], p3 = x > L.v[3];
     const float v0 = L.v[0], v1 = L.v[1], v2 = L.v[2];
@@ -1032,21 +1021,6 @@ __device__ __forceinline__ float2 slot_of(const TopList &L, int k) {
 
 __device__ __forceinline__ void push_slot(TopList &L, float2 e) { top_push(L, e.x, __float_as_int(e.y)); }
 
-// 16-byte vector q of a row (p -> column 0, off = p's offset in floats within
-// 16 bytes): columns 4q - off ... +3, NaN (never kept) outside [0, vocab).
-__device__ __forceinline__ float4 load_vec(const float *p, int off, int vocab, int q, int qlo, int qhi) {
-    if (q >= qlo && q < qhi) return ld_stream_f4(reinterpret_cast<const float4 *>(p - off) + q);
-    float v[4];
-#pragma unroll
-    for (int l = 0; l < 4; ++l) {
-        const int col = 4 * q - off + l;
-        v[l] = (col >= 0 && col < vocab) ? ld_stream_f1(p + col) : __int_as_float(0x7fffffff);
-    }
-    return make_float4(v[0], v[1], v[2], v[3]);
-}
-
-__device__ __forceinline__ float lane4(float4 v, int l) { return l == 0 ? v.x : l == 1 ? v.y : l == 2 ? v.z : v.w; }
-
 __device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float2 v) {
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
 }
@@ -1057,83 +1031,62 @@ __device__ __forceinline__ void cluster_arrive_release() {
 
 }  // namespace cand
 
-// Dynamic shared memory: S, 4 groups x 4 ranks x 256 logical threads of
-// (value, column) float2; then X, the merged lists of CTAs 1..C-1 of the
-// cluster (in CTA 0 only), C - 1 x 4 x 256 float2.
-__global__ void __launch_bounds__(kCandThreads, 3) k_candidates(Args a, float *__restrict__ out) {
+// k_candidates: thread t of a 256-thread CTA is the pages' logical thread t
+// itself and keeps one list: it reads columns t + 256 j (the warp's 32 loads
+// are 128 contiguous bytes) for the blocks j = rank, rank + C, ... of the
+// cluster's C CTAs. The insertion sits behind a real branch (x > the list's
+// 4th value): the warp runs it when any of its 32 lanes inserts, which late in
+// a list's stream is rarely. The cluster's CTAs merge in CTA 0 through
+// distributed shared memory; CTA 0 writes the row.
+constexpr int kLaneUnroll = 16;  // 4-byte loads in flight per thread
+
+__global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *__restrict__ out) {
     using namespace cand;
     extern __shared__ __align__(128) unsigned char smem[];
-    float2 *S = reinterpret_cast<float2 *>(smem);
-    float2 *X = S + kGroups * kTopEach * kCandThreads;
+    float2 *X = reinterpret_cast<float2 *>(smem);  // lists of CTAs 1..C-1 (in CTA 0)
     const uint32_t rank = cluster_rank(), C = cluster_size();
-    const int tid = threadIdx.x, u = tid & 63, grp = tid >> 6;
-    const int G = static_cast<int>(rank) * kGroups + grp, NG = static_cast<int>(C) * kGroups;
+    const int t = threadIdx.x;
+    const int Ci = static_cast<int>(C), ri = static_cast<int>(rank);
     const int64_t cid = cluster_id_x(), GC = cluster_count_x();
     const bool vec_out = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+    const int nb = (a.vocab + kCandThreads - 1) / kCandThreads;  // blocks of 256 columns
+    const int nfull = a.vocab / kCandThreads;                     // blocks with every column < vocab
     if (C > 1) cluster_arrive();  // matched before the first write to CTA 0
     for (int64_t row = cid; row < a.rows; row += GC) {
         const float *p = a.logits + row * a.stride;
-        const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
-        const int nq = (a.vocab + off + 3) >> 2;  // vectors covering the row
-        const int qlo = off ? 1 : 0, qhi = (a.vocab + off) >> 2;  // whole vectors: [qlo, qhi)
-        const int nb = (nq + 63) >> 6;            // blocks of 64 vectors (256 columns)
-        TopList L[4];
+        TopList L;
+        top_init(L);
+        int j = ri;
+        for (; j + (kLaneUnroll - 1) * Ci < nfull; j += kLaneUnroll * Ci) {
+            float x[kLaneUnroll];
 #pragma unroll
-        for (int l = 0; l < 4; ++l) top_init(L[l]);
-        for (int n0 = G; n0 < nb; n0 += NG * kUnrollC) {
-            float4 v[kUnrollC];
+            for (int u = 0; u < kLaneUnroll; ++u) x[u] = ld_stream_f1(p + t + kCandThreads * (j + u * Ci));
 #pragma unroll
-            for (int i = 0; i < kUnrollC; ++i) {
-                const int q = 64 * (n0 + i * NG) + u;
-                v[i] = q < nq ? load_vec(p, off, a.vocab, q, qlo, qhi)
-                              : make_float4(__int_as_float(0x7fffffff), 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int i = 0; i < kUnrollC; ++i) {
-                const int q = 64 * (n0 + i * NG) + u;
-                if (q < nq) {
-#pragma unroll
-                    for (int l = 0; l < 4; ++l) stream_push(L[l], lane4(v[i], l), 4 * q - off + l);
-                }
+            for (int u = 0; u < kLaneUnroll; ++u)
+                if (x[u] > L.v[3]) stream_push(L, x[u], t + kCandThreads * (j + u * Ci));
+        }
+        for (; j < nb; j += Ci) {
+            const int col = t + kCandThreads * j;
+            if (col < a.vocab) {
+                const float x = ld_stream_f1(p + col);
+                if (x > L.v[3]) stream_push(L, x, col);
             }
         }
         // a list with an empty slot takes, in column order, its columns that
         // hold -inf (the scan kept every larger value already)
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-            if (L[l].c[3] != kEmptyCol) continue;
+        if (L.c[3] == kEmptyCol) {
             int r = 0;
 #pragma unroll
-            for (int k = 0; k < kTopEach; ++k) r += L[l].c[k] != kEmptyCol;
-            for (int n = G; n < nb && r < kTopEach; n += NG) {
-                const int col = 4 * (64 * n + u) - off + l;
-                if (col < 0 || col >= a.vocab || p[col] != -INFINITY) continue;
+            for (int k = 0; k < kTopEach; ++k) r += L.c[k] != kEmptyCol;
+            for (int jj = ri; jj < nb && r < kTopEach; jj += Ci) {
+                const int col = t + kCandThreads * jj;
+                if (col >= a.vocab || p[col] != -INFINITY) continue;
 #pragma unroll
                 for (int k = 0; k < kTopEach; ++k)
-                    if (k == r) L[l].c[k] = col;  // its value is already -inf
+                    if (k == r) L.c[k] = col;  // its value is already -inf
                 ++r;
             }
         }
-        // the CTA's 4 groups: S[grp][k][t], t the logical thread of the list
-#pragma unroll
-        for (int l = 0; l < 4; ++l) {
-            const int t = (4 * u + l - off) & (kCandThreads - 1);
-#pragma unroll
-            for (int k = 0; k < kTopEach; ++k) S[(grp * kTopEach + k) * kCandThreads + t] = slot_of(L[l], k);
-        }
-        __syncthreads();
-        TopList M;
-        const int t = tid;  // from here on, thread t merges logical thread t's lists
-#pragma unroll
-        for (int k = 0; k < kTopEach; ++k) {
-            const float2 e = S[k * kCandThreads + t];
-            M.v[k] = e.x;
-            M.c[k] = __float_as_int(e.y);
-        }
-#pragma unroll
-        for (int g = 1; g < kGroups; ++g)
-#pragma unroll
-            for (int k = 0; k < kTopEach; ++k) push_slot(M, S[(g * kTopEach + k) * kCandThreads + t]);
         if (C > 1) {
             cluster_wait();  // CTA 0 is running, and (later rows) done with X
             if (rank != 0) {
@@ -1141,25 +1094,23 @@ __global__ void __launch_bounds__(kCandThreads, 3) k_candidates(Args a, float *_
 #pragma unroll
                 for (int k = 0; k < kTopEach; ++k)
                     st_dsmem_f2(x0 + 8u * static_cast<uint32_t>(((rank - 1) * kTopEach + k) * kCandThreads + t),
-                                slot_of(M, k));
+                                slot_of(L, k));
             }
             cluster_arrive_release();
             cluster_wait();
             if (rank == 0)
                 for (uint32_t r = 1; r < C; ++r)
 #pragma unroll
-                    for (int k = 0; k < kTopEach; ++k) push_slot(M, X[((r - 1) * kTopEach + k) * kCandThreads + t]);
-            cluster_arrive_release();  // X and S may be rewritten once every CTA is past here
-        } else {
-            __syncthreads();  // S is rewritten for the next row
+                    for (int k = 0; k < kTopEach; ++k) push_slot(L, X[((r - 1) * kTopEach + k) * kCandThreads + t]);
+            cluster_arrive_release();  // X may be rewritten once every CTA is past here
         }
         if (rank == 0) {
             float o[8];
 #pragma unroll
             for (int k = 0; k < kTopEach; ++k) {
-                const bool empty = M.c[k] == kEmptyCol;
-                o[2 * k] = empty ? -INFINITY : M.v[k];
-                o[2 * k + 1] = empty ? -1.0f : static_cast<float>(M.c[k]);
+                const bool empty = L.c[k] == kEmptyCol;
+                o[2 * k] = empty ? -INFINITY : L.v[k];
+                o[2 * k + 1] = empty ? -1.0f : static_cast<float>(L.c[k]);
             }
             float *dst = out + row * static_cast<int64_t>(kCandRow) + 8 * t;
             if (vec_out) {
@@ -1452,7 +1403,7 @@ cudaError_t launch_candidates(const Plan &p, const Args &a, float *cand, cudaStr
     Args aa = a;
     float *cc = cand;
     void *args[] = {&aa, &cc};
-    return launch_clustered(reinterpret_cast<const void *>(&k_candidates), p, args, s);
+    return launch_clustered(kernel_of(p, kOpCandidates), p, args, s);
 }
 
 cudaError_t launch_split_sum(float *y, const float *parts, int64_t total, int64_t splits, bool add, int sms,

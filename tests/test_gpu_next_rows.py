@@ -197,7 +197,7 @@ def test_candidates_decode_in_full(orc):
                   orc.argmax(b.logits.cpu().numpy(), w.vocab, threads=THREADS), "best candidate")
 
 
-CAND_PLANS = [(0, 0, 0), (0, 1, 0), (0, 2, 0), (0, 3, 256), (2, 4, 0), (0, 8, 0)]
+CAND_PLANS = [(0, 0, 0), (0, 1, 0), (0, 2, 0), (0, 3, 256), (2, 4, 0), (0, 5, 256), (0, 8, 0)]
 
 
 @pytest.mark.parametrize("plan", CAND_PLANS, ids=lambda p: f"path{p[0]}-c{p[1]}-t{p[2]}")
@@ -215,7 +215,7 @@ def test_candidates_shapes_ties_and_clusters(orc, plan):
                 assert_candidates(cand, orc.candidates(x.numpy(), vocab), f"{plan} {rows}x{vocab}")
 
 
-@pytest.mark.parametrize("plan", [(0, 0, 0), (0, 1, 0), (0, 4, 0)], ids=str)
+@pytest.mark.parametrize("plan", [(0, 0, 0), (0, 1, 0), (0, 3, 0), (0, 4, 0)], ids=str)
 @pytest.mark.parametrize("offset", [1, 2, 3])
 def test_candidates_misaligned_base_and_odd_stride(orc, plan, offset):
     rows, vocab = 7, 5003
@@ -231,7 +231,7 @@ def test_candidates_misaligned_base_and_odd_stride(orc, plan, offset):
             assert_candidates(out, orc.candidates(x.numpy(), vocab), f"off{offset} stride{stride} {plan}")
 
 
-@pytest.mark.parametrize("plan", [(0, 0, 0), (0, 1, 0), (0, 4, 0)], ids=str)
+@pytest.mark.parametrize("plan", [(0, 0, 0), (0, 1, 0), (0, 4, 0), (0, 7, 0)], ids=str)
 def test_candidates_nonfinite_rows(orc, plan):
     nan, inf = float("nan"), float("inf")
     V = 3000

@@ -21,7 +21,7 @@ N_CASES = 48
 
 FUSED_PLANS = [(0, 0, 0), (1, 0, 0), (1, 2, 128), (1, 5, 0), (2, 0, 0), (2, 3, 128), (4, 0, 0)]
 ROW_PLANS = [(0, 0, 0), (2, 0, 0), (2, 4, 128), (6, 0, 0)]
-CAND_PLANS = [(0, 0, 0), (0, 1, 0), (0, 3, 0), (0, 8, 0)]
+CAND_PLANS = [(0, 0, 0), (0, 1, 0), (0, 3, 0), (0, 4, 0), (0, 8, 0)]
 
 
 @pytest.fixture(scope="module", autouse=True)
