@@ -219,6 +219,27 @@ CE_API int candidates_rows(const float *logits, int64_t rows, int64_t vocab, int
                            ce_stream_t stream);
 
 /*
+ * argmaxInto and candidatesInto in their indirect form (gizml:netops,
+ * Functions): the entries read "rows of `stride`, of the head blocks in
+ * `blocks` when `indirect`"; the extracted sentence is garbled, and this
+ * library takes its plainest reading -- row i is read at the device address
+ * row_addrs[i] instead of at logits + i * stride (rows picked in place, e.g.
+ * each sequence's last position, without gathering them first). Same rules,
+ * outputs and kernels as argmax_rows / candidates_rows.
+ *   row_addrs: [rows] uint64 device addresses of f32 rows, each with `vocab`
+ *              readable floats; 8-byte aligned table, read only. Rows may
+ *              repeat and may sit anywhere (4-byte aligned).
+ *   top:  [rows] f32, written.   cand: [rows, 2048] f32, written.
+ * An address that is null or not 4-byte aligned is detected on the device and
+ * never read: that row's token is NaN, its candidates all (-inf, -1). The
+ * outputs must not overlap any row. A forced even split (path 5) is refused.
+ */
+CE_API int argmax_rows_indirect(const uint64_t *row_addrs, int64_t rows, int64_t vocab, float *top,
+                                ce_stream_t stream);
+CE_API int candidates_rows_indirect(const uint64_t *row_addrs, int64_t rows, int64_t vocab, float *cand,
+                                    ce_stream_t stream);
+
+/*
  * splitSumInto (gizml:netops, Functions): joins `splits` partial results of
  * `total` f32 values each (part s at parts + s * total, e.g. the partial
  * products of a split reduction):

@@ -19,6 +19,8 @@ Functions, and section Methods for the argmax rule):
 - ``argmax_rows``  argmaxInto: each row's token (first of equals, NaN never wins) as f32
 - ``candidates_rows``  candidatesInto: each row's 2048-float sampling candidates
                    (256 threads x TOP_EACH = 4 (value, token) pairs)
+- ``argmax_rows_indirect`` / ``candidates_rows_indirect``  the same over rows
+                   given by a device table of addresses (the indirect form)
 - ``softmax_rows`` / ``log_softmax_rows``  the softmax and the log probabilities
                    of each row, from the same row statistics as the loss
 - ``split_sum``    splitSumInto: y (+)= the sum of split partial results
@@ -79,6 +81,8 @@ def _bind(lib):
         "log_softmax_rows": [vp, i64, i64, i64, vp, vp],
         "candidates_rows": [vp, i64, i64, i64, vp, vp],
         "split_sum": [vp, vp, i64, i64, i32, vp],
+        "argmax_rows_indirect": [vp, i64, i64, vp, vp],
+        "candidates_rows_indirect": [vp, i64, i64, vp, vp],
         "ce_stats": [vp, i64, i64, i64, i64, vp, vp, vp],
         "ce_stats_combine": [vp, i64, i64, i64, vp, vp, vp, vp, vp],
         "ce_grad_from_stats": [vp, i64, i64, i64, i64, vp, vp, ctypes.c_double, vp, vp],
@@ -293,6 +297,46 @@ def candidates_rows(logits: torch.Tensor, vocab: int | None = None,
     thread t's rank-k (value, token) of the columns t, t + 256, ...; (-inf, -1)
     where thread t read fewer than 4 values."""
     return _rows_out("candidates_rows", logits, vocab, out, CANDIDATE_ROW)
+
+
+def row_addresses(logits: torch.Tensor, index: torch.Tensor) -> torch.Tensor:
+    """Device addresses (int64) of the rows ``logits[index]``, for the indirect calls."""
+    if not logits.is_cuda or logits.dim() != 2 or logits.dtype != torch.float32:
+        raise ValueError("logits must be a 2-D float32 CUDA tensor")
+    index = index.to(device=logits.device, dtype=torch.int64)
+    return logits.data_ptr() + index * (logits.stride(0) * 4)
+
+
+def _row_table(row_addrs: torch.Tensor):
+    if row_addrs.dtype not in (torch.int64, torch.uint64) or row_addrs.dim() != 1 or not row_addrs.is_cuda \
+            or not row_addrs.is_contiguous():
+        raise ValueError("row_addrs must be a contiguous 1-D int64 CUDA tensor of row addresses")
+    return row_addrs
+
+
+def argmax_rows_indirect(row_addrs: torch.Tensor, vocab: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """argmaxInto, indirect form: the token (f32) of each row read at the device
+    address ``row_addrs[i]`` (``vocab`` floats each); NaN for a null or
+    misaligned address."""
+    row_addrs = _row_table(row_addrs)
+    rows, dev = row_addrs.shape[0], row_addrs.device
+    out = _out(out, (rows,), torch.float32, dev, "out")
+    with torch.cuda.device(dev):
+        _check("argmax_rows_indirect", lib().argmax_rows_indirect(row_addrs.data_ptr(), rows, int(vocab),
+                                                                  out.data_ptr(), _stream(dev)))
+    return out
+
+
+def candidates_rows_indirect(row_addrs: torch.Tensor, vocab: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """candidatesInto, indirect form: ``[rows, 2048]`` candidates of the rows at
+    the addresses ``row_addrs``."""
+    row_addrs = _row_table(row_addrs)
+    rows, dev = row_addrs.shape[0], row_addrs.device
+    out = _out(out, (rows, CANDIDATE_ROW), torch.float32, dev, "out")
+    with torch.cuda.device(dev):
+        _check("candidates_rows_indirect", lib().candidates_rows_indirect(row_addrs.data_ptr(), rows, int(vocab),
+                                                                          out.data_ptr(), _stream(dev)))
+    return out
 
 
 def split_sum(parts: torch.Tensor, y: torch.Tensor | None = None, add: bool = False) -> torch.Tensor:

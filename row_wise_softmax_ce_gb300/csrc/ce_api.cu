@@ -436,6 +436,49 @@ int split_sum(float *y, const float *parts, int64_t total, int64_t splits, int a
     return cuda_status(launch_split_sum(y, parts, total, splits, add != 0, dev.sms, stream));
 }
 
+// argmax_rows_indirect / candidates_rows_indirect: the rows at the addresses
+// of a device table (argmaxInto's indirect form); same kernels and plans as
+// the direct calls, less the even split (which walks rows by their stride).
+int check_row_table(const uint64_t *row_addrs, int64_t rows, int64_t vocab) {
+    if (rows < 0 || vocab < 1 || vocab > kMaxVocab) return CE_EINVAL;
+    if (rows > 0 && row_addrs == nullptr) return CE_EINVAL;
+    if (misaligned(row_addrs, 8)) return CE_EALIGN;
+    return CE_OK;
+}
+
+int argmax_rows_indirect(const uint64_t *row_addrs, int64_t rows, int64_t vocab, float *top, ce_stream_t stream) {
+    int st = check_row_table(row_addrs, rows, vocab);
+    if (st) return st;
+    if (rows > 0 && top == nullptr) return CE_EINVAL;
+    if (misaligned(top, 4)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(kOpArgmax, rows, vocab, dev, &p))) return st;
+    if (p.path == kPathFlat) return CE_EINVAL;  // forced even split: needs strided rows
+    Args a = make_args(nullptr, rows, vocab, vocab, nullptr);
+    a.row_at = row_addrs;
+    a.top = top;
+    return cuda_status(launch_rows_stream(p, a, false, stream));
+}
+
+int candidates_rows_indirect(const uint64_t *row_addrs, int64_t rows, int64_t vocab, float *cand,
+                             ce_stream_t stream) {
+    int st = check_row_table(row_addrs, rows, vocab);
+    if (st) return st;
+    if (rows > 0 && cand == nullptr) return CE_EINVAL;
+    if (misaligned(cand, 4)) return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(kOpCandidates, rows, vocab, dev, &p))) return st;
+    Args a = make_args(nullptr, rows, vocab, vocab, nullptr);
+    a.row_at = row_addrs;
+    return cuda_status(launch_candidates(p, a, cand, stream));
+}
+
 int ce_stats(const float *logits, int64_t rows, int64_t vocab, int64_t stride, int64_t col0, const int64_t *labels,
              float *stats, ce_stream_t stream) {
     int st = check_logits(logits, rows, vocab, stride);

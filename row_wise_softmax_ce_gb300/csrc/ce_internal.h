@@ -74,6 +74,7 @@ struct Args {
     float *top;
     float *stats;   // vocab-sharded rows: [rows] float4 (m, t, top, x[label]) of the slice
     int64_t col0;   // vocab-sharded rows: global column of the slice's first column
+    const uint64_t *row_at;  // rows given by address (argmaxInto's indirect form), or null
 };
 
 cudaError_t set_kernel_attributes(const DeviceInfo &dev);

@@ -52,6 +52,15 @@ static_assert(sizeof(StagedHeader) <= kStagedHeaderBytes, "staged header too lar
 
 __device__ __forceinline__ bool label_valid(int64_t label, int vocab) { return label >= 0 && label < vocab; }
 
+// Row `row`'s first column: logits + row * stride, or, when the rows are given
+// by a table of addresses, that address -- null when the address is null or
+// not 4-byte aligned, a row that is then never read.
+__device__ __forceinline__ const float *row_start(const Args &a, int64_t row) {
+    if (!a.row_at) return a.logits + row * a.stride;
+    const uint64_t v = a.row_at[row];
+    return (v == 0 || (v & 3)) ? nullptr : reinterpret_cast<const float *>(v);
+}
+
 // The row loss from the merged state: (m - x[label]) + log1p(t); NaN for a
 // bad label, or a row whose max is +-inf (a +inf entry, or all -inf / NaN),
 // or whose t is NaN (a NaN entry).
@@ -183,16 +192,17 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
     int64_t k = 0;
     for (int64_t row = cid; row < a.rows; row += G, ++k) {
         // the label and x[label], fetched early by the thread that writes the loss
+        const float *rp = row_start(a, row);  // the same for every CTA of the cluster
         int64_t label = 0;
         float xl = 0.0f;
         bool lab_ok = true;
         if (kStats && rank == 0 && tid == 0) {
             label = a.labels[row] - a.col0;  // col0: 0 but for a vocab slice
             lab_ok = label_valid(label, a.vocab);
-            if (lab_ok) xl = a.logits[row * a.stride + label];
+            if (lab_ok && rp) xl = rp[label];
         }
         RowState st = empty_state();
-        if (n > 0) st = scan_global<kStats>(a.logits + row * a.stride + c0, c0, n);
+        if (n > 0 && rp) st = scan_global<kStats>(rp + c0, c0, n);
         st = block_reduce_w0<kStats>(st, red);
         if (tid == 0) push_xchg_publish(xg, k, rank, C, st, 0.0f);
         if (tid < 32) {
@@ -207,7 +217,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
                     a.loss[row] = row_loss(g, xl, lab_ok);
                     if (!lab_ok) atomicAdd(&g_status[0], 1ull);
                 }
-                if (a.top) a.top[row] = row_token(g);
+                if (a.top) a.top[row] = rp ? row_token(g) : __int_as_float(0x7fffffff);
             }
         }
         __syncthreads();  // red is rewritten for the next row
@@ -230,15 +240,16 @@ __global__ void __launch_bounds__(256) k_rows_warp(Args a) {
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < a.rows;
          row += nwarps) {
+        const float *rp = row_start(a, row);
         int64_t label = 0;
         float xl = 0.0f;
         bool lab_ok = true;
         if (kStats && lane == 0) {
             label = a.labels[row] - a.col0;  // col0: 0 but for a vocab slice
             lab_ok = label_valid(label, a.vocab);
-            if (lab_ok) xl = a.logits[row * a.stride + label];
+            if (lab_ok && rp) xl = rp[label];
         }
-        RowState g = scan_global<kStats>(a.logits + row * a.stride, 0, a.vocab, lane, 32);
+        RowState g = rp ? scan_global<kStats>(rp, 0, a.vocab, lane, 32) : empty_state();
         g = warp_reduce<kStats>(g);
         if (lane == 0) {
             if (kStats && a.stats) {
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(256) k_rows_warp(Args a) {
                 a.loss[row] = row_loss(g, xl, lab_ok);
                 if (!lab_ok) atomicAdd(&g_status[0], 1ull);
             }
-            if (a.top) a.top[row] = row_token(g);
+            if (a.top) a.top[row] = rp ? row_token(g) : __int_as_float(0x7fffffff);
         }
     }
 }
@@ -1053,10 +1064,10 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
     const int nfull = a.vocab / kCandThreads;                     // blocks with every column < vocab
     if (C > 1) cluster_arrive();  // matched before the first write to CTA 0
     for (int64_t row = cid; row < a.rows; row += GC) {
-        const float *p = a.logits + row * a.stride;
+        const float *p = row_start(a, row);  // null: a row without values
         TopList L;
         top_init(L);
-        int j = ri;
+        int j = p ? ri : nb;
         for (; j + (kLaneUnroll - 1) * Ci < nfull; j += kLaneUnroll * Ci) {
             float x[kLaneUnroll];
 #pragma unroll
@@ -1074,7 +1085,7 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
         }
         // a list with an empty slot takes, in column order, its columns that
         // hold -inf (the scan kept every larger value already)
-        if (L.c[3] == kEmptyCol) {
+        if (p && L.c[3] == kEmptyCol) {
             int r = 0;
 #pragma unroll
             for (int k = 0; k < kTopEach; ++k) r += L.c[k] != kEmptyCol;

@@ -21,7 +21,8 @@ def test_exports_every_declared_function(lib):
                           "ce_status_string",
                           "ce_version", "ce_last_cuda_error", "ce_device_error_count",
                           "ce_device_error_reset", "ce_debug_force", "ce_plan", "softmax_rows",
-                          "log_softmax_rows", "candidates_rows", "split_sum", "argmax_rows_noalloc"}
+                          "log_softmax_rows", "candidates_rows", "split_sum", "argmax_rows_noalloc",
+                          "argmax_rows_indirect", "candidates_rows_indirect"}
     missing = [n for n in names if not hasattr(lib, n)]
     assert not missing, f"declared but not exported: {missing}"
 
@@ -129,6 +130,18 @@ def test_vocab_sharded_validation(lib):
     assert lib.ce_grad_from_stats(V(256), 4, 10, 10, 0, V(512), V(1032), 1.0, V(8192), None) == ce.CE_EALIGN
     assert lib.ce_grad_from_stats(V(4096), 4, 10, 12, 0, V(512), V(1024), 1.0, V(4096), None) == ce.CE_EINVAL
     assert lib.ce_grad_from_stats(V(256), 4, 10, 10, 0, V(512), None, 1.0, V(8192), None) == ce.CE_EINVAL
+
+
+def test_indirect_validation(lib):
+    for fn in (lib.argmax_rows_indirect, lib.candidates_rows_indirect):
+        assert fn(None, 4, 10, V(4096), None) == ce.CE_EINVAL                 # no table
+        assert fn(V(4100), 4, 10, V(4096), None) == ce.CE_EALIGN              # table not 8-byte aligned
+        assert fn(V(4096), 4, 0, V(8192), None) == ce.CE_EINVAL               # vocab < 1
+        assert fn(V(4096), 4, (1 << 24) + 1, V(8192), None) == ce.CE_EINVAL   # token not exact in f32
+        assert fn(V(4096), -1, 10, V(8192), None) == ce.CE_EINVAL
+        assert fn(V(4096), 4, 10, None, None) == ce.CE_EINVAL                 # no output
+        assert fn(V(4096), 4, 10, V(8194), None) == ce.CE_EALIGN
+        assert fn(None, 0, 10, None, None) == ce.CE_OK                        # nothing launched
 
 
 def test_zero_rows_is_a_no_op_without_device(lib):
