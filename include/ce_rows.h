@@ -123,8 +123,8 @@ CE_API int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t str
  * over `rows` rows of `stride` elements, the index of the largest of the
  * first `vocab` entries -- the first of equals; NaN never wins; a row with
  * no non-NaN entry gives 0 -- written as f32 (exact, since vocab <= 2^24)
- * into top[rows]. Only the direct form (rows at logits + i * stride); the
- * page's indirect form over head blocks is not provided.
+ * into top[rows]. The direct form (rows at logits + i * stride); for rows
+ * given by a table of addresses see argmax_rows_indirect.
  *   logits:    [rows, stride] f32, read only.   top: [rows] f32, written.
  *   workspace: NULL, or workspace_bytes of device memory (8-byte aligned,
  *              any contents, owned by the caller, not read by the host) that
@@ -211,7 +211,8 @@ CE_API int log_softmax_rows(const float *logits, int64_t rows, int64_t vocab, in
  * float 2(4t + k) is thread t's rank-k value and float 2(4t + k) + 1 its
  * column as f32 (exact, vocab <= 2^24); a slot for which thread t read no
  * value holds (-inf, -1). Bit-exact: the values are copies of the logits.
- * Only the direct form (rows at logits + i * stride), as argmax_rows.
+ * The direct form (rows at logits + i * stride); for rows given by a table of
+ * addresses see candidates_rows_indirect.
  *   logits: [rows, stride] f32, read only.
  *   cand:   [rows, 2048] f32, written; must not overlap the logits.
  */
