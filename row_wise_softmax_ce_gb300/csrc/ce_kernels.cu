@@ -1,5 +1,6 @@
 // ce_kernels.cu -- sm_103a kernels of the row-wise softmax cross-entropy
-// path and their launchers.
+// path and of the rows a language model's step reads beside it, and their
+// launchers.
 //
 // What they compute is defined on the API reference page "gizml:netops"
 // (gizstack.com/docs/reference/gizml/netops.md), section Functions:
@@ -7,23 +8,32 @@
 //   crossEntropyLoss  the mean of the row losses in f64
 //   crossEntropyGrad  (softmax - onehot) * scale, softmax = exp(x - m) * f32(1/sum)
 //   argmaxInto        each row's token (first of equals, NaN never wins) as f32
+//   candidatesInto    each row's sampling candidates (TOP_EACH per thread of 256)
+//   splitSumInto      the join of split partial sums
 // and section Methods: Tensor.argmax (the tie and NaN rules).
 //
-// Kernel families (every one HBM-bound; none uses tensor cores):
+// Kernel families (every one HBM-bound by design; none uses tensor cores):
 //   k_rows_stream   one read of each logit: the online (m, t, idx) state of
 //                   each thread's columns, merged over the CTA and then over
 //                   the CTAs of a thread-block cluster that share one row
-//                   through distributed shared memory. Writes the row loss
-//                   and/or the argmax token.
-//   k_grad_staged   fused loss + gradient: the cluster's CTAs bulk-copy
-//                   (TMA engine) their slices of a row into shared memory,
-//                   compute the state from there, exchange it over DSMEM,
-//                   then write the gradient from shared memory. HBM sees
-//                   each logit read once and each gradient written once.
+//                   through distributed shared memory. Writes the row loss,
+//                   the argmax token, or a vocab slice's statistics.
+//   k_rows_warp     the same for many moderate rows, one warp per row.
+//   k_grad_staged   fused loss + gradient (or softmax / log-softmax rows): the
+//                   cluster's CTAs bulk-copy (TMA engine) their slices of a
+//                   row into shared memory, compute the state from there,
+//                   exchange it over DSMEM, then write from shared memory. HBM
+//                   sees each logit read once and each output written once.
 //   k_grad_stream   the same for rows too long to stage: two reads.
+//   k_grad_ring     a persistent warp-specialized alternative (forced only).
+//   k_argmax_flat   argmax of few long rows split evenly over the GPU, with
+//                   k_argmax_combine (forced, and the no-allocation call).
+//   k_candidates    sampling candidates, one list per thread.
+//   k_split_sum     split sums in one resident wave.
+//   k_stats_combine / k_grad_from_stats  the vocab-sharded loss and gradient.
 //   k_mean          the mean of the row losses, an f64 fixed-shape tree.
 //
-// Every kernel loops over rows (row = cluster id, + number of clusters), so
+// The row kernels loop over rows (row = cluster id, + number of clusters), so
 // any row count fits one launch.
 #include <algorithm>
 #include <cmath>
