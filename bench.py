@@ -11,11 +11,14 @@ Printed (one JSON line, rank 0):
   roofline    the dominant kernel (the fused one) against measured HBM bandwidth
   argmax      rows/s of argmax_rows on the decode workload (256 x 151936,
               row stride 152064), L2 flushed before every timed launch
+  candidates  rows/s of candidates_rows on the same decode batch, likewise
   e2e         the same metric with the inputs copied from pinned host memory
               and the mean loss and tokens copied back inside the timed region
   cpu_baseline the CPU oracle (f64) timed on the host cores on a row sample
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --case grad|rows|argmax|softmax|log_softmax|candidates|split_sum|sharded
+                    [--workload W] [--rows R] [--force "path,cluster,threads;..."] [--flush]
 
 With N > 1 (launched by torch.distributed.run) every rank runs its own batch
 on its own GPU (rows are independent: weak scaling, no collective on the
@@ -332,7 +335,22 @@ def run_ours(args):
         times.append((e0, e1))
     torch.cuda.synchronize()
     arg_ms = max_over_ranks(statistics.median(a.elapsed_time(c) for a, c in times), ws)
-    del flush, bd
+    # sampling candidates (candidatesInto) of the same decode batch, L2 flushed too
+    cand = torch.empty((wd.rows, ce.CANDIDATE_ROW), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        ce.candidates_rows(bd.logits, vocab=wd.vocab, out=cand)
+    times = []
+    for _ in range(n_arg):
+        l2_flush(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ce.candidates_rows(bd.logits, vocab=wd.vocab, out=cand)
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    cand_ms = max_over_ranks(statistics.median(a.elapsed_time(c) for a, c in times), ws)
+    cand_bytes = 4 * wd.rows * wd.vocab + 4 * ce.CANDIDATE_ROW * wd.rows
+    del flush, bd, cand
 
     # ---- end to end: inputs from pinned host memory, results back to the host
     xh = torch.empty((R, V), dtype=torch.float32, pin_memory=True)
@@ -398,6 +416,11 @@ def run_ours(args):
                        "GB/s": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9, 1),
                        "frac": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9 / peak, 4),
                        "l2": "flushed before each launch"},
+            "candidates": {"workload": wd.name, "rows_per_s": round(ws * wd.rows / (cand_ms * 1e-3), 1),
+                           "ms": round(cand_ms, 5),
+                           "GB/s": round(cand_bytes / (cand_ms * 1e-3) / 1e9, 1),
+                           "frac": round(cand_bytes / (cand_ms * 1e-3) / 1e9 / peak, 4),
+                           "l2": "flushed before each launch"},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
             "gpu_launches": 2 * K,

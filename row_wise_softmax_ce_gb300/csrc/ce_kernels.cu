@@ -1261,12 +1261,14 @@ __global__ void __launch_bounds__(256) k_stats_combine(const float4 *__restrict_
 
 // One CTA per row (looping): grad[j] = (exp(x_j - M) * f32(1/(1 + T)) - [col0
 // + j == label]) * scale over the slice, dense [rows, vocab]; NaN rows where
-// the whole row is degenerate. Loads and stores are coherent (grad may be the
-// slice itself when the slice is dense).
+// the whole row is degenerate. 16-byte loads and stores when the row and its
+// gradient row share their 16-byte phase (a scalar head, vectors, a scalar
+// tail), single floats otherwise. Loads and stores are coherent (grad may be
+// the slice itself when the slice is dense).
 constexpr int kGradStatsUnroll = 4;
 
 __global__ void __launch_bounds__(256) k_grad_from_stats(Args a, const float4 *__restrict__ combined) {
-    const int T = blockDim.x;
+    const int T = blockDim.x, tid = threadIdx.x;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const float4 st = combined[row];
         const float M = st.x;
@@ -1277,21 +1279,40 @@ __global__ void __launch_bounds__(256) k_grad_from_stats(Args a, const float4 *_
         const int lab = (local >= 0 && local < a.vocab) ? static_cast<int>(local) : -1;
         const float *p = a.logits + row * a.stride;
         float *g = a.grad + row * static_cast<int64_t>(a.vocab);
-        int j = threadIdx.x;
-        for (; j + (kGradStatsUnroll - 1) * T < a.vocab; j += kGradStatsUnroll * T) {
-            float x[kGradStatsUnroll];
+        auto one = [&](int j, float x) {
+            const float e = exp_le0(x - M);
+            return j == lab ? (e * rcp - 1.0f) * a.scale : e * cm;
+        };
+        const int offp = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+        const int offg = static_cast<int>((reinterpret_cast<uintptr_t>(g) >> 2) & 3);
+        int head = a.vocab, nvec = 0;
+        if (offp == offg) {
+            head = min(a.vocab, (4 - offp) & 3);
+            nvec = (a.vocab - head) >> 2;
+        }
+        // the scalar head (or the whole row when the phases differ)
+        for (int j = tid; j < head; j += T) __stcs(g + j, one(j, __ldcs(p + j)));
+        const float4 *pv = reinterpret_cast<const float4 *>(p + head);
+        float4 *gv = reinterpret_cast<float4 *>(g + head);
+        int q = tid;
+        for (; q + (kGradStatsUnroll - 1) * T < nvec; q += kGradStatsUnroll * T) {
+            float4 x[kGradStatsUnroll];
 #pragma unroll
-            for (int u = 0; u < kGradStatsUnroll; ++u) x[u] = __ldcs(p + j + u * T);
+            for (int u = 0; u < kGradStatsUnroll; ++u) x[u] = __ldcs(pv + q + u * T);
 #pragma unroll
             for (int u = 0; u < kGradStatsUnroll; ++u) {
-                const float e = exp_le0(x[u] - M);
-                __stcs(g + j + u * T, j + u * T == lab ? (e * rcp - 1.0f) * a.scale : e * cm);
+                const int j = head + 4 * (q + u * T);
+                __stcs(gv + q + u * T, make_float4(one(j, x[u].x), one(j + 1, x[u].y), one(j + 2, x[u].z),
+                                                   one(j + 3, x[u].w)));
             }
         }
-        for (; j < a.vocab; j += T) {
-            const float e = exp_le0(__ldcs(p + j) - M);
-            __stcs(g + j, j == lab ? (e * rcp - 1.0f) * a.scale : e * cm);
+        for (; q < nvec; q += T) {
+            const float4 x = __ldcs(pv + q);
+            const int j = head + 4 * q;
+            __stcs(gv + q, make_float4(one(j, x.x), one(j + 1, x.y), one(j + 2, x.z), one(j + 3, x.w)));
         }
+        // the scalar tail
+        for (int j = head + 4 * nvec + tid; j < a.vocab; j += T) __stcs(g + j, one(j, __ldcs(p + j)));
     }
 }
 
