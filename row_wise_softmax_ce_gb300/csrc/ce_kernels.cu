@@ -290,20 +290,19 @@ __global__ void __launch_bounds__(256) k_rows_warp(Args a) {
 // T*i of each range c. Per row:
 //   sweep 1  each thread's max m over its vectors, and the first vector
 //            holding it;
-//   sweep 2  e = exp(x - m), kept in place; t = their sum but for the first
-//            element holding m;
+//   sweep 2  t = the sum of exp(x - m) but for the first element holding m
+//            (x stays in shared memory: storing e back measured slower);
 //   merge    over the CTA; then each CTA pushes its state into every CTA of
 //            the cluster (st.async, completing bytes on their mbarrier) and
 //            merges the C states in rank order, so every CTA holds the same
 //            row state -- no cluster barrier per row;
-//   write    grad = e * exp(m - M) * f32(1/(1 + T)) * scale (the label column
+//   write    grad = exp(x - M) * f32(1/(1 + T)) * scale (the label column
 //            less scale) range by range; as soon as a range is written the
 //            bulk copy of the next row's chunk into it starts.
 //
 // The same kernel writes two other rows of the same statistics (kMode):
-//   kModeSoftmax     out = e * exp(m - M) * f32(1/(1 + T)): no label, no scale;
-//   kModeLogSoftmax  out = (x - M) - log1p(T): sweep 2 sums e without storing
-//                    it, so the write reads x back from shared memory.
+//   kModeSoftmax     out = exp(x - M) * f32(1/(1 + T)): no label, no scale;
+//   kModeLogSoftmax  out = (x - M) - log1p(T).
 template <int kMode>
 __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, int cols) {
     constexpr bool kCE = kMode == kModeGrad;
@@ -409,11 +408,10 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                 for (int q = c * W + tid; q < qend; q += T) {
                     const float4 e = exp4_sub(buf4[q], m);
                     acc = __fadd2_rn(acc, __fadd2_rn(make_float2(e.x, e.y), make_float2(e.z, e.w)));
-                    if (!kLog) buf4[q] = e;
                 }
             }
             const float t = acc.x + acc.y;
-            buf[4 * qm + lm] = kLog ? m : 1.0f;
+            buf[4 * qm + lm] = m;
             st = RowState{m, t, jbase + 4 * qm + lm};
         } else {
             // no value above -inf among this thread's columns: the exact
@@ -426,7 +424,6 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
                         const int i = 4 * q + l;
                         const float x = buf[i];
                         if (i >= off && i - off < n) push<true>(st, x, jbase + i);
-                        if (!kLog) buf[i] = x != x ? x : 0.0f;
                     }
                 }
             }
@@ -459,15 +456,13 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         // the output, range by range; each freed range takes the next
         // row's chunk
         const float M = h.bc[0], rcp = h.bc[1];
-        const float shift = (m != -INFINITY && M != m) ? exp_le0(m - M) : 1.0f;
-        const float sr = shift * rcp;
-        const float cm = sr * scale;
+        const float cm = rcp * scale;
         float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;  // column c0
         const bool vec_store = ((reinterpret_cast<uintptr_t>(gp) >> 2) & 3) == static_cast<uintptr_t>(off);
         for (int c = 0; c < kChunks; ++c) {
             const int qend = min(nq, (c + 1) * W);
             for (int q = c * W + tid; q < qend; q += T) {
-                const float4 g = kLog ? sub2_4(buf4[q], M, rcp) : mul4(buf4[q], cm);
+                const float4 g = kLog ? sub2_4(buf4[q], M, rcp) : mul4(exp4_sub(buf4[q], M), cm);
                 if (vec_store && static_cast<unsigned>(q - qa) < static_cast<unsigned>(nvec)) {
                     __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
                 } else {
@@ -481,7 +476,7 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
             // the label column: its owner stored e * c there above; this
             // later store by the same thread replaces it
             if (lab_q >= c * W && lab_q < qend && owner(lab_q) == tid)
-                __stcs(gp + lab_local, (buf[lab_f] * sr - 1.0f) * scale);
+                __stcs(gp + lab_local, (exp_le0(buf[lab_f] - M) * rcp - 1.0f) * scale);
             if (more) {
                 __syncthreads();  // range c is free
                 if (tid == 0) {
