@@ -400,3 +400,26 @@ def test_step_replayed_from_a_cuda_graph(orc):
     assert_log_softmax(logp, orc.log_softmax(x.numpy(), V), "graph log-softmax")
     for m, (x, y) in zip(means, batches):
         assert_mean(m.item(), orc.ce_mean(orc.ce_rows(x.numpy(), V, y.numpy())), "graph mean")
+
+
+def test_every_row_family_gives_the_same_bits_every_run():
+    """Fixed-shape reductions and merges: five runs, identical bits (a race in a
+    split-row combine or an exchange would show as a difference)."""
+    x, y = W.random_logits(300, 20011, sigma=3.0, seed=44)
+    xd, yd = x.to(DEV), y.to(DEV)
+    cuts = [0, 7001, 13000, 20011]
+    parts = xd[:4].contiguous()
+    runs = []
+    for _ in range(5):
+        out = {
+            "softmax": ce.softmax_rows(xd), "log_softmax": ce.log_softmax_rows(xd),
+            "candidates": ce.candidates_rows(xd), "split_sum": ce.split_sum(parts),
+        }
+        stats = torch.stack([ce.ce_stats(xd, yd, col0=a, vocab=b - a) for a, b in zip(cuts, cuts[1:])])
+        loss, top, comb = ce.ce_stats_combine(stats, yd, cuts[-1])
+        out.update(stats=stats, sharded_loss=loss, sharded_top=top, combined=comb)
+        torch.cuda.synchronize()
+        runs.append({k: v.cpu().numpy().copy() for k, v in out.items()})
+    for k in runs[0]:
+        for r in runs[1:]:
+            assert np.array_equal(runs[0][k].view(np.int32), r[k].view(np.int32)), k
