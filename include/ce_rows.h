@@ -330,7 +330,7 @@ CE_API int ce_device_error_reset(ce_stream_t stream);
 /*
  * Launch-plan override, for tests and tuning: forces the kernel family
  * (path: 0 automatic, 1 shared-memory-staged (persistent), 2 streaming from
- * global, 3 persistent ring of bulk copies (ce_grad only), 4
+ * global, 3 refused (formerly a ring-of-copies kernel), 4
  * shared-memory-staged with one row per cluster, 5 argmax split evenly over
  * the GPU -- needs a workspace, 6 one warp per row -- ce_rows, ce_loss,
  * argmax_rows and ce_stats only), the CTAs that share one row (cluster: 0

@@ -166,27 +166,6 @@ bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &
     return true;
 }
 
-// Launch shape of the persistent ring kernel: one 256-thread CTA per SM;
-// the fewest CTAs per row whose slices are at most 128 KB (so that the second
-// read of a slice finds it in L2); as many clusters as fit at once.
-bool plan_ring(Plan &p, int64_t rows, int64_t vocab, int cluster) {
-    p.path = kPathRing;
-    p.threads = kRingThreads;
-    int64_t c = cluster ? cluster : std::max<int64_t>(1, ceil_div(vocab * 4, 128 * 1024));
-    if (c > kMaxCluster) c = kMaxCluster;
-    p.cluster = static_cast<int>(c);
-    p.cols = round_up4(ceil_div(vocab, c));
-    p.smem = kRingSmemBytes;
-    int active = 0;
-    if (max_active_clusters(p, kOpGrad, &active) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
-    }
-    if (active < 1) return false;
-    p.clusters = std::min<int64_t>(rows, active);
-    return true;
-}
-
 // The even split of few long rows (argmax only): two 512-thread CTAs per SM,
 // each CTA at least 8192 elements. Taken only when forced (path 5): measured
 // on GB300 it is not yet ahead of the cluster split (256 x 151936, L2
@@ -239,10 +218,8 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
     }
     Plan p;
     if (op == kOpGrad || op == kOpSoftmax || op == kOpLogSoftmax) {
-        if (f.path == kPathRing) {
-            // the ring kernel writes the gradient only
-            if (op != kOpGrad || (f.threads && f.threads != kRingThreads)) return CE_EINVAL;
-            if (!plan_ring(p, rows, vocab, f.cluster)) return CE_EINVAL;
+        if (f.path == kPathRetired3) {
+            return CE_EINVAL;
         } else if (f.path == kPathStaged || f.path == kPathStagedPerRow) {
             if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, f.path == kPathStagedPerRow, false))
                 return CE_EINVAL;

@@ -308,57 +308,6 @@ __device__ __forceinline__ RowState warp_reduce(RowState s) {
     return s;
 }
 
-// Push a block of N 16-byte vectors (columns j[u] .. j[u] + 3, increasing in
-// u) whose valid[u] is set: the block's max cm first, then every exp against
-// max(m, cm), so the N * 4 exps are independent.
-//   cm <= m (m above -inf): t += sum exp(x - m) (ties add 1, NaN poisons).
-//   cm >  m: the old max becomes an ordinary term, t <- (1 + t) exp(m - cm),
-//            then the block adds exp(x - cm) over x != cm plus (count of
-//            x == cm) - 1 -- exact integers for the ties, so nothing cancels;
-//            idx <- the first column holding cm.
-//   no value above -inf yet, in the state or the block: the exact update.
-template <int N>
-__device__ __forceinline__ void push_block(RowState &s, const float4 (&x)[N], const int (&j)[N],
-                                           const bool (&valid)[N]) {
-    float cm = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < N; ++u)
-        if (valid[u]) cm = fmaxf(cm, max4(x[u]));
-    if (cm <= s.m && s.m != -INFINITY) {
-        float acc[N];
-#pragma unroll
-        for (int u = 0; u < N; ++u) {
-            acc[u] = valid[u] ? (exp_le0(x[u].x - s.m) + exp_le0(x[u].y - s.m)) +
-                                    (exp_le0(x[u].z - s.m) + exp_le0(x[u].w - s.m))
-                              : 0.0f;
-        }
-#pragma unroll
-        for (int u = 0; u < N; ++u) s.t += acc[u];
-    } else if (cm > s.m) {
-        float acc = 0.0f;
-        int cnt = 0, first = kNoIndex;
-#pragma unroll
-        for (int u = 0; u < N; ++u) {
-            if (!valid[u]) continue;
-            const float v[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-#pragma unroll
-            for (int l = 0; l < 4; ++l) {
-                const bool eq = v[l] == cm;
-                acc += eq ? 0.0f : exp_le0(v[l] - cm);
-                cnt += eq ? 1 : 0;
-                first = (eq && first == kNoIndex) ? j[u] + l : first;
-            }
-        }
-        const float keep = (s.m == -INFINITY) ? 0.0f : exp_le0(s.m - cm);
-        s.t = fmaf(1.0f + s.t, keep, acc) + static_cast<float>(cnt - 1);
-        s.m = cm;
-        s.idx = first;
-    } else {
-#pragma unroll
-        for (int u = 0; u < N; ++u)
-            if (valid[u]) push4<true>(s, x[u], j[u]);
-    }
-}
 
 // Reduce over the CTA into warp 0: every lane of warp 0 returns the CTA's
 // state (other warps return garbage). `red` holds >= 32 states in shared

@@ -11,7 +11,7 @@ enum Path : int {
     kPathAuto = 0,
     kPathStaged = 1,
     kPathStream = 2,
-    kPathRing = 3,
+    kPathRetired3 = 3,  // once a ring-of-copies kernel; now refused
     kPathStagedPerRow = 4,
     kPathFlat = 5,
     kPathWarp = 6,  // one warp per row (ce_rows, argmax, slice statistics of many short rows)
@@ -38,13 +38,6 @@ constexpr int kMaxCluster = 16;
 // Largest CTA each kernel family is compiled for (its __launch_bounds__).
 constexpr int kStagedMaxThreads = 256;
 constexpr int kStreamMaxThreads = 256;
-// The persistent ring kernel: CTA size (8 consumer warps + 1 producer warp),
-// chunks in flight (16 KB each), and its dynamic shared memory (header + ring).
-constexpr int kRingThreads = 288;
-constexpr int kRingSlots = 13;
-constexpr int kRingHeaderBytes = 2048;
-constexpr int kRingSmemBytes = kRingHeaderBytes + kRingSlots * (kRingThreads - 32) * 4 * 16;
-
 struct Plan {
     int path = kPathStream;
     int cluster = 1;       // CTAs per row (a thread-block cluster)
@@ -81,7 +74,7 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev);
 cudaError_t max_active_clusters(const Plan &p, Op op, int *n);
 
 cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStream_t s);
-// the two-pass kernels (staged, stream or ring, as p.path says) for kOpGrad,
+// the two-pass kernels (staged or stream, as p.path says) for kOpGrad,
 // kOpSoftmax or kOpLogSoftmax; the output row goes to a.grad
 cudaError_t launch_fused(const Plan &p, Op op, const Args &a, cudaStream_t s);
 // cand: rows * kCandRow floats

@@ -25,7 +25,6 @@
 //                   exchange it over DSMEM, then write from shared memory. HBM
 //                   sees each logit read once and each output written once.
 //   k_grad_stream   the same for rows too long to stage: two reads.
-//   k_grad_ring     a persistent warp-specialized alternative (forced only).
 //   k_argmax_flat   argmax of few long rows split evenly over the GPU, with
 //                   k_argmax_combine (forced, and the no-allocation call).
 //   k_candidates    sampling candidates, one list per thread.
@@ -567,343 +566,6 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
 }
 
 // ---------------------------------------------------------------------------
-// k_grad_ring: fused loss + gradient (+ token), persistent, on a ring of bulk
-// copies.
-//
-// One CTA per SM: 8 consumer warps and 1 producer warp. A cluster of C CTAs
-// shares each row (CTA `rank` owns columns [rank * cols, rank * cols + cols));
-// cluster `cid` of G takes rows cid, cid + G, ... The producer keeps a ring of
-// kSlots chunks (16 KB: 4 vectors per consumer thread) in shared memory full
-// with bulk copies, in the order the consumers take them:
-//   P1(row 0), then for k = 0, 1, ...: P1(row k+1), P2(row k).
-// A consumer warp frees a slot by arriving on its "empty" mbarrier; nothing
-// synchronises the whole CTA per chunk.
-// P1 streams the row slice from HBM into each thread's online state (max,
-// first index, exp-sum), block by block. The CTA's state is then pushed to
-// every CTA of the cluster (st.async into their shared memory, completing
-// bytes on their mbarrier): no cluster barrier per row. P2 streams the slice
-// again -- from L2, as only one slice per SM has been read in between -- and
-// writes the gradient. Doing P1 of the next row before P2 of this one hides
-// the exchange. Four exchange slots: a peer can run at most three row states
-// ahead of a CTA that has not yet read a slot.
-namespace ring {
-
-constexpr int kConsumers = kRingThreads - 32;  // 8 warps
-constexpr int kWarps = kConsumers / 32;
-constexpr int kRingUnroll = 4;
-constexpr int kVpc = kConsumers * kRingUnroll;  // 16-byte vectors per chunk
-constexpr int kSlots = kRingSlots;
-constexpr int kXSlots = 4;
-
-struct alignas(16) Header {
-    Xchg xchg[kXSlots][kMaxCluster];  // row states pushed by the cluster's CTAs
-    uint64_t full[kSlots];
-    uint64_t empty[kSlots];
-    uint64_t xbar[kXSlots];
-    RowState red[kWarps];
-    float bc[2][2];  // per row parity: M, f32(1/sum)
-    float xl;        // x[label], found in this CTA's slice during P1
-};
-static_assert(sizeof(Header) <= kRingHeaderBytes, "ring header too large");
-static_assert(kRingHeaderBytes % 128 == 0, "ring data must stay 128-byte aligned");
-static_assert(kRingSmemBytes == kRingHeaderBytes + kSlots * kVpc * 16, "ring size");
-
-// A CTA's slice of one row: p -> column c0; `head` scalar columns up to the
-// first 16-byte boundary, `nvec` whole vectors, then `tail` scalar columns.
-struct Geo {
-    const float *p;
-    int head, nvec, tail, nch;
-};
-
-__device__ __forceinline__ Geo geo(const Args &a, int64_t row, int c0, int n) {
-    Geo g;
-    g.p = a.logits + row * a.stride + c0;
-    const int off = static_cast<int>((reinterpret_cast<uintptr_t>(g.p) >> 2) & 3);
-    g.head = min(n, (4 - off) & 3);
-    g.nvec = (n - g.head) >> 2;
-    g.tail = n - g.head - 4 * g.nvec;
-    g.nch = (g.nvec + kVpc - 1) / kVpc;
-    return g;
-}
-
-__device__ __forceinline__ float lane_of(float4 v, int l) {
-    return l == 0 ? v.x : l == 1 ? v.y : l == 2 ? v.z : v.w;
-}
-
-// barrier among the consumer warps only
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-}  // namespace ring
-
-__global__ void __launch_bounds__(kRingThreads, 1) k_grad_ring(Args a, int cols) {
-    using namespace ring;
-    extern __shared__ __align__(128) unsigned char smem[];
-    Header &h = *reinterpret_cast<Header *>(smem);
-    float4 *ringv = reinterpret_cast<float4 *>(smem + kRingHeaderBytes);
-    const uint32_t rank = cluster_rank(), C = cluster_size();
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int c0 = static_cast<int>(rank) * cols;
-    const int n = max(0, min(a.vocab, c0 + cols) - c0);
-    const int64_t cid = cluster_id_x(), G = cluster_count_x();
-    const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;  // rows of this cluster
-    const float scale = a.scale;
-    bool failed = false;
-
-    if (tid == 0) {
-        for (int i = 0; i < kSlots; ++i) {
-            mbar_init(&h.full[i], 1);
-            mbar_init(&h.empty[i], kWarps);
-        }
-        for (int i = 0; i < kXSlots; ++i) mbar_init(&h.xbar[i], 1);
-        fence_mbar_init();
-        // each exchange slot expects C row states for its first row
-        for (int i = 0; i < kXSlots; ++i)
-            if (i < K) mbar_arrive_expect_tx(&h.xbar[i], 16u * C);
-    }
-    __syncthreads();
-    cluster_arrive();  // every CTA's barriers exist before a peer pushes to them
-    cluster_wait();
-
-    if (warp == kWarps) {
-        // ---------------- producer warp (lane 0 issues) ----------------
-        if (lane == 0) {
-            const uint64_t pol_keep = l2_policy_evict_last();
-            const uint64_t pol_stream = l2_policy_evict_first();
-            uint32_t issued = 0;
-            // segment 0: P1(0); 2k+1: P1(k+1); 2k+2: P2(k)
-            for (int64_t seg = 0; seg <= 2 * K; ++seg) {
-                const bool p1 = seg == 0 || (seg & 1);
-                const int64_t rk = seg == 0 ? 0 : (p1 ? (seg + 1) / 2 : (seg - 2) / 2);
-                if (rk >= K) continue;
-                const Geo g = geo(a, cid + rk * G, c0, n);
-                for (int c = 0; c < g.nch; ++c, ++issued) {
-                    const int slot = static_cast<int>(issued % kSlots);
-                    if (issued >= static_cast<uint32_t>(kSlots) && !failed)
-                        failed = !mbar_wait_bounded(&h.empty[slot], ((issued / kSlots) - 1) & 1u);
-                    const int v0 = c * kVpc;
-                    const uint32_t bytes = static_cast<uint32_t>(min(kVpc, g.nvec - v0)) * 16u;
-                    mbar_arrive_expect_tx(&h.full[slot], bytes);
-                    bulk_copy_g2s(ringv + slot * kVpc, g.p + g.head + 4 * v0, bytes, &h.full[slot],
-                                  p1 ? pol_keep : pol_stream);
-                }
-            }
-        }
-        __syncwarp();
-    } else {
-        // ---------------- consumer warps ----------------
-        uint32_t s = 0;  // chunks consumed
-        auto wait_chunk = [&]() -> const float4 * {
-            const int slot = static_cast<int>(s % kSlots);
-            if (!failed) failed = !mbar_wait_bounded(&h.full[slot], (s / kSlots) & 1u);
-            return ringv + slot * kVpc;
-        };
-        auto release_chunk = [&]() {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&h.empty[s % kSlots]);
-            ++s;
-        };
-        auto label_at = [&](int64_t row, const Geo &g, int *ll, int *lab_v, bool *lab_ok) {
-            const int64_t label = a.labels[row];
-            *lab_ok = label_valid(label, a.vocab);
-            *ll = (*lab_ok && label >= c0 && label < c0 + n) ? static_cast<int>(label - c0) : -1;
-            *lab_v = (*ll >= g.head && *ll < g.head + 4 * g.nvec) ? (*ll - g.head) >> 2 : -1;
-        };
-
-        // P1: this CTA's state of row k
-        auto pass1 = [&](int64_t k) -> RowState {
-            const int64_t row = cid + k * G;
-            const Geo g = geo(a, row, c0, n);
-            int ll, lab_v;
-            bool lab_ok;
-            label_at(row, g, &ll, &lab_v, &lab_ok);
-            const int jv = c0 + g.head;
-            float hx[3], tx[3];  // the unaligned end columns, loaded early by thread 0
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                hx[i] = (tid == 0 && i < g.head) ? g.p[i] : 0.0f;
-                tx[i] = (tid == 0 && i < g.tail) ? g.p[g.head + 4 * g.nvec + i] : 0.0f;
-            }
-            RowState st = empty_state();
-            for (int c = 0; c < g.nch; ++c) {
-                const float4 *buf = wait_chunk();
-                float4 x[kRingUnroll];
-                int j[kRingUnroll];
-                bool ok[kRingUnroll];
-#pragma unroll
-                for (int u = 0; u < kRingUnroll; ++u) {
-                    const int v = c * kVpc + tid + kConsumers * u;
-                    ok[u] = v < g.nvec;
-                    x[u] = ok[u] ? buf[v - c * kVpc] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    j[u] = jv + 4 * v;
-                    if (v == lab_v) h.xl = lane_of(x[u], (ll - g.head) & 3);
-                }
-                release_chunk();
-                push_block<kRingUnroll>(st, x, j, ok);
-            }
-            if (tid == 0) {
-                RowState se = empty_state();
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    if (i < g.head) {
-                        push<true>(se, hx[i], c0 + i);
-                        if (ll == i) h.xl = hx[i];
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    if (i < g.tail) {
-                        const int col = g.head + 4 * g.nvec + i;
-                        push<true>(se, tx[i], c0 + col);
-                        if (ll == col) h.xl = tx[i];
-                    }
-                }
-                st = merge<true>(st, se);
-            }
-            return st;
-        };
-
-        // push this CTA's state of row k into exchange slot k % 4 of every CTA
-        auto publish = [&](int64_t k, RowState st) {
-            st = warp_reduce<true>(st);
-            if (lane == 0) h.red[warp] = st;
-            consumers_sync();
-            if (warp == 0) {
-                RowState r = lane < kWarps ? h.red[lane] : empty_state();
-                r = warp_reduce<true>(r);
-                if (lane == 0) {
-                    const int64_t label = a.labels[cid + k * G];
-                    const bool mine = label_valid(label, a.vocab) && label >= c0 && label < c0 + n;
-                    const int xs = static_cast<int>(k & (kXSlots - 1));
-                    const float4 v = make_float4(r.m, r.t, __int_as_float(r.idx), mine ? h.xl : 0.0f);
-                    for (uint32_t q = 0; q < C; ++q)
-                        st_async_peer(peer_smem(&h.xchg[xs][rank], q), v, peer_smem(&h.xbar[xs], q));
-                }
-            }
-        };
-
-        // merge the cluster's states of row k; write its loss and token
-        auto finish = [&](int64_t k) {
-            const int xs = static_cast<int>(k & (kXSlots - 1));
-            if (warp == 0) {
-                if (!failed) failed = !mbar_wait_bounded(&h.xbar[xs], static_cast<uint32_t>(k >> 2) & 1u);
-                const int64_t row = cid + k * G;
-                const int64_t label = a.labels[row];
-                const bool lab_ok = label_valid(label, a.vocab);
-                const uint32_t owner = lab_ok ? static_cast<uint32_t>(label / cols) : 0u;
-                RowState q = empty_state();
-                float v = 0.0f;
-                if (lane < static_cast<int>(C)) {
-                    const Xchg x = h.xchg[xs][lane];
-                    q = RowState{x.m, x.t, x.idx};
-                    v = x.xl;
-                }
-                const float xl = __shfl_sync(kFullMask, v, static_cast<int>(owner));
-                const RowState g = warp_reduce<true>(q);
-                if (lane == 0) {
-                    const bool bad = !isfinite(g.m) || isnan(g.t);
-                    h.bc[k & 1][0] = g.m;
-                    h.bc[k & 1][1] = bad ? __int_as_float(0x7fffffff) : 1.0f / (1.0f + g.t);  // f32(1/sum)
-                    if (rank == 0) {
-                        if (a.loss) a.loss[row] = row_loss(g, xl, lab_ok);
-                        if (!lab_ok) atomicAdd(&g_status[0], 1ull);
-                        if (a.top) a.top[row] = row_token(g);
-                    }
-                    if (k + kXSlots < K) mbar_arrive_expect_tx(&h.xbar[xs], 16u * C);  // re-arm for row k + 4
-                }
-            }
-            consumers_sync();
-        };
-
-        // P2: the gradient of row k
-        auto pass2 = [&](int64_t k) {
-            const int64_t row = cid + k * G;
-            const Geo g = geo(a, row, c0, n);
-            int ll, lab_v;
-            bool lab_ok;
-            label_at(row, g, &ll, &lab_v, &lab_ok);
-            const float M = h.bc[k & 1][0], rcp = h.bc[k & 1][1];
-            const float cm = rcp * scale;
-            float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;
-            float *gb = gp + g.head;
-            const bool vec = (reinterpret_cast<uintptr_t>(gb) & 15) == 0;
-            float hx[3], tx[3];
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                hx[i] = (tid == 0 && i < g.head) ? g.p[i] : 0.0f;
-                tx[i] = (tid == 0 && i < g.tail) ? g.p[g.head + 4 * g.nvec + i] : 0.0f;
-            }
-            for (int c = 0; c < g.nch; ++c) {
-                const float4 *buf = wait_chunk();
-                float4 x[kRingUnroll];
-#pragma unroll
-                for (int u = 0; u < kRingUnroll; ++u) {
-                    const int v = c * kVpc + tid + kConsumers * u;
-                    x[u] = v < g.nvec ? buf[v - c * kVpc] : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-                release_chunk();
-#pragma unroll
-                for (int u = 0; u < kRingUnroll; ++u) {
-                    const int v = c * kVpc + tid + kConsumers * u;
-                    if (v < g.nvec) {
-                        const float4 e = make_float4(exp_le0(x[u].x - M), exp_le0(x[u].y - M),
-                                                     exp_le0(x[u].z - M), exp_le0(x[u].w - M));
-                        float4 o = make_float4(e.x * cm, e.y * cm, e.z * cm, e.w * cm);
-                        if (v == lab_v) {
-                            const int l = (ll - g.head) & 3;
-                            const float gl = (lane_of(e, l) * rcp - 1.0f) * scale;
-                            o.x = l == 0 ? gl : o.x;
-                            o.y = l == 1 ? gl : o.y;
-                            o.z = l == 2 ? gl : o.z;
-                            o.w = l == 3 ? gl : o.w;
-                        }
-                        if (vec) {
-                            __stcs(reinterpret_cast<float4 *>(gb) + v, o);
-                        } else {
-                            __stcs(gb + 4 * v, o.x);
-                            __stcs(gb + 4 * v + 1, o.y);
-                            __stcs(gb + 4 * v + 2, o.z);
-                            __stcs(gb + 4 * v + 3, o.w);
-                        }
-                    }
-                }
-            }
-            if (tid == 0) {
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    if (i < g.head) {
-                        const float e = exp_le0(hx[i] - M);
-                        __stcs(gp + i, ll == i ? (e * rcp - 1.0f) * scale : e * cm);
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    if (i < g.tail) {
-                        const int col = g.head + 4 * g.nvec + i;
-                        const float e = exp_le0(tx[i] - M);
-                        __stcs(gp + col, ll == col ? (e * rcp - 1.0f) * scale : e * cm);
-                    }
-                }
-            }
-        };
-
-        if (K > 0) publish(0, pass1(0));
-        for (int64_t k = 0; k < K; ++k) {
-            if (k + 1 < K) publish(k + 1, pass1(k + 1));
-            finish(k);
-            pass2(k);
-        }
-    }
-    cluster_arrive();  // no CTA leaves while a peer may still push to it
-    cluster_wait();
-    if (__syncthreads_or(failed) && tid == 0) atomicAdd(&g_status[1], 1ull);
-}
-
-// ---------------------------------------------------------------------------
 // Argmax of few long rows, split evenly over one wave of CTAs.
 //
 // k_argmax_flat: CTA j of P scans elements [e_j, e_{j+1}), e_j = floor(j E / P),
@@ -1356,7 +1018,6 @@ const void *fused_kernel(int path) {
 
 const void *kernel_of(const Plan &p, Op op) {
     if (op == kOpGrad) {
-        if (p.path == kPathRing) return reinterpret_cast<const void *>(&k_grad_ring);
         return fused_kernel<kModeGrad>(p.path);
     }
     if (op == kOpSoftmax) return fused_kernel<kModeSoftmax>(p.path);
@@ -1380,7 +1041,6 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
                          reinterpret_cast<const void *>(&k_grad_stream<kModeGrad>),
                          reinterpret_cast<const void *>(&k_grad_stream<kModeSoftmax>),
                          reinterpret_cast<const void *>(&k_grad_stream<kModeLogSoftmax>),
-                         reinterpret_cast<const void *>(&k_grad_ring),
                          reinterpret_cast<const void *>(&k_candidates)};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -1395,9 +1055,7 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
     }
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_candidates),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kCandMaxSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_grad_ring),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingSmemBytes);
+    return e;
 }
 
 cudaError_t max_active_clusters(const Plan &p, Op op, int *n) {

@@ -87,13 +87,13 @@ def test_softmax_shapes_and_paths(orc, plan):
                 check_softmaxes(orc, p, lp, x.numpy(), vocab, f"{plan} {rows}x{vocab}")
 
 
-def test_softmax_ring_path_is_rejected():
+def test_retired_path_3_is_refused():
     x = torch.zeros((2, 100), device=DEV)
+    y = torch.zeros((2,), dtype=torch.int64, device=DEV)
     with forced((3, 1, 0)):
-        with pytest.raises(ce.CeError):
-            ce.softmax_rows(x)
-        with pytest.raises(ce.CeError):
-            ce.log_softmax_rows(x)
+        for call in (lambda: ce.softmax_rows(x), lambda: ce.log_softmax_rows(x), lambda: ce.ce_grad(x, y, 1.0)):
+            with pytest.raises(ce.CeError):
+                call()
 
 
 @pytest.mark.parametrize("plan", [(0, 0, 0), (1, 4, 0), (2, 5, 0)], ids=str)
