@@ -19,6 +19,7 @@ Printed (one JSON line, rank 0):
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --case grad|rows|argmax|softmax|log_softmax|candidates|split_sum|sharded
                     [--workload W] [--rows R] [--force "path,cluster,threads;..."] [--flush]
+    python bench.py --report     every operation on every workload
 
 With N > 1 (launched by torch.distributed.run) every rank runs its own batch
 on its own GPU (rows are independent: weak scaling, no collective on the
@@ -542,6 +543,8 @@ def main():
     ap.add_argument("--case", choices=["grad", "rows", "argmax", "softmax", "log_softmax", "candidates",
                                        "split_sum", "sharded"],
                     help="time one operation only (sweeps, profiler captures)")
+    ap.add_argument("--report", action="store_true",
+                    help="time every operation on every workload (one JSON line each)")
     ap.add_argument("--splits", type=int, default=4,
                     help="with --case split_sum: parts to join; with --case sharded: vocab slices")
     ap.add_argument("--workload", choices=sorted(W.WORKLOADS), help="with --case: the workload")
@@ -549,6 +552,18 @@ def main():
     ap.add_argument("--force", default="", help="with --case: path,cluster,threads (see ce_debug_force)")
     ap.add_argument("--flush", action="store_true", help="with --case: flush L2 before each launch")
     args = ap.parse_args()
+    if args.report:
+        # every workload x operation, one JSON line each (L2 flushed for the
+        # workloads smaller than a few L2 sizes)
+        import copy
+        for name, w in W.WORKLOADS.items():
+            small = 4 * w.rows * w.stride < 4 * torch.cuda.get_device_properties(0).L2_cache_size
+            for case in ("rows", "grad", "argmax", "softmax", "candidates"):
+                a = copy.copy(args)
+                a.case, a.workload, a.rows, a.force, a.flush = case, name, 0, "", small
+                a.steps = min(args.steps, 50)
+                run_case(a)
+        return 0
     if args.case:
         return run_case(args)
     if args.impl == "reference":
