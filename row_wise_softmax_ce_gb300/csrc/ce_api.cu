@@ -24,6 +24,7 @@ constexpr int kVersion = 10000;            // 1.0.0
 constexpr int64_t kMaxVocab = 1ll << 24;   // tokens are written exactly as f32
 constexpr int kMaxDevices = 64;
 constexpr int kStagedTargetCols = 16384;   // 64 KB of f32 per CTA: 3 CTAs per SM
+constexpr int kStagedTargetCols4 = 13312;  // 52 KB of f32 per CTA: 4 CTAs per SM
 constexpr int kStreamMinCols = 2048;       // columns per CTA, at least, when a row is split
 constexpr int64_t kMaxClusters = 1ll << 20;
 
@@ -136,25 +137,32 @@ bool plan_warp(Plan &p, Op op, int64_t rows) {
 
 // Launch shape of the staged fused kernel: the fewest CTAs per row whose
 // slices are at most kStagedTargetCols columns (at most 16 CTAs).
+// The staged kernel's geometry for `c` CTAs per row: columns per CTA and the
+// shared memory that covers any row misalignment (4 * kChunks * W floats);
+// false when it does not fit. *active: the clusters resident at once.
+bool staged_shape(Plan &p, Op op, int64_t vocab, const DeviceInfo &dev, int64_t c, int *active) {
+    if (c > kMaxCluster) c = kMaxCluster;
+    p.cluster = static_cast<int>(c);
+    p.cols = round_up4(ceil_div(vocab, c));
+    const int w = ((p.cols + 9) / 4 + 3) / 4;
+    p.smem = kStagedHeaderBytes + 16 * 4 * w;
+    if (p.smem > dev.max_smem_optin) return false;
+    *active = 0;
+    if (max_active_clusters(p, op, active) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return *active >= 1;
+}
+
 bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster,
                  bool per_row, bool auto_form) {
     p.path = kPathStaged;
     p.threads = threads ? threads : 256;
     if (p.threads > kStagedMaxThreads) return false;
-    int64_t c = cluster ? cluster : std::max<int64_t>(1, ceil_div(vocab, kStagedTargetCols));
-    if (c > kMaxCluster) c = kMaxCluster;
-    p.cluster = static_cast<int>(c);
-    p.cols = round_up4(ceil_div(vocab, c));
-    // the kernel's fixed ranges cover any row misalignment: 4 * kChunks * W floats
-    const int w = ((p.cols + 9) / 4 + 3) / 4;
-    p.smem = kStagedHeaderBytes + 16 * 4 * w;
-    if (p.smem > dev.max_smem_optin) return false;
     int active = 0;
-    if (max_active_clusters(p, op, &active) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return false;
-    }
-    if (active < 1) return false;
+    const int64_t c = cluster ? cluster : std::max<int64_t>(1, ceil_div(vocab, kStagedTargetCols));
+    if (!staged_shape(p, op, vocab, dev, c, &active)) return false;
     // persistent (every cluster resident at once, looping over rows), or one
     // row per cluster with the hardware scheduling clusters as others finish.
     // Measured on GB300: persistent is ahead when each cluster loops over
@@ -162,6 +170,20 @@ bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &
     // bandwidth), one row per cluster when it would loop over few (4096 x
     // 32000: 18 rows per cluster, 93% vs 89%).
     if (auto_form) per_row = rows < 32 * static_cast<int64_t>(active);
+    if (auto_form && !cluster && !threads && !per_row) {
+        // persistent: slices small enough for four CTAs per SM pay when they
+        // put more CTAs on the GPU at once. Measured on GB300, 8192 x 128256
+        // (8 CTAs of 66 KB per row, 408 resident: 94.8% of copy bandwidth;
+        // 10 of 53 KB, 580 resident: 98.9%; 9, 11: 87.8%, 96.3%).
+        Plan q = p;
+        int active4 = 0;
+        const int64_t c4 = std::max<int64_t>(1, ceil_div(vocab, kStagedTargetCols4));
+        if (c4 != c && staged_shape(q, op, vocab, dev, c4, &active4) && rows >= 32 * static_cast<int64_t>(active4) &&
+            static_cast<int64_t>(active4) * q.cluster > static_cast<int64_t>(active) * p.cluster) {
+            p = q;
+            active = active4;
+        }
+    }
     p.clusters = per_row ? std::min<int64_t>(rows, kMaxClusters) : std::min<int64_t>(rows, active);
     return true;
 }
