@@ -201,22 +201,23 @@ bool flat_applies(int64_t rows, int64_t vocab, const DeviceInfo &dev, bool force
 int64_t flat_workspace_bytes(int64_t rows, const DeviceInfo &dev) { return 8 * (2 * static_cast<int64_t>(dev.sms) + rows); }
 
 // Launch shape of the candidates kernel: 256 threads (the pages' workgroup);
-// a row split over C CTAs below two rows per SM: 4, or 8 for 32 rows or fewer;
-// each CTA at least 2048 columns. Measured on GB300, rows x 151936, L2
-// flushed (us): 256 rows 56.6 / 55.4 / 57.7 / 53.7 / 78.1 for C = 1 / 2 / 3 /
-// 4 / 8; 128 rows 38.9 / 36.9 / 45.2 for C = 2 / 4 / 8; 64 rows 34.1 / 24.9 /
-// 27.4; 32 rows 33.3 / 22.8 / 21.4.
+// a row split over C = 2 x SMs / rows CTAs (about two per SM), 1 <= C <= 8,
+// each with at least 2048 columns. Measured on GB300, rows x 151936, L2
+// flushed (us, C = 1 / 2 / 3 / 4 / 8): 256 rows 40.6 / 41.0 / 46.5 / 47.1 /
+// 67.6; 128 rows 32.8 / 28.2 / 28.9 / 30.9 / 39.2; 64 rows 33.2 / 22.5 / 24.6
+// / 22.5 / 26.6; 32 rows 32.7 / 22.8 / 20.0 / 18.8 / 18.4.
 void plan_candidates(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int cluster) {
     p.path = kPathStream;
     p.threads = kCandThreads;
     int64_t c = cluster;
     if (!c) {
-        c = rows >= 2 * static_cast<int64_t>(dev.sms) ? 1 : rows > 32 ? 4 : 8;
+        const int64_t target = 2 * static_cast<int64_t>(dev.sms);
+        c = std::max<int64_t>(1, std::min<int64_t>(kCandMaxCluster, target / std::max<int64_t>(1, rows)));
         c = std::min<int64_t>(c, std::min<int64_t>(kCandMaxCluster, ceil_div(vocab, kStreamMinCols)));
     }
     p.cluster = static_cast<int>(std::max<int64_t>(1, c));
     p.cols = round_up4(ceil_div(vocab, p.cluster));
-    p.smem = (p.cluster - 1) * kCandListBytes;
+    p.smem = kCandRingBytes + (p.cluster > 1 ? kCandListBytes : 0);
     p.clusters = std::min<int64_t>(rows, kMaxClusters);
 }
 

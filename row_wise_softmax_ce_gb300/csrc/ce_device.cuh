@@ -46,6 +46,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// atomic add on a shared counter, acquire + release at CTA scope; returns
+// the old value
+__device__ __forceinline__ uint32_t atom_add_acq_rel_smem(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v) : "memory");
+    return old;
+}
+
 // One poll of the phase with the given parity. A thread whose phase has not
 // completed is suspended in hardware (it issues nothing) until the phase
 // completes or about `suspend_ns` nanoseconds pass.

@@ -26,10 +26,22 @@ constexpr int kCandThreads = 256;
 constexpr int kTopEach = 4;
 constexpr int kCandRow = 2 * kCandThreads * kTopEach;
 constexpr int kCandMaxCluster = 8;
-// shared memory of the candidates kernel (split rows): the lists the cluster's
-// other CTAs send to CTA 0
-constexpr int kCandListBytes = kCandThreads * kTopEach * 8;  // one (value, column) list set
-constexpr int kCandMaxSmemBytes = (kCandMaxCluster - 1) * kCandListBytes;
+// Shared memory of the candidates kernel: mbarriers and counters, a ring of
+// kCandStages chunks of a row (kCandChunkBlocks blocks of 256 columns on the
+// 16-byte grid of the logits: up to 3 floats before the chunk and 1 after),
+// and, for rows split over a cluster, the lists CTA 0 pulls from the others.
+// 15 blocks keep a split-row CTA at 54 KB: four fit on an SM.
+constexpr int kCandChunkBlocks = 15;
+constexpr int kCandStages = 3;
+constexpr int kCandStageFloats = kCandChunkBlocks * kCandThreads + 4;
+constexpr int kCandHeaderBytes = 48;
+constexpr int kCandListBytes = kCandThreads * kTopEach * 8;
+constexpr int kCandRingBytes = kCandHeaderBytes + kCandStages * kCandStageFloats * 4;
+constexpr int kCandMaxSmemBytes = kCandRingBytes + kCandListBytes;
+constexpr int kCandCtasPerSm = 4;  // resident CTAs per SM the shared memory allows
+static_assert(kCandStages * 12 <= kCandHeaderBytes && kCandHeaderBytes % 16 == 0 && kCandStageFloats % 4 == 0 &&
+                  kCandCtasPerSm * (kCandMaxSmemBytes + 1024) <= 228 * 1024,
+              "candidates smem layout");
 constexpr int kSplitThreads = 256;
 
 // Per-CTA shared bytes the staged kernel reserves before its row buffer.

@@ -699,96 +699,206 @@ __device__ __forceinline__ float2 slot_of(const TopList &L, int k) {
 
 __device__ __forceinline__ void push_slot(TopList &L, float2 e) { top_push(L, e.x, __float_as_int(e.y)); }
 
-__device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float2 v) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y) : "memory");
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
+// Insert the values whose bits are set in `mask` (bit u: the value of the
+// thread's column col0 + 256 u, read by val(u, col)), in column order: each is
+// later in column order than every pair the list holds, as stream_push needs.
+// The warp runs as many steps as its busiest lane has marks; a lane out of
+// marks inserts -inf, which changes nothing (nor does a marked value that is
+// no longer above the list's 4th).
+template <typename Val>
+__device__ __forceinline__ void insert_marked(TopList &L, uint32_t mask, int col0, Val val) {
+    const int steps = static_cast<int>(__reduce_max_sync(kFullMask, static_cast<unsigned>(__popc(mask))));
+    for (int i = 0; i < steps; ++i) {
+        const int u = __ffs(mask) - 1;  // -1 once the lane's marks are used
+        mask &= mask - 1;
+        const int col = col0 + kCandThreads * u;
+        stream_push(L, u >= 0 ? val(u, col) : -INFINITY, col);
+    }
+}
+
 }  // namespace cand
 
 // k_candidates: thread t of a 256-thread CTA is the pages' logical thread t
-// itself and keeps one list: it reads columns t + 256 j (the warp's 32 loads
-// are 128 contiguous bytes) for the blocks j = rank, rank + C, ... of the
-// cluster's C CTAs. The insertion sits behind a real branch (x > the list's
-// 4th value): the warp runs it when any of its 32 lanes inserts, which late in
-// a list's stream is rarely. The cluster's CTAs merge in CTA 0 through
-// distributed shared memory; CTA 0 writes the row.
-constexpr int kLaneUnroll = 16;  // 4-byte loads in flight per thread
-
+// itself and keeps one sorted list in registers. CTA `rank` of a cluster of C
+// reads the blocks of 256 columns [jr0, jr1) of each of the cluster's rows
+// (an even split of the row's blocks), chunk by chunk: kCandChunkBlocks blocks
+// arrive by one bulk copy into a ring of kCandStages shared-memory stages
+// (mbarrier full[s]), up to kCandStages chunks ahead, across rows: each warp
+// counts itself done with a stage (an acq_rel atomic on used[s]), and the last
+// warp to finish a chunk issues the copy of chunk + kCandStages into it.
+// A chunk sits on the 16-byte grid of the logits (float i of a stage holds
+// column cs - off + i); the at most 3 columns of a row before its first
+// 16-byte boundary and after its last are read from global memory by their
+// threads. Per chunk a thread marks its values above the list's 4th value (as
+// of the chunk's start, never above the current one, so no value that belongs
+// in the list is left out) and then inserts the marked ones: a warp runs the
+// insertion once per value that some lane keeps, not once per value read.
+// For C > 1, CTAs 1..C-1 leave their lists in shared memory and CTA 0 pulls
+// and merges them through distributed shared memory and writes the row.
 __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *__restrict__ out) {
     using namespace cand;
     extern __shared__ __align__(128) unsigned char smem[];
-    float2 *X = reinterpret_cast<float2 *>(smem);  // lists of CTAs 1..C-1 (in CTA 0)
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint32_t *used = reinterpret_cast<uint32_t *>(full + kCandStages);  // warps done with the stage, ever
+    float *stages = reinterpret_cast<float *>(smem + kCandHeaderBytes);
+    float2 *lt = reinterpret_cast<float2 *>(smem + kCandRingBytes) + threadIdx.x;  // this thread's list slots
+    const int t = threadIdx.x, lane = t & 31;
     const uint32_t rank = cluster_rank(), C = cluster_size();
-    const int t = threadIdx.x;
-    const int Ci = static_cast<int>(C), ri = static_cast<int>(rank);
-    const int64_t cid = cluster_id_x(), GC = cluster_count_x();
+    const int64_t cid = cluster_id_x(), G = cluster_count_x();
     const bool vec_out = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
     const int nb = (a.vocab + kCandThreads - 1) / kCandThreads;  // blocks of 256 columns
-    const int nfull = a.vocab / kCandThreads;                     // blocks with every column < vocab
-    if (C > 1) cluster_arrive();  // matched before the first write to CTA 0
-    for (int64_t row = cid; row < a.rows; row += GC) {
+    const int jr0 = static_cast<int>(static_cast<int64_t>(nb) * rank / C);
+    const int jr1 = static_cast<int>(static_cast<int64_t>(nb) * (rank + 1) / C);
+    const int nk = (jr1 - jr0 + kCandChunkBlocks - 1) / kCandChunkBlocks;  // chunks of a row here
+    const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;      // rows of this cluster
+    const int64_t total = K * nk;                                           // chunks this CTA reads
+    constexpr int kChunkCols = kCandChunkBlocks * kCandThreads;
+
+    // A row's 16-byte phase `off` (floats), its columns [0, h) before the
+    // first boundary and [e, vocab) after the last.
+    struct Geom {
+        int off, h, e;
+    };
+    auto geom = [&](const float *p) {
+        const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
+        const int h = min(a.vocab, (4 - off) & 3);
+        return Geom{off, h, h + ((a.vocab - h) & ~3)};
+    };
+    // chunk k of `row` into stage s: the grid-aligned body of its columns [cs, ce)
+    auto issue = [&](int64_t row, int k, int s, uint64_t policy) {
+        const float *p = row_start(a, row);
+        uint32_t bytes = 0;
+        int dst = 0, c_lo = 0;
+        if (p) {
+            const Geom r = geom(p);
+            const int cs = kCandThreads * (jr0 + kCandChunkBlocks * k);
+            const int ce = min(a.vocab, kCandThreads * min(jr0 + kCandChunkBlocks * (k + 1), jr1));
+            c_lo = max(cs - r.off, r.h);
+            const int c_hi = min(cs - r.off + ((ce - cs + r.off + 3) & ~3), r.e);
+            if (c_hi > c_lo) {
+                bytes = 4u * static_cast<uint32_t>(c_hi - c_lo);
+                dst = c_lo - (cs - r.off);
+            }
+        }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        if (bytes) bulk_copy_g2s(stages + s * kCandStageFloats + dst, p + c_lo, bytes, &full[s], policy);
+    };
+
+    constexpr uint32_t kWarps = kCandThreads / 32;
+    const uint64_t policy = l2_policy_evict_first();
+    if (t == 0) {
+        for (int s = 0; s < kCandStages; ++s) {
+            mbar_init(&full[s], 1);
+            used[s] = 0;
+        }
+        fence_mbar_init();
+        int64_t row = cid;
+        for (int k = 0, s = 0; s < kCandStages && row < a.rows && nk > 0; ++s) {
+            issue(row, k, s, policy);
+            if (++k == nk) k = 0, row += G;
+        }
+    }
+    __syncthreads();
+
+    bool failed = false;
+    int s = 0;          // stage of the next chunk
+    uint32_t ph = 0;    // and the parity of its phase
+    // Cluster barrier phases, per row: a wait before the list slots are
+    // written (CTA 0 has pulled the previous row's lists), an arrive once they
+    // are, a wait before the pull, an arrive after it.
+    if (C > 1) cluster_arrive();
+    for (int64_t row = cid; row < a.rows; row += G) {
         const float *p = row_start(a, row);  // null: a row without values
+        const Geom r = p ? geom(p) : Geom{0, 0, 0};
         TopList L;
         top_init(L);
-        int j = p ? ri : nb;
-        for (; j + (kLaneUnroll - 1) * Ci < nfull; j += kLaneUnroll * Ci) {
-            float x[kLaneUnroll];
+        for (int k = 0; k < nk; ++k) {
+            if (!mbar_wait_bounded(&full[s], ph)) failed = true;
+            if (p) {
+                const int cs = kCandThreads * (jr0 + kCandChunkBlocks * k);
+                const int ce = min(a.vocab, kCandThreads * min(jr0 + kCandChunkBlocks * (k + 1), jr1));
+                const float *sv = stages + s * kCandStageFloats + r.off + t;  // sv[256 u]: column cs + t + 256 u
+                const float thr = L.v[3];
+                uint32_t mask = 0;
+                if (ce - cs == kChunkCols && cs >= r.h && ce <= r.e) {
 #pragma unroll
-            for (int u = 0; u < kLaneUnroll; ++u) x[u] = ld_stream_f1(p + t + kCandThreads * (j + u * Ci));
-#pragma unroll
-            for (int u = 0; u < kLaneUnroll; ++u)
-                if (x[u] > L.v[3]) stream_push(L, x[u], t + kCandThreads * (j + u * Ci));
-        }
-        for (; j < nb; j += Ci) {
-            const int col = t + kCandThreads * j;
-            if (col < a.vocab) {
-                const float x = ld_stream_f1(p + col);
-                if (x > L.v[3]) stream_push(L, x, col);
+                    for (int u = 0; u < kCandChunkBlocks; ++u) mask |= sv[kCandThreads * u] > thr ? 1u << u : 0u;
+                    insert_marked(L, mask, cs + t, [&](int u, int) { return sv[kCandThreads * u]; });
+                } else {
+                    // a chunk at the row's ends or cut short: columns past ce
+                    // are skipped, those outside the grid body read from global
+                    auto val = [&](int u, int col) {
+                        return (col >= r.h && col < r.e) ? sv[kCandThreads * u] : ld_stream_f1(p + col);
+                    };
+#pragma unroll 4
+                    for (int u = 0; u < kCandChunkBlocks; ++u) {
+                        const int col = cs + t + kCandThreads * u;
+                        if (col < ce && val(u, col) > thr) mask |= 1u << u;
+                    }
+                    insert_marked(L, mask, cs + t, val);
+                }
             }
+            // done with the stage: the warp that finishes it last refills it
+            // with the chunk kCandStages ahead (in this row or a later one)
+            int kn = k + kCandStages;
+            int64_t rn = row;
+            while (kn >= nk) kn -= nk, rn += G;
+            __syncwarp();
+            if (lane == 0 && rn < a.rows && atom_add_acq_rel_smem(&used[s], 1u) % kWarps == kWarps - 1)
+                issue(rn, kn, s, policy);
+            if (++s == kCandStages) s = 0, ph ^= 1u;
         }
         // a list with an empty slot takes, in column order, its columns that
         // hold -inf (the scan kept every larger value already)
         if (p && L.c[3] == kEmptyCol) {
-            int r = 0;
+            int q = 0;
 #pragma unroll
-            for (int k = 0; k < kTopEach; ++k) r += L.c[k] != kEmptyCol;
-            for (int jj = ri; jj < nb && r < kTopEach; jj += Ci) {
+            for (int k = 0; k < kTopEach; ++k) q += L.c[k] != kEmptyCol;
+            for (int jj = jr0; jj < jr1 && q < kTopEach; ++jj) {
                 const int col = t + kCandThreads * jj;
                 if (col >= a.vocab || p[col] != -INFINITY) continue;
 #pragma unroll
                 for (int k = 0; k < kTopEach; ++k)
-                    if (k == r) L.c[k] = col;  // its value is already -inf
-                ++r;
+                    if (k == q) L.c[k] = col;  // its value is already -inf
+                ++q;
             }
         }
         if (C > 1) {
-            cluster_wait();  // CTA 0 is running, and (later rows) done with X
-            if (rank != 0) {
-                const uint32_t x0 = peer_smem(X, 0u);
+            cluster_wait();  // CTA 0 has pulled the previous row's lists
+            if (rank != 0)
 #pragma unroll
-                for (int k = 0; k < kTopEach; ++k)
-                    st_dsmem_f2(x0 + 8u * static_cast<uint32_t>(((rank - 1) * kTopEach + k) * kCandThreads + t),
-                                slot_of(L, k));
-            }
+                for (int k = 0; k < kTopEach; ++k) lt[k * kCandThreads] = slot_of(L, k);
             cluster_arrive_release();
             cluster_wait();
             if (rank == 0)
-                for (uint32_t r = 1; r < C; ++r)
+                for (uint32_t q = 1; q < C; ++q) {
+                    const uint32_t src = peer_smem(lt, q);
+                    float2 e[kTopEach];
 #pragma unroll
-                    for (int k = 0; k < kTopEach; ++k) push_slot(L, X[((r - 1) * kTopEach + k) * kCandThreads + t]);
-            cluster_arrive_release();  // X may be rewritten once every CTA is past here
+                    for (int k = 0; k < kTopEach; ++k)
+                        e[k] = ld_dsmem_f2(src + 8u * static_cast<uint32_t>(k * kCandThreads));
+#pragma unroll
+                    for (int k = 0; k < kTopEach; ++k) push_slot(L, e[k]);
+                }
+            cluster_arrive_release();  // the peers' list slots may be rewritten once CTA 0 is past here
         }
         if (rank == 0) {
             float o[8];
 #pragma unroll
             for (int k = 0; k < kTopEach; ++k) {
-                const bool empty = L.c[k] == kEmptyCol;
-                o[2 * k] = empty ? -INFINITY : L.v[k];
-                o[2 * k + 1] = empty ? -1.0f : static_cast<float>(L.c[k]);
+                const bool empty_slot = L.c[k] == kEmptyCol;
+                o[2 * k] = empty_slot ? -INFINITY : L.v[k];
+                o[2 * k + 1] = empty_slot ? -1.0f : static_cast<float>(L.c[k]);
             }
             float *dst = out + row * static_cast<int64_t>(kCandRow) + 8 * t;
             if (vec_out) {
@@ -800,7 +910,14 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
             }
         }
     }
-    if (C > 1) cluster_wait();  // the last arrive's match: no CTA leaves before its peers
+    if (C > 1) cluster_wait();  // the last arrive's match: no CTA leaves while CTA 0 may still pull
+    if (__syncthreads_or(failed) && t == 0) {
+        atomicAdd(&g_status[1], 1ull);
+        // give copies still in flight a last bounded chance to land: the last
+        // use of each stage
+        for (int64_t gl = total > kCandStages ? total - kCandStages : 0; gl < total; ++gl)
+            (void)mbar_wait_bounded(&full[gl % kCandStages], static_cast<uint32_t>(gl / kCandStages) & 1u, 10000000ull);
+    }
 }
 
 // ---------------------------------------------------------------------------

@@ -197,7 +197,7 @@ def test_candidates_decode_in_full(orc):
                   orc.argmax(b.logits.cpu().numpy(), w.vocab, threads=THREADS), "best candidate")
 
 
-CAND_PLANS = [(0, 0, 0), (0, 1, 0), (0, 2, 0), (0, 3, 256), (2, 4, 0), (0, 5, 256), (0, 8, 0)]
+CAND_PLANS = [(0, 0, 0), (0, 1, 0), (0, 2, 0), (0, 3, 256), (2, 4, 0), (0, 5, 256), (0, 6, 0), (0, 8, 0)]
 
 
 @pytest.mark.parametrize("plan", CAND_PLANS, ids=lambda p: f"path{p[0]}-c{p[1]}-t{p[2]}")
