@@ -343,6 +343,14 @@ CE_API int ce_device_error_reset(ce_stream_t stream);
 CE_API int ce_debug_force(int path, int cluster, int threads);
 
 /*
+ * Grid override, for tests: at most `clusters` clusters (0: no cap) in every
+ * later launch of a row kernel (all but the even-split argmax), so that each
+ * cluster loops over several rows even when the rows are few. Results are
+ * the same; only the schedule changes. Returns CE_EINVAL for clusters < 0.
+ */
+CE_API int ce_debug_grid_cap(int64_t clusters);
+
+/*
  * The plan the library would pick (host only, launches nothing) for
  * op (0 ce_rows, 1 ce_grad, 2 argmax_rows, 3 softmax_rows, 4
  * log_softmax_rows, 5 candidates_rows) on the current device:

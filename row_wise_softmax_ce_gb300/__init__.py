@@ -91,6 +91,7 @@ def _bind(lib):
         "ce_device_error_count": [vp, ctypes.POINTER(ctypes.c_uint64)],
         "ce_device_error_reset": [vp],
         "ce_debug_force": [i32, i32, i32],
+        "ce_debug_grid_cap": [i64],
         "ce_plan": [i32, i64, i64, i64, ctypes.POINTER(ctypes.c_int64)],
     }
     for name, args in sig.items():
@@ -462,6 +463,11 @@ def device_error_reset(device=None) -> None:
 def debug_force(path: int = 0, cluster: int = 0, threads: int = 0) -> None:
     """Force the launch plan of later calls (0 = automatic); see ce_debug_force."""
     _check("ce_debug_force", lib().ce_debug_force(path, cluster, threads))
+
+
+def debug_grid_cap(clusters: int = 0) -> None:
+    """Cap the grid of later row-kernel launches at `clusters` clusters (0 = no cap); see ce_debug_grid_cap."""
+    _check("ce_debug_grid_cap", lib().ce_debug_grid_cap(clusters))
 
 
 def plan(op: int, rows: int, vocab: int, stride: int | None = None) -> dict:

@@ -40,6 +40,7 @@ uint64_t *g_noalloc_ptr[kMaxDevices] = {};
 
 struct Force {
     int path = 0, cluster = 0, threads = 0;
+    int64_t grid_cap = 0;  // at most this many clusters (0: no cap)
 };
 Force g_force;
 std::mutex g_mu;
@@ -276,6 +277,9 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
     }
     if (p.cluster < 1 || p.cluster > kMaxCluster) return CE_EINVAL;
     if (p.path == kPathStream && p.threads > kStreamMaxThreads) return CE_EINVAL;
+    // every row kernel but the even split loops over rows with a stride of
+    // the cluster count, so a smaller grid only gives each cluster more rows
+    if (f.grid_cap > 0 && p.path != kPathFlat) p.clusters = std::min(p.clusters, f.grid_cap);
     *out = p;
     return CE_OK;
 }
@@ -654,6 +658,13 @@ int ce_debug_force(int path, int cluster, int threads) {
     g_force.path = path;
     g_force.cluster = cluster;
     g_force.threads = threads;
+    return CE_OK;
+}
+
+int ce_debug_grid_cap(int64_t clusters) {
+    if (clusters < 0) return CE_EINVAL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_force.grid_cap = clusters;
     return CE_OK;
 }
 

@@ -20,7 +20,7 @@ def test_exports_every_declared_function(lib):
     assert set(names) >= {"ce_rows", "ce_mean", "ce_loss", "ce_grad", "argmax_rows", "argmax_workspace_bytes",
                           "ce_status_string",
                           "ce_version", "ce_last_cuda_error", "ce_device_error_count",
-                          "ce_device_error_reset", "ce_debug_force", "ce_plan", "softmax_rows",
+                          "ce_device_error_reset", "ce_debug_force", "ce_debug_grid_cap", "ce_plan", "softmax_rows",
                           "log_softmax_rows", "candidates_rows", "split_sum", "argmax_rows_noalloc",
                           "argmax_rows_indirect", "candidates_rows_indirect"}
     missing = [n for n in names if not hasattr(lib, n)]
@@ -159,6 +159,9 @@ def test_debug_force_validation(lib):
     assert lib.ce_debug_force(0, 0, 1024) == ce.CE_EINVAL
     assert lib.ce_debug_force(0, 0, 96) == ce.CE_EINVAL
     assert lib.ce_debug_force(0, 0, 0) == ce.CE_OK
+    assert lib.ce_debug_grid_cap(-1) == ce.CE_EINVAL
+    assert lib.ce_debug_grid_cap(3) == ce.CE_OK
+    assert lib.ce_debug_grid_cap(0) == ce.CE_OK
 
 
 def test_no_device_here_reports_edevice(lib):
