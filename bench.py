@@ -371,22 +371,16 @@ def run_ours(args):
     cand_bytes = 4 * wd.rows * wd.vocab + 4 * ce.CANDIDATE_ROW * wd.rows
     del flush, bd, cand
 
-    # ---- end to end: inputs from pinned host memory, results back to the host
+    # ---- end to end through ce_grad_host: logits and labels from pinned host
+    # memory (copied in chunks of rows, each chunk's kernel running as soon as
+    # it has landed), the mean and the tokens back into pinned host memory
     xh = torch.empty((R, V), dtype=torch.float32, pin_memory=True)
     xh.copy_(x)
     yh = y.cpu().pin_memory()
-    mean_h = torch.empty((), dtype=torch.float64, pin_memory=True)
-    top_h = torch.empty(R, dtype=torch.float32, pin_memory=True)
-    xd = torch.empty_like(x)
-    yd = torch.empty_like(y)
+    hs = ce.HostStep(R, V, dev)
 
     def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        yd.copy_(yh, non_blocking=True)
-        ce.ce_grad(xd, yd, scale, grad=grad, loss_rows=loss_rows, top=top)
-        ce.ce_mean(loss_rows, out=mean)
-        mean_h.copy_(mean, non_blocking=True)
-        top_h.copy_(top, non_blocking=True)
+        ce.ce_grad_host(xh, yh, scale, hs)
 
     for _ in range(2):
         e2e_step()
@@ -402,8 +396,8 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K2, ws)
     e2e_value = aggregate_gbs(ws, bytes_step, e2e_ms)
     h2d = xh.numel() * 4 + yh.numel() * 8
-    d2h = 8 + top_h.numel() * 4
-    del xh, xd
+    d2h = 8 + hs.top_h.numel() * 4
+    del xh, hs
 
     # ---- the CPU oracle on a row sample (rank 0, N = 1 only)
     cpu = None

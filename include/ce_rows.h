@@ -119,6 +119,38 @@ CE_API int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t str
             ce_stream_t stream);
 
 /*
+ * crossEntropyGrad and crossEntropyLoss of a batch that is in HOST memory:
+ * the training step fed from the host, with the host-to-device copy
+ * overlapped with the kernels. The labels, then the logits in chunks of
+ * rows, are copied into caller-owned device buffers on a copy stream the
+ * library keeps per device; the fused kernel (as ce_grad) runs on each chunk
+ * on `stream` as soon as that chunk has landed, so chunk c is computed while
+ * chunk c + 1 is copied. Then ce_mean, and the mean and tokens back to the
+ * host. Everything is enqueued: the call returns at once, and the host and
+ * device buffers must stay valid, and the host outputs unread, until
+ * `stream` has reached this point. Host inputs in page-locked memory copy
+ * asynchronously; pageable ones work but the copies may block the caller.
+ *   logits_h:    [rows, stride_h] f32, host, read only.
+ *   labels_h:    [rows] int64, host, read only.
+ *   logits_d:    [rows, vocab] f32 dense, device, written (the staged copy).
+ *   labels_d:    [rows] int64, device, written.
+ *   grad:        [rows, vocab] f32 dense, device, written; grad == logits_d
+ *                (the gradient over the staged copy) is allowed.
+ *   loss_rows:   [rows] f32, device, written.   top: [rows] f32 device or NULL.
+ *   loss_mean:   1 double, device, written.
+ *   loss_mean_h: 1 double, host, or NULL.    top_h: [rows] f32 host or NULL
+ *                (needs top).
+ *   chunk_rows:  rows per copied chunk; 0 picks 16 chunks (at most 64).
+ * Calls that share device buffers must be ordered by their streams. The
+ * same argument checks as ce_grad apply (CE_EINVAL / CE_EALIGN before any
+ * copy); rows == 0 writes a NaN mean.
+ */
+CE_API int ce_grad_host(const float *logits_h, int64_t rows, int64_t vocab, int64_t stride_h,
+                        const int64_t *labels_h, double scale, float *logits_d, int64_t *labels_d,
+                        float *grad, float *loss_rows, float *top, double *loss_mean,
+                        double *loss_mean_h, float *top_h, int64_t chunk_rows, ce_stream_t stream);
+
+/*
  * argmaxInto (gizml:netops, Functions) with Tensor.argmax's rule (Methods):
  * over `rows` rows of `stride` elements, the index of the largest of the
  * first `vocab` entries -- the first of equals; NaN never wins; a row with

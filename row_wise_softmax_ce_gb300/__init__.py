@@ -92,6 +92,7 @@ def _bind(lib):
         "ce_device_error_reset": [vp],
         "ce_debug_force": [i32, i32, i32],
         "ce_debug_grid_cap": [i64],
+        "ce_grad_host": [vp, i64, i64, i64, vp, ctypes.c_double, vp, vp, vp, vp, vp, vp, vp, vp, i64, vp],
         "ce_plan": [i32, i64, i64, i64, ctypes.POINTER(ctypes.c_int64)],
     }
     for name, args in sig.items():
@@ -232,6 +233,54 @@ def ce_grad(logits: torch.Tensor, labels: torch.Tensor, scale: float, vocab: int
     if loss_rows is False and top is False:
         return grad
     return grad, lr, tp
+
+
+class HostStep:
+    """Device buffers of ``ce_grad_host`` for batches of one shape, kept and
+    reused across steps, and the page-locked host outputs it copies back."""
+
+    def __init__(self, rows: int, vocab: int, device, in_place: bool = False):
+        dev = torch.device(device)
+        self.rows, self.vocab, self.device = rows, vocab, dev
+        self.logits = torch.empty((rows, vocab), dtype=torch.float32, device=dev)
+        self.labels = torch.empty(rows, dtype=torch.int64, device=dev)
+        self.grad = self.logits if in_place else torch.empty((rows, vocab), dtype=torch.float32, device=dev)
+        self.loss_rows = torch.empty(rows, dtype=torch.float32, device=dev)
+        self.top = torch.empty(rows, dtype=torch.float32, device=dev)
+        self.mean = torch.empty((), dtype=torch.float64, device=dev)
+        self.mean_h = torch.empty((), dtype=torch.float64, pin_memory=True)
+        self.top_h = torch.empty(rows, dtype=torch.float32, pin_memory=True)
+
+
+def ce_grad_host(logits_h: torch.Tensor, labels_h: torch.Tensor, scale: float, step: HostStep,
+                 vocab: int | None = None, chunk_rows: int = 0) -> HostStep:
+    """crossEntropyGrad + crossEntropyLoss of a batch in host memory: the
+    logits and labels are copied into ``step``'s device buffers chunk by
+    chunk, each chunk's gradient, row losses and tokens computed as soon as
+    it has landed, then the mean; the mean and tokens come back into
+    ``step.mean_h`` / ``step.top_h``. Enqueued on the current stream: read the
+    host outputs after synchronising it."""
+    if not isinstance(logits_h, torch.Tensor) or logits_h.dtype != torch.float32 or logits_h.is_cuda:
+        raise TypeError("logits_h must be a float32 CPU tensor")
+    if logits_h.dim() != 2 or (logits_h.shape[1] > 1 and logits_h.stride(1) != 1):
+        raise ValueError("logits_h must be 2-D with contiguous rows")
+    rows, cols = logits_h.shape
+    vocab = cols if vocab is None else int(vocab)
+    if not 1 <= vocab <= cols:
+        raise ValueError(f"need 1 <= vocab <= logits_h.shape[1] (vocab={vocab}, cols={cols})")
+    stride = max(logits_h.stride(0) if rows > 1 else cols, vocab)
+    if labels_h.dtype != torch.int64 or labels_h.is_cuda or tuple(labels_h.shape) != (rows,) or \
+            not labels_h.is_contiguous():
+        raise ValueError(f"labels_h must be a contiguous int64 CPU tensor [rows={rows}]")
+    if (step.rows, step.vocab) != (rows, vocab):
+        raise ValueError(f"step buffers are for {step.rows} x {step.vocab}, not {rows} x {vocab}")
+    dev = step.device
+    with torch.cuda.device(dev):
+        _check("ce_grad_host", lib().ce_grad_host(
+            logits_h.data_ptr(), rows, vocab, stride, labels_h.data_ptr(), float(scale), step.logits.data_ptr(),
+            step.labels.data_ptr(), step.grad.data_ptr(), step.loss_rows.data_ptr(), step.top.data_ptr(),
+            step.mean.data_ptr(), step.mean_h.data_ptr(), step.top_h.data_ptr(), int(chunk_rows), _stream(dev)))
+    return step
 
 
 def argmax_rows(logits: torch.Tensor, vocab: int | None = None,

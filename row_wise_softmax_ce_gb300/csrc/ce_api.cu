@@ -284,6 +284,36 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
     return CE_OK;
 }
 
+// ce_grad_host's copy stream and events, one set per device, created on
+// first use and kept for the life of the process (like the error counter).
+constexpr int kHostChunksMax = 64;
+struct HostPipe {
+    std::mutex mu;  // held while a call enqueues, so calls do not interleave their events
+    bool ready = false;
+    cudaStream_t copy = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t chunk[kHostChunksMax] = {};
+};
+HostPipe g_pipe[kMaxDevices];
+
+// caller holds h.mu
+cudaError_t host_pipe_ready(HostPipe &h) {
+    if (h.ready) return cudaSuccess;
+    cudaError_t e = cudaStreamCreateWithFlags(&h.copy, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
+    for (int i = 0; i < kHostChunksMax && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(&h.chunk[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        for (int i = 0; i < kHostChunksMax; ++i)
+            if (h.chunk[i]) (void)cudaEventDestroy(h.chunk[i]), h.chunk[i] = nullptr;
+        if (h.start) (void)cudaEventDestroy(h.start), h.start = nullptr;
+        if (h.copy) (void)cudaStreamDestroy(h.copy), h.copy = nullptr;
+        return e;
+    }
+    h.ready = true;
+    return cudaSuccess;
+}
+
 int check_logits(const float *logits, int64_t rows, int64_t vocab, int64_t stride) {
     if (rows < 0 || vocab < 1 || vocab > kMaxVocab || stride < vocab) return CE_EINVAL;
     if (rows > 0 && logits == nullptr) return CE_EINVAL;
@@ -626,6 +656,67 @@ const char *ce_status_string(int status) {
     case CE_ERANGE: return "too many rows for argmax_rows_noalloc's fixed scratch (rows + 2 * SMs must be <= 8192)";
     default: return "unknown status";
     }
+}
+
+int ce_grad_host(const float *logits_h, int64_t rows, int64_t vocab, int64_t stride_h, const int64_t *labels_h,
+                 double scale, float *logits_d, int64_t *labels_d, float *grad, float *loss_rows, float *top,
+                 double *loss_mean, double *loss_mean_h, float *top_h, int64_t chunk_rows, ce_stream_t stream) {
+    int st = check_logits(logits_h, rows, vocab, stride_h);
+    if (st) return st;
+    if (!std::isfinite(scale) || chunk_rows < 0 || loss_mean == nullptr) return CE_EINVAL;
+    if (rows > 0 && (labels_h == nullptr || logits_d == nullptr || labels_d == nullptr || grad == nullptr ||
+                     loss_rows == nullptr))
+        return CE_EINVAL;
+    if (top_h != nullptr && top == nullptr) return CE_EINVAL;
+    if (misaligned(labels_h, 8) || misaligned(logits_d, 4) || misaligned(labels_d, 8) || misaligned(grad, 4) ||
+        misaligned(loss_rows, 4) || misaligned(top, 4) || misaligned(loss_mean, 8) || misaligned(loss_mean_h, 8) ||
+        misaligned(top_h, 4))
+        return CE_EALIGN;
+    const int64_t dense = rows * vocab * 4;
+    if (grad != logits_d && ranges_overlap(grad, dense, logits_d, dense)) return CE_EINVAL;
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    HostPipe &h = g_pipe[dev.device];
+    std::lock_guard<std::mutex> lock(h.mu);
+    cudaError_t e = host_pipe_ready(h);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (rows > 0) {
+        int64_t n = chunk_rows > 0 ? ceil_div(rows, chunk_rows) : std::min<int64_t>(rows, 16);
+        n = std::min<int64_t>(n, kHostChunksMax);
+        const int64_t chunk = ceil_div(rows, n);
+        n = ceil_div(rows, chunk);
+        // the copies start once earlier work on the stream (which may still
+        // read logits_d or labels_d) is done
+        if ((e = cudaEventRecord(h.start, stream)) != cudaSuccess) return cuda_status(e);
+        if ((e = cudaStreamWaitEvent(h.copy, h.start, 0)) != cudaSuccess) return cuda_status(e);
+        if ((e = cudaMemcpyAsync(labels_d, labels_h, static_cast<size_t>(rows) * 8, cudaMemcpyHostToDevice,
+                                 h.copy)) != cudaSuccess)
+            return cuda_status(e);
+        for (int64_t c = 0; c < n; ++c) {
+            const int64_t r0 = c * chunk, r1 = std::min(rows, r0 + chunk);
+            e = cudaMemcpy2DAsync(logits_d + r0 * vocab, static_cast<size_t>(vocab) * 4, logits_h + r0 * stride_h,
+                                  static_cast<size_t>(stride_h) * 4, static_cast<size_t>(vocab) * 4,
+                                  static_cast<size_t>(r1 - r0), cudaMemcpyHostToDevice, h.copy);
+            if (e == cudaSuccess) e = cudaEventRecord(h.chunk[c], h.copy);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        // chunk c's kernel runs while chunk c + 1 is copied
+        for (int64_t c = 0; c < n; ++c) {
+            const int64_t r0 = c * chunk, r1 = std::min(rows, r0 + chunk);
+            if ((e = cudaStreamWaitEvent(stream, h.chunk[c], 0)) != cudaSuccess) return cuda_status(e);
+            st = ce_grad(logits_d + r0 * vocab, r1 - r0, vocab, vocab, labels_d + r0, scale, grad + r0 * vocab,
+                         loss_rows + r0, top ? top + r0 : nullptr, stream);
+            if (st) return st;
+        }
+    }
+    if ((st = ce_mean(loss_rows, rows, loss_mean, stream))) return st;
+    if (loss_mean_h && (e = cudaMemcpyAsync(loss_mean_h, loss_mean, 8, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+        return cuda_status(e);
+    if (top_h && rows > 0 &&
+        (e = cudaMemcpyAsync(top_h, top, static_cast<size_t>(rows) * 4, cudaMemcpyDeviceToHost, stream)) !=
+            cudaSuccess)
+        return cuda_status(e);
+    return CE_OK;
 }
 
 int ce_version(void) { return kVersion; }

@@ -180,3 +180,25 @@ def test_binding_rejects_cpu_tensors():
         ce.argmax_rows(x)
     with pytest.raises(TypeError):
         ce.argmax_rows(x.double())
+
+
+def test_grad_host_validation(lib):
+    """ce_grad_host: every argument check answers before any device call."""
+    def call(logits_h=V(256), rows=4, vocab=10, stride=10, labels_h=V(512), scale=1.0, logits_d=V(1 << 16),
+             labels_d=V(1 << 17), grad=V(1 << 18), loss_rows=V(1 << 19), top=V(1 << 20), mean=V(1 << 21),
+             mean_h=V(1 << 22), top_h=V(1 << 23), chunk=0):
+        return lib.ce_grad_host(logits_h, rows, vocab, stride, labels_h, scale, logits_d, labels_d, grad,
+                                loss_rows, top, mean, mean_h, top_h, chunk, None)
+    assert call(logits_h=None) == ce.CE_EINVAL
+    assert call(stride=9) == ce.CE_EINVAL
+    assert call(vocab=(1 << 24) + 1, stride=(1 << 24) + 1) == ce.CE_EINVAL
+    assert call(scale=float("nan")) == ce.CE_EINVAL
+    assert call(chunk=-1) == ce.CE_EINVAL
+    assert call(mean=None) == ce.CE_EINVAL
+    for k in ("labels_h", "logits_d", "labels_d", "grad", "loss_rows"):
+        assert call(**{k: None}) == ce.CE_EINVAL, k
+    assert call(top=None) == ce.CE_EINVAL                        # tokens back need the device tokens
+    assert call(labels_h=V(516)) == ce.CE_EALIGN                 # int64 on 8 bytes
+    assert call(mean_h=V((1 << 22) + 4)) == ce.CE_EALIGN         # double on 8 bytes
+    assert call(top_h=V((1 << 23) + 2)) == ce.CE_EALIGN
+    assert call(grad=V((1 << 16) + 40)) == ce.CE_EINVAL          # grad overlaps the staged logits
