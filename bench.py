@@ -12,9 +12,12 @@ Printed (one JSON line, rank 0):
   argmax      rows/s of argmax_rows on the decode workload (256 x 151936,
               row stride 152064), L2 flushed before every timed launch
   candidates  rows/s of candidates_rows on the same decode batch, likewise
-  e2e         the same metric with the inputs copied from pinned host memory
-              and the mean loss and tokens copied back inside the timed region
-  cpu_baseline the CPU oracle (f64) timed on the host cores on a row sample
+  e2e         the same metric through ce_grad_host: the inputs copied from
+              pinned host memory (in chunks, overlapped with the kernels) and
+              the mean loss and tokens copied back inside the timed region
+  d2d_copy    a plain device copy of the same bytes, for comparison
+  cpu_baseline the CPU oracle (f64) timed on the host cores on a row sample,
+              and on one core
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --case grad|rows|argmax|softmax|log_softmax|candidates|split_sum|sharded
