@@ -227,6 +227,37 @@ def time_oracle(batch, sample_rows: int, threads: int, chunk: int = 1024):
     return total + time.perf_counter() - t0
 
 
+def time_oracle_argmax(batch, sample_rows: int, threads: int, chunk: int = 1024):
+    """Wall time of the oracle's argmax over the first sample_rows rows."""
+    import oracle
+    orc = oracle.load()
+    total = 0.0
+    for a in range(0, sample_rows, chunk):
+        xs = batch.logits[a:min(sample_rows, a + chunk)].cpu().numpy()
+        t0 = time.perf_counter()
+        orc.argmax(xs, batch.workload.vocab, threads=threads)
+        total += time.perf_counter() - t0
+    return total
+
+
+def report_oracle(w, cores: int):
+    """The oracle on one core and on all cores for one workload: the whole
+    workload where it is small, else a 256-row sample scaled to the
+    workload's rows ("sampled"). One JSON line per thread count."""
+    sampled = w.rows * w.vocab > 2e8
+    n = 256 if sampled else w.rows
+    b = W.generate(w.with_rows(n), device="cuda")
+    grad_ops = "grad" in w.ops
+    nbytes = step_bytes(w.rows, w.vocab) if grad_ops else argmax_bytes(w.rows, w.vocab)
+    for threads in (1, cores):
+        dt = time_oracle(b, n, threads) if grad_ops else time_oracle_argmax(b, n, threads)
+        full = dt * w.rows / n
+        print(json.dumps({"oracle": w.name, "step": "loss rows + gradient + argmax + mean" if grad_ops else "argmax",
+                          "threads": threads, "rows_timed": n, "seconds": round(dt, 4),
+                          "seconds_full": round(full, 4), "sampled": sampled,
+                          "GB/s": round(nbytes / full / 1e9, 3)}), flush=True)
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -586,6 +617,9 @@ def main():
                 a.case, a.workload, a.rows, a.force, a.flush = case, name, 0, "", small
                 a.steps = min(args.steps, 50)
                 run_case(a)
+        # the oracle beside, single-threaded and on every host core
+        for w in W.WORKLOADS.values():
+            report_oracle(w, cpu_cores())
         return 0
     if args.case:
         return run_case(args)

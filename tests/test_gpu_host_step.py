@@ -104,3 +104,28 @@ def test_host_step_shape_mismatch_refused():
     step = ce.HostStep(4, 10, DEV)
     with pytest.raises(ValueError):
         ce.ce_grad_host(torch.zeros(5, 10), torch.zeros(5, dtype=torch.int64), 1.0, step)
+
+
+def test_host_step_replayed_from_a_cuda_graph(orc):
+    """The host-fed step captured once (the copy stream forks from the
+    captured stream and joins it again inside the graph); each replay copies
+    what the pinned inputs hold at that moment."""
+    rows, vocab = 64, 5003
+    xh = torch.zeros((rows, vocab)).pin_memory()
+    yh = torch.zeros(rows, dtype=torch.int64).pin_memory()
+    step = ce.HostStep(rows, vocab, DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        ce.ce_grad_host(xh, yh, 1.0 / rows, step, chunk_rows=16)  # warm-up: streams and events made outside
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        ce.ce_grad_host(xh, yh, 1.0 / rows, step, chunk_rows=16)
+    for seed in (1, 2):
+        x, y = W.random_logits(rows, vocab, sigma=3.0, seed=seed)
+        xh.copy_(x)
+        yh.copy_(y)
+        graph.replay()
+        torch.cuda.synchronize()
+        check(orc, step, x, y, vocab, 1.0 / rows, f"graph replay {seed}")
