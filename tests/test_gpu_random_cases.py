@@ -32,6 +32,7 @@ def _built():
     ce.debug_force(0, 0, 0)
     yield
     ce.debug_force(0, 0, 0)
+    ce.debug_grid_cap(0)
     ce.device_error_reset()
 
 
@@ -68,6 +69,9 @@ def draw_case(seed):
                  rows=ROW_PLANS[rng.integers(len(ROW_PLANS))],
                  cand=CAND_PLANS[rng.integers(len(CAND_PLANS))])
     scale = float(rng.choice([1.0, 1.0 / rows, 0.5]))
+    # drawn last, so the earlier draws of a seed stay as they were
+    plans["grid_cap"] = int(rng.choice([0, 0, 0, 1, 2, 5]))     # clusters looping over several rows
+    plans["host_chunk"] = int(rng.choice([0, 1, 5, rows]))      # ce_grad_host's rows per copied chunk
     return x, labels, vocab, offset, scale, plans
 
 
@@ -100,14 +104,22 @@ def test_random_case(orc, seed):
             # a forced staged plan may not fit this shape; the automatic plan always does
             return fn(*args, **kw)
 
-    grad, lr, top = fused(ce.ce_grad, dx, dy, scale, vocab=vocab, loss_rows=True, top=True)
-    soft = fused(ce.softmax_rows, dx, vocab=vocab)
-    logp = fused(ce.log_softmax_rows, dx, vocab=vocab)
-    lr2 = forced_call(plans["rows"], ce.ce_rows, dx, dy, vocab=vocab)
-    top2 = forced_call(plans["rows"], ce.argmax_rows, dx, vocab=vocab)
-    mean = ce.ce_mean(lr2)
-    cand = forced_call(plans["cand"], ce.candidates_rows, dx, vocab=vocab)
-    torch.cuda.synchronize()
+    xh = torch.from_numpy(x).pin_memory()
+    yh = torch.from_numpy(labels).pin_memory()
+    ce.debug_grid_cap(plans["grid_cap"])
+    try:
+        grad, lr, top = fused(ce.ce_grad, dx, dy, scale, vocab=vocab, loss_rows=True, top=True)
+        soft = fused(ce.softmax_rows, dx, vocab=vocab)
+        logp = fused(ce.log_softmax_rows, dx, vocab=vocab)
+        lr2 = forced_call(plans["rows"], ce.ce_rows, dx, dy, vocab=vocab)
+        top2 = forced_call(plans["rows"], ce.argmax_rows, dx, vocab=vocab)
+        mean = ce.ce_mean(lr2)
+        cand = forced_call(plans["cand"], ce.candidates_rows, dx, vocab=vocab)
+        hs = ce.ce_grad_host(xh[:, :vocab], yh, scale, ce.HostStep(x.shape[0], vocab, DEV),
+                             chunk_rows=plans["host_chunk"])
+        torch.cuda.synchronize()
+    finally:
+        ce.debug_grid_cap(0)
 
     g_ref, l_ref = orc.ce_grad(x, vocab, labels, scale, threads=THREADS)
     a_ref = orc.argmax(x, vocab, threads=THREADS)
@@ -120,3 +132,6 @@ def test_random_case(orc, seed):
     assert_softmax(soft, orc.softmax(x, vocab, threads=THREADS), f"{what}: softmax_rows")
     assert_log_softmax(logp, orc.log_softmax(x, vocab, threads=THREADS), f"{what}: log_softmax_rows")
     assert_candidates(cand, orc.candidates(x, vocab, threads=THREADS), f"{what}: candidates_rows")
+    assert_grad(hs.grad, g_ref, f"{what}: ce_grad_host grad")
+    assert_tokens(hs.top_h, a_ref, f"{what}: ce_grad_host tokens")
+    assert_mean(hs.mean_h.item(), orc.ce_mean(l_ref), f"{what}: ce_grad_host mean", loss_rows=l_ref)
