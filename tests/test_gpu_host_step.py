@@ -2,6 +2,8 @@
 logits copied in chunks of rows with each chunk's fused kernel running as
 soon as it has landed. Checked against the f64 CPU oracle, and against
 ce_grad + ce_mean on the same batch already on the device."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -129,3 +131,34 @@ def test_host_step_replayed_from_a_cuda_graph(orc):
         graph.replay()
         torch.cuda.synchronize()
         check(orc, step, x, y, vocab, 1.0 / rows, f"graph replay {seed}")
+
+
+@pytest.mark.parametrize("name", ["ce_8192x128256", "ce_16384x50257_x30"])
+def test_host_step_full_size_sampled_rows(orc, name):
+    """The bench's end-to-end step at full size (16 chunks, from pinned host
+    memory): sampled rows against the oracle, every row against ce_grad on
+    the same batch resident on the device."""
+    w = W.WORKLOADS[name]
+    b = W.generate(w, device=DEV)
+    V = w.vocab
+    xh = b.logits.cpu().pin_memory()
+    yh = b.labels.cpu().pin_memory()
+    step = ce.ce_grad_host(xh[:, :V], yh, b.scale, ce.HostStep(w.rows, V, DEV))
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(1)
+    rows = torch.unique(torch.cat([torch.randint(0, w.rows, (24,), generator=g), b.special_rows()[:24],
+                                   torch.tensor([0, w.rows - 1])])).long()
+    xs = xh[rows, :V].numpy()
+    g_ref, l_ref = orc.ce_grad(xs, V, yh[rows].numpy(), b.scale, threads=os.cpu_count() or 1)
+    idx = rows.to(DEV)
+    assert_grad(step.grad[idx], g_ref, f"{name}: host step grad (sampled)")
+    assert_loss(step.loss_rows[idx], l_ref, f"{name}: host step loss (sampled)")
+    assert_tokens(step.top_h[rows], orc.argmax(xs, V), f"{name}: host step tokens (sampled)")
+    # every row: the tokens are exact whatever the chunking; the losses within tolerance
+    _, lr, top = ce.ce_grad(b.logits[:, :V], b.labels, b.scale, loss_rows=True, top=True)
+    torch.cuda.synchronize()
+    assert torch.equal(step.top, top)
+    assert torch.equal(step.top_h, top.cpu())
+    rel = ((step.loss_rows.double() - lr.double()).abs() / lr.double().clamp_min(1e-3)).max().item()
+    assert rel <= 2 * 2e-5, f"{name}: host step vs device step losses: {rel}"
+    assert_mean(step.mean_h.item(), lr.double().sum().item() / w.rows, f"{name}: host step mean")
