@@ -365,10 +365,12 @@ CE_API int ce_device_error_reset(ce_stream_t stream);
  * global, 3 refused (formerly a ring-of-copies kernel), 4
  * shared-memory-staged with one row per cluster, 5 argmax split evenly over
  * the GPU -- needs a workspace, 6 one warp per row -- ce_rows, ce_loss,
- * argmax_rows and ce_stats only), the CTAs that share one row (cluster: 0
- * automatic, else 1..16; candidates_rows takes at most 8) and the threads of
- * a CTA (threads: 0 automatic, else 128 or 256; 512 is rejected by every
- * kernel family; candidates_rows takes 256 only).
+ * argmax_rows and ce_stats only, 7 argmax through a ring of bulk-copied row
+ * chunks -- argmax_rows and argmax_rows_indirect only), the CTAs that share
+ * one row (cluster: 0 automatic, else 1..16; candidates_rows and path 7 take
+ * at most 8) and the threads of a CTA (threads: 0 automatic, else 128 or
+ * 256; 512 is rejected by every kernel family; candidates_rows and path 7
+ * take 256 only).
  * Applies to every later call in the process. A forced plan that cannot
  * launch on this device makes the calls return CE_EINVAL.
  */

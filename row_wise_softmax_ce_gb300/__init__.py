@@ -47,7 +47,7 @@ LIB_PATH = os.path.join(_PKG, "libcerows.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "ce_rows.h")
 
 CE_OK, CE_EINVAL, CE_EALIGN, CE_ECUDA, CE_EDEVICE, CE_ERANGE = 0, -1, -2, -3, -4, -5
-PATH_AUTO, PATH_STAGED, PATH_STREAM, PATH_STAGED_PER_ROW, PATH_FLAT, PATH_WARP = 0, 1, 2, 4, 5, 6
+PATH_AUTO, PATH_STAGED, PATH_STREAM, PATH_STAGED_PER_ROW, PATH_FLAT, PATH_WARP, PATH_RING = 0, 1, 2, 4, 5, 6, 7
 OP_ROWS, OP_GRAD, OP_ARGMAX, OP_SOFTMAX, OP_LOG_SOFTMAX, OP_CANDIDATES = 0, 1, 2, 3, 4, 5
 # candidatesInto's workgroup, TOP_EACH and CANDIDATE_ROW (gizml:netops, Constants)
 CANDIDATE_THREADS, TOP_EACH, CANDIDATE_ROW = 256, 4, 2048

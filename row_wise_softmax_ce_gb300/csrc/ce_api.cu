@@ -222,6 +222,21 @@ void plan_candidates(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev
     p.clusters = std::min<int64_t>(rows, kMaxClusters);
 }
 
+// Where the ring argmax beats the streaming one (both measured on GB300,
+// where one warp per row does not apply): from four rows per SM up -- 1024 x
+// 151936 (L2 flushed) 93.7 vs 105.0 us, 16384 x 50257 447 vs 462 us, 8192 x
+// 128256 568 vs 571 us; 256 x 151936 31.4 vs 30.7 us and 64 rows 14.8 vs 14.6
+// us stay with the streaming kernel.
+bool ring_argmax_applies(int64_t rows, const DeviceInfo &dev) { return rows >= 4 * static_cast<int64_t>(dev.sms); }
+
+// Launch shape of the ring argmax: the candidates kernel's chunk ring, one
+// (value, column) state per thread; the row split like the candidates'.
+void plan_argmax_ring(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int cluster) {
+    plan_candidates(p, rows, vocab, dev, cluster);
+    p.path = kPathRing;
+    p.smem = kCandRingBytes + (p.cluster > 1 ? kRingArgmaxSlotBytes : 0);
+}
+
 // Where one warp per row beats a CTA (or cluster) per row, measured on GB300
 // with L2 flushed: ce_rows 4096 x 32000 81% vs 66% of copy bandwidth, 16384 x
 // 50257 97% vs 83%, slices of 16032 columns x 8192 rows 2.24 vs 2.49 ms for
@@ -249,7 +264,7 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
                 return CE_EINVAL;
         } else if (f.path == kPathStream) {
             plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster);
-        } else if (f.path == kPathFlat || f.path == kPathWarp) {
+        } else if (f.path == kPathFlat || f.path == kPathWarp || f.path == kPathRing) {
             return CE_EINVAL;
         } else if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, false, true)) {
             plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
@@ -259,6 +274,10 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
         if (f.threads && f.threads != kCandThreads) return CE_EINVAL;
         if (f.cluster > kCandMaxCluster) return CE_EINVAL;
         plan_candidates(p, rows, vocab, dev, f.cluster);
+    } else if (f.path == kPathRing) {
+        if (op != kOpArgmax || (f.threads && f.threads != kCandThreads) || f.cluster > kCandMaxCluster)
+            return CE_EINVAL;
+        plan_argmax_ring(p, rows, vocab, dev, f.cluster);
     } else if (op == kOpArgmax && (f.path == kPathFlat || (f.path == kPathAuto && f.cluster == 0 && f.threads == 0)) &&
                flat_applies(rows, vocab, dev, f.path == kPathFlat)) {
         p.path = kPathFlat;
@@ -272,6 +291,9 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
     } else if (f.path == kPathAuto && f.cluster == 0 && f.threads == 0 && warp_applies(op, rows, vocab, dev) &&
                plan_warp(p, op, rows)) {
         // many rows of moderate width: one warp per row
+    } else if (op == kOpArgmax && f.path == kPathAuto && f.cluster == 0 && f.threads == 0 &&
+               ring_argmax_applies(rows, dev)) {
+        plan_argmax_ring(p, rows, vocab, dev, 0);
     } else {
         plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster);
     }
@@ -743,7 +765,7 @@ int ce_device_error_reset(ce_stream_t stream) {
 }
 
 int ce_debug_force(int path, int cluster, int threads) {
-    if (path < 0 || path > kPathWarp || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
+    if (path < 0 || path > kPathRing || cluster < 0 || cluster > kMaxCluster) return CE_EINVAL;
     if (threads != 0 && threads != 128 && threads != 256 && threads != 512) return CE_EINVAL;
     std::lock_guard<std::mutex> lock(g_mu);
     g_force.path = path;

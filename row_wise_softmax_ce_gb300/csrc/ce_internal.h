@@ -15,6 +15,7 @@ enum Path : int {
     kPathStagedPerRow = 4,
     kPathFlat = 5,
     kPathWarp = 6,  // one warp per row (ce_rows, argmax, slice statistics of many short rows)
+    kPathRing = 7,  // argmax through a ring of bulk-copied row chunks (few long rows)
 };
 enum Op : int { kOpRows = 0, kOpGrad = 1, kOpArgmax = 2, kOpSoftmax = 3, kOpLogSoftmax = 4, kOpCandidates = 5 };
 // What the fused two-pass kernels write from a row's (max, exp-sum) state.
@@ -38,6 +39,7 @@ constexpr int kCandHeaderBytes = 48;
 constexpr int kCandListBytes = kCandThreads * kTopEach * 8;
 constexpr int kCandRingBytes = kCandHeaderBytes + kCandStages * kCandStageFloats * 4;
 constexpr int kCandMaxSmemBytes = kCandRingBytes + kCandListBytes;
+constexpr int kRingArgmaxSlotBytes = kCandThreads * 8;  // one (value, column) per thread (split rows)
 constexpr int kCandCtasPerSm = 4;  // resident CTAs per SM the shared memory allows
 static_assert(kCandStages * 12 <= kCandHeaderBytes && kCandHeaderBytes % 16 == 0 && kCandStageFloats % 4 == 0 &&
                   kCandCtasPerSm * (kCandMaxSmemBytes + 1024) <= 228 * 1024,

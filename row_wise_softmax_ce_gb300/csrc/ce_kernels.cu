@@ -733,61 +733,62 @@ __device__ __forceinline__ void insert_marked(TopList &L, uint32_t mask, int col
 
 }  // namespace cand
 
-// k_candidates: thread t of a 256-thread CTA is the pages' logical thread t
-// itself and keeps one sorted list in registers. CTA `rank` of a cluster of C
-// reads the blocks of 256 columns [jr0, jr1) of each of the cluster's rows
-// (an even split of the row's blocks), chunk by chunk: kCandChunkBlocks blocks
-// arrive by one bulk copy into a ring of kCandStages shared-memory stages
-// (mbarrier full[s]), up to kCandStages chunks ahead, across rows: each warp
-// counts itself done with a stage (an acq_rel atomic on used[s]), and the last
-// warp to finish a chunk issues the copy of chunk + kCandStages into it.
-// A chunk sits on the 16-byte grid of the logits (float i of a stage holds
-// column cs - off + i); the at most 3 columns of a row before its first
-// 16-byte boundary and after its last are read from global memory by their
-// threads. Per chunk a thread marks its values above the list's 4th value (as
-// of the chunk's start, never above the current one, so no value that belongs
-// in the list is left out) and then inserts the marked ones: a warp runs the
-// insertion once per value that some lane keeps, not once per value read.
-// For C > 1, CTAs 1..C-1 leave their lists in shared memory and CTA 0 pulls
-// and merges them through distributed shared memory and writes the row.
-__global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *__restrict__ out) {
-    using namespace cand;
-    extern __shared__ __align__(128) unsigned char smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint32_t *used = reinterpret_cast<uint32_t *>(full + kCandStages);  // warps done with the stage, ever
-    float *stages = reinterpret_cast<float *>(smem + kCandHeaderBytes);
-    float2 *lt = reinterpret_cast<float2 *>(smem + kCandRingBytes) + threadIdx.x;  // this thread's list slots
-    const int t = threadIdx.x, lane = t & 31;
-    const uint32_t rank = cluster_rank(), C = cluster_size();
-    const int64_t cid = cluster_id_x(), G = cluster_count_x();
-    const bool vec_out = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
-    const int nb = (a.vocab + kCandThreads - 1) / kCandThreads;  // blocks of 256 columns
-    const int jr0 = static_cast<int>(static_cast<int64_t>(nb) * rank / C);
-    const int jr1 = static_cast<int>(static_cast<int64_t>(nb) * (rank + 1) / C);
-    const int nk = (jr1 - jr0 + kCandChunkBlocks - 1) / kCandChunkBlocks;  // chunks of a row here
-    const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;      // rows of this cluster
-    const int64_t total = K * nk;                                           // chunks this CTA reads
-    constexpr int kChunkCols = kCandChunkBlocks * kCandThreads;
+// ChunkRing: a CTA's even share [jr0, jr1) of the blocks of 256 columns of
+// each of its cluster's rows (cluster cid of G takes rows cid, cid + G, ...),
+// streamed chunk by chunk: kCandChunkBlocks blocks arrive by one bulk copy
+// into a ring of kCandStages shared-memory stages (mbarrier full[s]), up to
+// kCandStages chunks ahead, across rows. Each warp counts itself done with a
+// stage (an acq_rel atomic on used[s]); the warp that finishes a chunk last
+// issues the copy of the chunk kCandStages ahead into its stage. A chunk sits
+// on the 16-byte grid of the logits (float i of a stage holds column
+// cs - off + i), so any row phase is one aligned copy; the at most 3 columns
+// of a row before its first 16-byte boundary and after its last are not
+// copied (their threads read them from global memory).
+struct RowGeom {
+    int off, h, e;  // 16-byte phase (floats); columns [0, h) and [e, vocab) outside the copied grid
+};
 
-    // A row's 16-byte phase `off` (floats), its columns [0, h) before the
-    // first boundary and [e, vocab) after the last.
-    struct Geom {
-        int off, h, e;
-    };
-    auto geom = [&](const float *p) {
+struct ChunkRing {
+    const Args *a;
+    uint64_t *full;
+    uint32_t *used;
+    float *stages;
+    int jr0, jr1, nk;  // blocks [jr0, jr1) of every row, in nk chunks
+    int64_t cid, G;
+    uint64_t policy;
+
+    __device__ __forceinline__ ChunkRing(const Args &args, unsigned char *smem) : a(&args) {
+        full = reinterpret_cast<uint64_t *>(smem);
+        used = reinterpret_cast<uint32_t *>(full + kCandStages);
+        stages = reinterpret_cast<float *>(smem + kCandHeaderBytes);
+        const uint32_t rank = cluster_rank(), C = cluster_size();
+        const int nb = (args.vocab + kCandThreads - 1) / kCandThreads;
+        jr0 = static_cast<int>(static_cast<int64_t>(nb) * rank / C);
+        jr1 = static_cast<int>(static_cast<int64_t>(nb) * (rank + 1) / C);
+        nk = (jr1 - jr0 + kCandChunkBlocks - 1) / kCandChunkBlocks;
+        cid = cluster_id_x();
+        G = cluster_count_x();
+        policy = l2_policy_evict_first();
+    }
+    __device__ __forceinline__ RowGeom geom(const float *p) const {
         const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
-        const int h = min(a.vocab, (4 - off) & 3);
-        return Geom{off, h, h + ((a.vocab - h) & ~3)};
-    };
-    // chunk k of `row` into stage s: the grid-aligned body of its columns [cs, ce)
-    auto issue = [&](int64_t row, int k, int s, uint64_t policy) {
-        const float *p = row_start(a, row);
+        const int h = min(a->vocab, (4 - off) & 3);
+        return RowGeom{off, h, h + ((a->vocab - h) & ~3)};
+    }
+    // the columns [cs, ce) of chunk k
+    __device__ __forceinline__ int chunk_begin(int k) const { return kCandThreads * (jr0 + kCandChunkBlocks * k); }
+    __device__ __forceinline__ int chunk_end(int k) const {
+        return min(a->vocab, kCandThreads * min(jr0 + kCandChunkBlocks * (k + 1), jr1));
+    }
+    __device__ __forceinline__ float *stage(int s) const { return stages + s * kCandStageFloats; }
+    // chunk k of `row` into stage s: the grid-aligned body of its columns
+    __device__ __forceinline__ void issue(int64_t row, int k, int s) const {
+        const float *p = row_start(*a, row);
         uint32_t bytes = 0;
         int dst = 0, c_lo = 0;
         if (p) {
-            const Geom r = geom(p);
-            const int cs = kCandThreads * (jr0 + kCandChunkBlocks * k);
-            const int ce = min(a.vocab, kCandThreads * min(jr0 + kCandChunkBlocks * (k + 1), jr1));
+            const RowGeom r = geom(p);
+            const int cs = chunk_begin(k), ce = chunk_end(k);
             c_lo = max(cs - r.off, r.h);
             const int c_hi = min(cs - r.off + ((ce - cs + r.off + 3) & ~3), r.e);
             if (c_hi > c_lo) {
@@ -796,43 +797,80 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
             }
         }
         mbar_arrive_expect_tx(&full[s], bytes);
-        if (bytes) bulk_copy_g2s(stages + s * kCandStageFloats + dst, p + c_lo, bytes, &full[s], policy);
-    };
-
-    constexpr uint32_t kWarps = kCandThreads / 32;
-    const uint64_t policy = l2_policy_evict_first();
-    if (t == 0) {
+        if (bytes) bulk_copy_g2s(stage(s) + dst, p + c_lo, bytes, &full[s], policy);
+    }
+    // thread 0, once, before a __syncthreads: the barriers and the first chunks
+    __device__ __forceinline__ void start() const {
         for (int s = 0; s < kCandStages; ++s) {
             mbar_init(&full[s], 1);
             used[s] = 0;
         }
         fence_mbar_init();
         int64_t row = cid;
-        for (int k = 0, s = 0; s < kCandStages && row < a.rows && nk > 0; ++s) {
-            issue(row, k, s, policy);
+        for (int k = 0, s = 0; s < kCandStages && row < a->rows && nk > 0; ++s) {
+            issue(row, k, s);
             if (++k == nk) k = 0, row += G;
         }
     }
+    // a warp is done with chunk k of `row` in stage s: the warp that finishes
+    // it last refills the stage with the chunk kCandStages ahead
+    __device__ __forceinline__ void release(int64_t row, int k, int s, int lane) const {
+        constexpr uint32_t kWarps = kCandThreads / 32;
+        int kn = k + kCandStages;
+        int64_t rn = row;
+        while (kn >= nk) kn -= nk, rn += G;
+        __syncwarp();
+        if (lane == 0 && rn < a->rows && atom_add_acq_rel_smem(&used[s], 1u) % kWarps == kWarps - 1)
+            issue(rn, kn, s);
+    }
+    // after a wait gave up: a last bounded wait for the copies still in flight
+    __device__ __forceinline__ void settle() const {
+        const int64_t K = cid < a->rows ? (a->rows - 1 - cid) / G + 1 : 0;
+        const int64_t total = K * nk;
+        for (int64_t gl = total > kCandStages ? total - kCandStages : 0; gl < total; ++gl)
+            (void)mbar_wait_bounded(&full[gl % kCandStages], static_cast<uint32_t>(gl / kCandStages) & 1u,
+                                    10000000ull);
+    }
+};
+
+// k_candidates: thread t of a 256-thread CTA is the pages' logical thread t
+// itself and keeps one sorted list in registers, over the columns t + 256 j of
+// its CTA's share of the row, streamed through a ChunkRing. Per chunk a thread
+// marks, in a 15-bit mask, its values above the list's 4th value as of the
+// chunk's start (never above the current one, so no value that belongs in the
+// list is left out) and then inserts the marked ones: a warp runs the
+// insertion once per value that some lane keeps, not once per value read.
+// For C > 1, CTAs 1..C-1 leave their lists in shared memory and CTA 0 pulls
+// and merges them through distributed shared memory and writes the row.
+__global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *__restrict__ out) {
+    using namespace cand;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const ChunkRing R(a, smem);
+    float2 *lt = reinterpret_cast<float2 *>(smem + kCandRingBytes) + threadIdx.x;  // list slots (split rows)
+    const int t = threadIdx.x, lane = t & 31;
+    const uint32_t rank = cluster_rank(), C = cluster_size();
+    const bool vec_out = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+    constexpr int kChunkCols = kCandChunkBlocks * kCandThreads;
+    if (t == 0) R.start();
     __syncthreads();
 
     bool failed = false;
-    int s = 0;          // stage of the next chunk
-    uint32_t ph = 0;    // and the parity of its phase
+    int s = 0;        // stage of the next chunk
+    uint32_t ph = 0;  // and the parity of its phase
     // Cluster barrier phases, per row: a wait before the list slots are
     // written (CTA 0 has pulled the previous row's lists), an arrive once they
     // are, a wait before the pull, an arrive after it.
     if (C > 1) cluster_arrive();
-    for (int64_t row = cid; row < a.rows; row += G) {
+    for (int64_t row = R.cid; row < a.rows; row += R.G) {
         const float *p = row_start(a, row);  // null: a row without values
-        const Geom r = p ? geom(p) : Geom{0, 0, 0};
+        const RowGeom r = p ? R.geom(p) : RowGeom{0, 0, 0};
         TopList L;
         top_init(L);
-        for (int k = 0; k < nk; ++k) {
-            if (!mbar_wait_bounded(&full[s], ph)) failed = true;
+        for (int k = 0; k < R.nk; ++k) {
+            if (!mbar_wait_bounded(&R.full[s], ph)) failed = true;
             if (p) {
-                const int cs = kCandThreads * (jr0 + kCandChunkBlocks * k);
-                const int ce = min(a.vocab, kCandThreads * min(jr0 + kCandChunkBlocks * (k + 1), jr1));
-                const float *sv = stages + s * kCandStageFloats + r.off + t;  // sv[256 u]: column cs + t + 256 u
+                const int cs = R.chunk_begin(k), ce = R.chunk_end(k);
+                const float *sv = R.stage(s) + r.off + t;  // sv[256 u]: column cs + t + 256 u
                 const float thr = L.v[3];
                 uint32_t mask = 0;
                 if (ce - cs == kChunkCols && cs >= r.h && ce <= r.e) {
@@ -853,14 +891,7 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
                     insert_marked(L, mask, cs + t, val);
                 }
             }
-            // done with the stage: the warp that finishes it last refills it
-            // with the chunk kCandStages ahead (in this row or a later one)
-            int kn = k + kCandStages;
-            int64_t rn = row;
-            while (kn >= nk) kn -= nk, rn += G;
-            __syncwarp();
-            if (lane == 0 && rn < a.rows && atom_add_acq_rel_smem(&used[s], 1u) % kWarps == kWarps - 1)
-                issue(rn, kn, s, policy);
+            R.release(row, k, s, lane);
             if (++s == kCandStages) s = 0, ph ^= 1u;
         }
         // a list with an empty slot takes, in column order, its columns that
@@ -869,7 +900,7 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
             int q = 0;
 #pragma unroll
             for (int k = 0; k < kTopEach; ++k) q += L.c[k] != kEmptyCol;
-            for (int jj = jr0; jj < jr1 && q < kTopEach; ++jj) {
+            for (int jj = R.jr0; jj < R.jr1 && q < kTopEach; ++jj) {
                 const int col = t + kCandThreads * jj;
                 if (col >= a.vocab || p[col] != -INFINITY) continue;
 #pragma unroll
@@ -918,10 +949,114 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
     if (C > 1) cluster_wait();  // the last arrive's match: no CTA leaves while CTA 0 may still pull
     if (__syncthreads_or(failed) && t == 0) {
         atomicAdd(&g_status[1], 1ull);
-        // give copies still in flight a last bounded chance to land: the last
-        // use of each stage
-        for (int64_t gl = total > kCandStages ? total - kCandStages : 0; gl < total; ++gl)
-            (void)mbar_wait_bounded(&full[gl % kCandStages], static_cast<uint32_t>(gl / kCandStages) & 1u, 10000000ull);
+        R.settle();
+    }
+}
+
+// k_argmax_ring: argmaxInto through the same ChunkRing, for few long rows.
+// Thread t keeps the first largest value of its columns t + 256 j (a strict
+// compare from -inf, so NaN never wins; a thread left without a value above
+// -inf takes its first -inf afterwards); for C > 1 CTA 0 pulls the peers'
+// thread-t states over distributed shared memory, then reduces its 256
+// states (larger value, then lower column) and writes the token, 0 for a row
+// of NaN only.
+__global__ void __launch_bounds__(kCandThreads, 4) k_argmax_ring(Args a) {
+    using namespace cand;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float2 red[kCandThreads / 32];
+    const ChunkRing R(a, smem);
+    float2 *lt = reinterpret_cast<float2 *>(smem + kCandRingBytes) + threadIdx.x;  // state slot (split rows)
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const uint32_t rank = cluster_rank(), C = cluster_size();
+    constexpr int kChunkCols = kCandChunkBlocks * kCandThreads;
+    if (t == 0) R.start();
+    __syncthreads();
+
+    bool failed = false;
+    int s = 0;
+    uint32_t ph = 0;
+    if (C > 1) cluster_arrive();
+    for (int64_t row = R.cid; row < a.rows; row += R.G) {
+        const float *p = row_start(a, row);
+        const RowGeom r = p ? R.geom(p) : RowGeom{0, 0, 0};
+        float best = -INFINITY;
+        int bcol = kNoIndex;
+        for (int k = 0; k < R.nk; ++k) {
+            if (!mbar_wait_bounded(&R.full[s], ph)) failed = true;
+            if (p) {
+                const int cs = R.chunk_begin(k), ce = R.chunk_end(k);
+                const float *sv = R.stage(s) + r.off + t;
+                if (ce - cs == kChunkCols && cs >= r.h && ce <= r.e) {
+#pragma unroll
+                    for (int u = 0; u < kCandChunkBlocks; ++u) {
+                        const float x = sv[kCandThreads * u];
+                        const bool gt = x > best;
+                        best = gt ? x : best;
+                        bcol = gt ? cs + t + kCandThreads * u : bcol;
+                    }
+                } else {
+#pragma unroll 4
+                    for (int u = 0; u < kCandChunkBlocks; ++u) {
+                        const int col = cs + t + kCandThreads * u;
+                        if (col < ce) {
+                            const float x = (col >= r.h && col < r.e) ? sv[kCandThreads * u] : ld_stream_f1(p + col);
+                            const bool gt = x > best;
+                            best = gt ? x : best;
+                            bcol = gt ? col : bcol;
+                        }
+                    }
+                }
+            }
+            R.release(row, k, s, lane);
+            if (++s == kCandStages) s = 0, ph ^= 1u;
+        }
+        // nothing above -inf among this thread's columns: its first -inf, if
+        // any, is its first value that is not NaN (rows of -inf and NaN only)
+        if (p && bcol == kNoIndex)
+            for (int jj = R.jr0; jj < R.jr1; ++jj) {
+                const int col = t + kCandThreads * jj;
+                if (col < a.vocab && p[col] == -INFINITY) {
+                    bcol = col;
+                    break;
+                }
+            }
+        if (C > 1) {
+            cluster_wait();  // CTA 0 has pulled the previous row's states
+            if (rank != 0) *lt = make_float2(best, __int_as_float(bcol));
+            cluster_arrive_release();
+            cluster_wait();
+            if (rank == 0)
+                for (uint32_t q = 1; q < C; ++q) {
+                    const float2 e = ld_dsmem_f2(peer_smem(lt, q));
+                    const int ec = __float_as_int(e.y);
+                    if (ranks_above(e.x, ec, best, bcol)) best = e.x, bcol = ec;
+                }
+            cluster_arrive_release();
+        }
+        if (rank == 0) {
+            // over the CTA: the larger value, then the lower column
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                const float ob = __shfl_xor_sync(kFullMask, best, d);
+                const int oc = __shfl_xor_sync(kFullMask, bcol, d);
+                if (ranks_above(ob, oc, best, bcol)) best = ob, bcol = oc;
+            }
+            if (lane == 0) red[warp] = make_float2(best, __int_as_float(bcol));
+            __syncthreads();
+            if (t == 0) {
+                for (int w = 1; w < kCandThreads / 32; ++w) {
+                    const int oc = __float_as_int(red[w].y);
+                    if (ranks_above(red[w].x, oc, best, bcol)) best = red[w].x, bcol = oc;
+                }
+                if (a.top) a.top[row] = !p ? __int_as_float(0x7fffffff) : static_cast<float>(bcol != kNoIndex ? bcol : 0);
+            }
+            __syncthreads();  // red is rewritten for the next row
+        }
+    }
+    if (C > 1) cluster_wait();
+    if (__syncthreads_or(failed) && t == 0) {
+        atomicAdd(&g_status[1], 1ull);
+        R.settle();
     }
 }
 
@@ -1145,6 +1280,7 @@ const void *kernel_of(const Plan &p, Op op) {
     if (op == kOpSoftmax) return fused_kernel<kModeSoftmax>(p.path);
     if (op == kOpLogSoftmax) return fused_kernel<kModeLogSoftmax>(p.path);
     if (op == kOpCandidates) return reinterpret_cast<const void *>(&k_candidates);
+    if (p.path == kPathRing) return reinterpret_cast<const void *>(&k_argmax_ring);
     if (p.path == kPathWarp)
         return op == kOpRows ? reinterpret_cast<const void *>(&k_rows_warp<true>)
                              : reinterpret_cast<const void *>(&k_rows_warp<false>);
@@ -1163,7 +1299,8 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
                          reinterpret_cast<const void *>(&k_grad_stream<kModeGrad>),
                          reinterpret_cast<const void *>(&k_grad_stream<kModeSoftmax>),
                          reinterpret_cast<const void *>(&k_grad_stream<kModeLogSoftmax>),
-                         reinterpret_cast<const void *>(&k_candidates)};
+                         reinterpret_cast<const void *>(&k_candidates),
+                         reinterpret_cast<const void *>(&k_argmax_ring)};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -1177,7 +1314,9 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
     }
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_candidates),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kCandMaxSmemBytes);
-    return e;
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_argmax_ring),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kCandMaxSmemBytes);
 }
 
 cudaError_t max_active_clusters(const Plan &p, Op op, int *n) {
@@ -1196,6 +1335,12 @@ cudaError_t max_active_clusters(const Plan &p, Op op, int *n) {
 }
 
 cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStream_t s) {
+    if (p.path == kPathRing) {
+        if (stats) return cudaErrorInvalidValue;  // the ring serves the argmax only
+        Args aa = a;
+        void *args[] = {&aa};
+        return launch_clustered(reinterpret_cast<const void *>(&k_argmax_ring), p, args, s);
+    }
     if (p.path == kPathWarp) {
         if (stats)
             k_rows_warp<true><<<static_cast<unsigned>(p.clusters), p.threads, 0, s>>>(a);

@@ -153,7 +153,8 @@ def test_zero_rows_is_a_no_op_without_device(lib):
 
 
 def test_debug_force_validation(lib):
-    assert lib.ce_debug_force(7, 0, 0) == ce.CE_EINVAL
+    assert lib.ce_debug_force(8, 0, 0) == ce.CE_EINVAL
+    assert lib.ce_debug_force(7, 0, 0) == ce.CE_OK
     assert lib.ce_debug_force(6, 0, 0) == ce.CE_OK
     assert lib.ce_debug_force(0, 17, 0) == ce.CE_EINVAL
     assert lib.ce_debug_force(0, 0, 1024) == ce.CE_EINVAL

@@ -86,7 +86,7 @@ def test_fused_and_row_kernels_in_sequence(orc, cap, vocab):
         assert_loss(loss, l_ref, f"grad loss cap {cap} {plan} V={vocab}")
         assert_tokens(top, a_ref, f"grad top cap {cap} {plan} V={vocab}")
         assert_softmax(soft, s_ref, f"softmax cap {cap} {plan} V={vocab}")
-    for plan in ((0, 0, 0), (2, 1, 0), (2, 3, 128), (6, 0, 0)):
+    for plan in ((0, 0, 0), (2, 1, 0), (2, 3, 128), (6, 0, 0), (7, 0, 0), (7, 3, 0)):
         lr = capped(cap, plan, ce.ce_rows, xd, yd, vocab=vocab)
         tk = capped(cap, plan, ce.argmax_rows, xd, vocab=vocab)
         torch.cuda.synchronize()

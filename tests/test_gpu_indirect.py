@@ -56,7 +56,7 @@ def table_of(pool, offs, pick):
     return (pool.data_ptr() + offs[pick] * 4).to(DEV)
 
 
-PLANS = [(0, 0, 0), (2, 1, 0), (2, 2, 0), (2, 4, 128), (6, 0, 0)]
+PLANS = [(0, 0, 0), (2, 1, 0), (2, 2, 0), (2, 4, 128), (6, 0, 0), (7, 0, 0), (7, 3, 0)]
 
 
 @pytest.mark.parametrize("plan", PLANS, ids=lambda p: f"path{p[0]}-c{p[1]}-t{p[2]}")

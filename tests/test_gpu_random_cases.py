@@ -72,6 +72,7 @@ def draw_case(seed):
     # drawn last, so the earlier draws of a seed stay as they were
     plans["grid_cap"] = int(rng.choice([0, 0, 0, 1, 2, 5]))     # clusters looping over several rows
     plans["host_chunk"] = int(rng.choice([0, 1, 5, rows]))      # ce_grad_host's rows per copied chunk
+    plans["ring"] = [(7, 0, 0), (7, 1, 0), (7, 3, 0), (7, 8, 0)][int(rng.integers(4))]  # the ring argmax
     return x, labels, vocab, offset, scale, plans
 
 
@@ -115,6 +116,7 @@ def test_random_case(orc, seed):
         top2 = forced_call(plans["rows"], ce.argmax_rows, dx, vocab=vocab)
         mean = ce.ce_mean(lr2)
         cand = forced_call(plans["cand"], ce.candidates_rows, dx, vocab=vocab)
+        top3 = forced_call(plans["ring"], ce.argmax_rows, dx, vocab=vocab)
         hs = ce.ce_grad_host(xh[:, :vocab], yh, scale, ce.HostStep(x.shape[0], vocab, DEV),
                              chunk_rows=plans["host_chunk"])
         torch.cuda.synchronize()
@@ -128,6 +130,7 @@ def test_random_case(orc, seed):
     assert_tokens(top, a_ref, f"{what}: ce_grad top")
     assert_loss(lr2, l_ref, f"{what}: ce_rows")
     assert_tokens(top2, a_ref, f"{what}: argmax_rows")
+    assert_tokens(top3, a_ref, f"{what}: argmax_rows (ring)")
     assert_mean(mean.item(), orc.ce_mean(l_ref), f"{what}: ce_mean", loss_rows=l_ref)
     assert_softmax(soft, orc.softmax(x, vocab, threads=THREADS), f"{what}: softmax_rows")
     assert_log_softmax(logp, orc.log_softmax(x, vocab, threads=THREADS), f"{what}: log_softmax_rows")
