@@ -258,6 +258,30 @@ def report_oracle(w, cores: int):
                           "GB/s": round(nbytes / full / 1e9, 3)}), flush=True)
 
 
+def report_page_f32(w):
+    """The oracle's page-f32 diagnostic (the literal f32 form of the loss,
+    16 lanes) beside the f64 oracle and the GPU's row losses, on up to 256
+    rows of a loss workload: reported, not graded -- the pages fix neither
+    the lanes nor their join."""
+    import numpy as np
+    import oracle
+    import row_wise_softmax_ce_gb300 as ce
+    n = min(w.rows, 256)
+    b = W.generate(w.with_rows(n), device="cuda")
+    gpu = ce.ce_rows(b.logits[:, : w.vocab], b.labels).double().cpu().numpy()
+    xs, ys = b.logits.cpu().numpy(), b.labels.cpu().numpy()
+    orc = oracle.load()
+    ref = orc.ce_rows(xs, w.vocab, ys, threads=cpu_cores())
+    page = orc.ce_rows_page_f32(xs, w.vocab, ys, threads=cpu_cores()).astype(np.float64)
+    ok = np.isfinite(ref) & (ref > 0)
+    rel_gpu = np.abs(gpu[ok] - ref[ok]) / ref[ok]
+    rel_page = np.abs(page[ok] - ref[ok]) / ref[ok]
+    print(json.dumps({"page_f32": w.name, "rows": n, "graded": False,
+                      "gpu_max_rel": float(rel_gpu.max()), "page_f32_max_rel": float(rel_page.max()),
+                      "gpu_rows_over_2e-5": int((rel_gpu > 2e-5).sum()),
+                      "page_f32_rows_over_2e-5": int((rel_page > 2e-5).sum())}), flush=True)
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -620,6 +644,10 @@ def main():
         # the oracle beside, single-threaded and on every host core
         for w in W.WORKLOADS.values():
             report_oracle(w, cpu_cores())
+        # the literal f32 form of the loss beside (a diagnostic, not graded)
+        for w in W.WORKLOADS.values():
+            if "loss" in w.ops or "rows" in w.ops:
+                report_page_f32(w)
         return 0
     if args.case:
         return run_case(args)

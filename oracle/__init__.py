@@ -74,6 +74,8 @@ class Oracle:
         lib.oracle_version.restype = ctypes.c_int
         lib.oracle_ce_rows.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
         lib.oracle_ce_rows.restype = ctypes.c_int
+        lib.oracle_ce_rows_page_f32.argtypes = [_vp, _i64, _i64, _i64, _vp, _vp]
+        lib.oracle_ce_rows_page_f32.restype = ctypes.c_int
         lib.oracle_ce_grad.argtypes = [_vp, _i64, _i64, _i64, _vp, ctypes.c_double, _vp, _vp]
         lib.oracle_ce_grad.restype = ctypes.c_int
         lib.oracle_ce_mean.argtypes = [_vp, _i64]
@@ -131,6 +133,22 @@ class Oracle:
                                          labels[a:b].ctypes.data, out[a:b].ctypes.data)
             if rc:
                 raise ValueError("oracle_ce_rows rejected its arguments")
+
+        self._run(fn, rows, threads)
+        return out
+
+    def ce_rows_page_f32(self, logits: np.ndarray, vocab: int, labels: np.ndarray, threads: int = 1):
+        """Diagnostic, not a reference: the row loss in the literal f32 form
+        (16 lanes joined pairwise, m + logf(s) - x[label]), f32 [rows]."""
+        rows, stride = self._check(logits, vocab)
+        labels = np.ascontiguousarray(labels, dtype=np.int64)
+        out = np.empty(rows, dtype=np.float32)
+
+        def fn(a, b):
+            rc = self.lib.oracle_ce_rows_page_f32(logits[a:b].ctypes.data, b - a, vocab, stride,
+                                                  labels[a:b].ctypes.data, out[a:b].ctypes.data)
+            if rc:
+                raise ValueError("oracle_ce_rows_page_f32 rejected its arguments")
 
         self._run(fn, rows, threads)
         return out

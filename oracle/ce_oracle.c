@@ -10,7 +10,9 @@
  *
  * Everything is computed in f64 from the f32 inputs (each input is widened
  * once), one row at a time, one column at a time, in column order, with no
- * blocking, vectorisation or fast-math. Build with plain gcc, e.g.
+ * blocking, vectorisation or fast-math -- but for one diagnostic,
+ * oracle_ce_rows_page_f32, which is f32 on purpose and graded by no test.
+ * Build with plain gcc, e.g.
  *     gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared ce_oracle.c -lm
  *
  * Source of every definition: the API reference page "gizml:netops"
@@ -114,6 +116,50 @@ int oracle_ce_rows(const float *logits, int64_t rows, int64_t vocab, int64_t str
             continue;
         }
         loss_out[i] = (st.m - (double)x[label]) + log1p(st.t);
+    }
+    return 0;
+}
+
+/*
+ * Diagnostic, not a reference (parity unpinned): crossEntropyRows computed
+ * the way the entry of crossEntropyLoss ("gizml:netops", Functions) writes
+ * it, in f32: m + log(sum exp(x - m)) - x[label] with "the sum in 16 lanes".
+ * The entry fixes neither which column goes to which lane nor how the lanes
+ * are joined; this reads them as 16 f32 partial sums, lane = column mod 16,
+ * joined pairwise in a tree of fixed shape (the join the page "Compute: all
+ * of the hardware from one program", section Parts, gives its strict sums).
+ * The max skips NaN (a compare with NaN is false); a NaN entry then makes
+ * the sum NaN. Every operation is f32: expf, logf, adds in the order above.
+ * It shows what the literal f32 form loses where the label holds a dominant
+ * max (m + log(s) with s just above 1 rounds the loss away).
+ * loss_out: rows floats. Returns 0, or -1 on a bad argument.
+ */
+int oracle_ce_rows_page_f32(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+                            const int64_t *labels, float *loss_out)
+{
+    if (rows < 0 || vocab < 1 || stride < vocab)
+        return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *x = logits + i * stride;
+        const int64_t label = labels[i];
+        float m = -INFINITY;
+        for (int64_t j = 0; j < vocab; ++j)
+            if (x[j] > m)
+                m = x[j];
+        float lane[16];
+        for (int k = 0; k < 16; ++k)
+            lane[k] = 0.0f;
+        for (int64_t j = 0; j < vocab; ++j)
+            lane[j % 16] += expf(x[j] - m);
+        for (int w = 8; w >= 1; w /= 2)
+            for (int k = 0; k < w; ++k)
+                lane[k] = lane[k] + lane[k + w];
+        if (label < 0 || label >= vocab) {
+            loss_out[i] = NAN;
+            continue;
+        }
+        const float ms = m + logf(lane[0]);
+        loss_out[i] = ms - x[label];
     }
     return 0;
 }
