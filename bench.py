@@ -20,7 +20,7 @@ Printed (one JSON line, rank 0):
               and on one core
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-    python bench.py --case grad|rows|argmax|softmax|log_softmax|candidates|split_sum|sharded
+    python bench.py --case grad|rows|loss|argmax|softmax|log_softmax|candidates|split_sum|sharded
                     [--workload W] [--rows R] [--force "path,cluster,threads;..."] [--flush]
     python bench.py --report     every operation on every workload
 
@@ -535,6 +535,11 @@ def run_case(args):
     elif args.case == "rows":
         op = lambda: ce.ce_rows(b.logits, b.labels, vocab=V, out=out)
         nbytes, opn = 4 * R * V + 12 * R, ce.OP_ROWS
+    elif args.case == "loss":
+        # crossEntropyLoss: the row losses, then their f64 mean on the device
+        mean = torch.empty((), dtype=torch.float64, device=dev)
+        op = lambda: ce.ce_loss(b.logits, b.labels, vocab=V, loss_rows=out, out=mean)
+        nbytes, opn = 4 * R * V + 16 * R + 8, ce.OP_ROWS
     elif args.case in ("softmax", "log_softmax"):
         dense = torch.empty((R, V), dtype=torch.float32, device=dev)
         fn = ce.softmax_rows if args.case == "softmax" else ce.log_softmax_rows
@@ -618,7 +623,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=8192, help="rows of the CPU-oracle sample")
     ap.add_argument("--ref-rows", type=int, default=256, help="rows per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["grad", "rows", "argmax", "softmax", "log_softmax", "candidates",
+    ap.add_argument("--case", choices=["grad", "rows", "loss", "argmax", "softmax", "log_softmax", "candidates",
                                        "split_sum", "sharded"],
                     help="time one operation only (sweeps, profiler captures)")
     ap.add_argument("--report", action="store_true",
@@ -636,7 +641,7 @@ def main():
         import copy
         for name, w in W.WORKLOADS.items():
             small = 4 * w.rows * w.stride < 4 * torch.cuda.get_device_properties(0).L2_cache_size
-            for case in ("rows", "grad", "argmax", "softmax", "candidates"):
+            for case in ("rows", "loss", "grad", "argmax", "softmax", "candidates"):
                 a = copy.copy(args)
                 a.case, a.workload, a.rows, a.force, a.flush = case, name, 0, "", small
                 a.steps = min(args.steps, 50)
