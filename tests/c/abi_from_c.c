@@ -39,6 +39,21 @@ int main(void)
     expect(ce_rows(NULL, 0, 10, 10, NULL, NULL, NULL) == CE_OK, "ce_rows: zero rows");
     expect(softmax_rows(NULL, 0, 10, 10, NULL, NULL) == CE_OK, "softmax_rows: zero rows");
     expect(ce_debug_force(0, 0, 0) == CE_OK, "debug_force reset");
+    expect(ce_debug_force(7, 2, 0) == CE_OK && ce_debug_force(0, 0, 0) == CE_OK, "debug_force: the ring path");
+    expect(ce_debug_grid_cap(-1) == CE_EINVAL, "grid cap: negative");
+    expect(ce_debug_grid_cap(0) == CE_OK, "grid cap: none");
+    /* the host-fed step: argument checks answer before any copy */
+    expect(ce_grad_host(NULL, 4, 10, 10, (const int64_t *)512, 1.0, (float *)4096, (int64_t *)8192,
+                        (float *)16384, (float *)32768, NULL, (double *)65536, NULL, NULL, 0, NULL) == CE_EINVAL,
+           "ce_grad_host: null host logits");
+    expect(ce_grad_host((const float *)256, 4, 10, 10, (const int64_t *)516, 1.0, (float *)4096,
+                        (int64_t *)8192, (float *)16384, (float *)32768, NULL, (double *)65536, NULL, NULL, 0,
+                        NULL) == CE_EALIGN,
+           "ce_grad_host: misaligned host labels");
+    expect(ce_grad_host((const float *)256, 4, 10, 10, (const int64_t *)512, 1.0, (float *)4096,
+                        (int64_t *)8192, (float *)16384, (float *)32768, NULL, (double *)65536, NULL,
+                        (float *)1024, 0, NULL) == CE_EINVAL,
+           "ce_grad_host: tokens back without device tokens");
     printf("%s\n", failures ? "abi from C: FAILED" : "abi from C: ok");
     return failures ? 1 : 0;
 }
