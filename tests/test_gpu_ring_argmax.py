@@ -116,3 +116,31 @@ def test_automatic_plans():
     assert ce.plan(ce.OP_ARGMAX, 256, 151936)["path"] == ce.PATH_STREAM
     assert ce.plan(ce.OP_ARGMAX, 4096, 32000)["path"] == ce.PATH_WARP
     assert ce.plan(ce.OP_ROWS, 8192, 128256)["path"] == ce.PATH_STREAM
+
+
+@pytest.mark.parametrize("cluster", [1, 3])
+def test_indirect_rows_and_bad_addresses(orc, cluster):
+    """Rows read at the addresses of a table (any 4-byte phase, repeats);
+    a null or misaligned address is never read: that row's token is NaN."""
+    vocab, n = 7681, 12
+    g = torch.Generator().manual_seed(cluster)
+    rows = (3.0 * torch.randn(n, vocab, generator=g)).float()
+    rows[2, ::3] = float("nan")
+    pool = torch.full((n * (vocab + 7) + 8,), 1e30, device=DEV)
+    offs = [r * (vocab + 7) + (r % 4) for r in range(n)]
+    for r, o in enumerate(offs):
+        pool[o: o + vocab] = rows[r].to(DEV)
+    pick = torch.tensor([5, 0, 11, 5, 2, 9, 1, 3])
+    table = (pool.data_ptr() + torch.tensor(offs)[pick] * 4).to(DEV)
+    table[1] = 0                      # null
+    table[6] = table[6] + 2           # not 4-byte aligned
+    ce.debug_force(ce.PATH_RING, cluster, 0)
+    try:
+        top = ce.argmax_rows_indirect(table, vocab)
+    finally:
+        ce.debug_force(0, 0, 0)
+    torch.cuda.synchronize()
+    t = top.cpu().numpy()
+    assert torch.isnan(top[1]) and torch.isnan(top[6])
+    good = [0, 2, 3, 4, 5, 7]
+    assert_tokens(t[good], orc.argmax(rows[pick[good]].numpy().copy(), vocab), f"ring indirect c{cluster}")
