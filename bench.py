@@ -2,19 +2,26 @@
 
 One step is one pass of the whole path over one batch of the training
 workload ce_8192x128256 (8192 rows x 128256 vocab, f32 logits N(0, 3^2),
-4.2 GB): ce_grad writes the gradient, each row's loss and each row's argmax
-token from one read of the logits, then ce_mean writes the f64 mean loss.
+4.2 GB): one ce_grad_step call, whose fused kernel writes the gradient, each
+row's loss and each row's argmax token from one read of the logits, and whose
+mean kernel (a programmatic dependent launch) writes the f64 mean loss.
 
 Printed (one JSON line, rank 0):
   value       fused loss + grad GB/s of the step: algorithmic bytes
               (8 * rows * vocab + 16 * rows + 8) / device time per step
-  roofline    the dominant kernel (the fused one) against measured HBM bandwidth
+  roofline    the dominant kernel (the fused one) against measured HBM
+              bandwidth: the same launch timed alone, K times, with events
+              around each launch, right after the steps
   argmax      rows/s of argmax_rows on the decode workload (256 x 151936,
-              row stride 152064), L2 flushed before every timed launch
+              row stride 152064), L2 flushed before every timed launch, with
+              a plain read of the same buffer beside it (torch.sum, same run,
+              same flush) as the ceiling of a read of that size
   candidates  rows/s of candidates_rows on the same decode batch, likewise
   e2e         the same metric through ce_grad_host: the inputs copied from
               pinned host memory (in chunks, overlapped with the kernels) and
-              the mean loss and tokens copied back inside the timed region
+              the mean loss and tokens copied back inside the timed region;
+              beside it a plain pinned host-to-device copy of the same logits
+              (same run), the host link's ceiling
   d2d_copy    a plain device copy of the same bytes, for comparison
   cpu_baseline the CPU oracle (f64) timed on the host cores on a row sample,
               and on one core
@@ -347,11 +354,16 @@ def run_ours(args):
     mean = torch.empty((), dtype=torch.float64, device=dev)
 
     def step():
+        # the fused kernel, then the mean as its programmatic dependent
+        ce.ce_grad_step(x, y, scale, grad=grad, loss_rows=loss_rows, top=top, mean=mean)
+
+    def fused_only():
+        # the same fused launch without the mean
         ce.ce_grad(x, y, scale, grad=grad, loss_rows=loss_rows, top=top)
-        ce.ce_mean(loss_rows, out=mean)
 
     for _ in range(max(3, args.warmup)):
         step()
+        fused_only()
     torch.cuda.synchronize()
 
     K = args.steps
@@ -360,13 +372,16 @@ def run_ours(args):
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        # the steps: nothing between the fused kernel and its mean
         t_start.record(stream)
+        for _ in range(K):
+            step()
+        t_end.record(stream)
+        # the dominant kernel alone, events around each launch
         for i in range(K):
             ev[i][0].record(stream)
-            ce.ce_grad(x, y, scale, grad=grad, loss_rows=loss_rows, top=top)
+            fused_only()
             ev[i][1].record(stream)
-            ce.ce_mean(loss_rows, out=mean)
-        t_end.record(stream)
         torch.cuda.synchronize()
     barrier(ws)
     step_ms_local = t_start.elapsed_time(t_end) / K
@@ -416,6 +431,22 @@ def run_ours(args):
     torch.cuda.synchronize()
     arg_all = [a.elapsed_time(c) for a, c in times]
     arg_ms = max_over_ranks(statistics.median(arg_all), ws)
+    # the ceiling of a read of this size on this machine, same run, same flush: a
+    # plain reduction over the same buffer (its padding included, +0.08%)
+    for _ in range(3):
+        torch.sum(bd.logits)
+    times = []
+    for _ in range(n_arg):
+        l2_flush(flush)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        torch.sum(bd.logits)
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    read_all = [a.elapsed_time(c) for a, c in times]
+    read_ms = statistics.median(read_all)
+    read_bytes = bd.logits.numel() * 4
     # sampling candidates (candidatesInto) of the same decode batch, L2 flushed too
     cand = torch.empty((wd.rows, ce.CANDIDATE_ROW), dtype=torch.float32, device=dev)
     for _ in range(3):
@@ -439,6 +470,7 @@ def run_ours(args):
     # it has landed), the mean and the tokens back into pinned host memory
     xh = torch.empty((R, V), dtype=torch.float32, pin_memory=True)
     xh.copy_(x)
+    xh_bytes = xh.numel() * 4
     yh = y.cpu().pin_memory()
     hs = ce.HostStep(R, V, dev)
 
@@ -460,6 +492,17 @@ def run_ours(args):
     e2e_value = aggregate_gbs(ws, bytes_step, e2e_ms)
     h2d = xh.numel() * 4 + yh.numel() * 8
     d2h = 8 + hs.top_h.numel() * 4
+    # the host link's ceiling, same run: one plain pinned copy of the same logits
+    link_ms = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        hs.logits.copy_(xh, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        link_ms.append(e0.elapsed_time(e1))
+    link_best = min(link_ms)
+    link_gbs = xh.numel() * 4 / (link_best * 1e-3) / 1e9
     del xh, hs
 
     # ---- the CPU oracle on a row sample (rank 0, N = 1 only)
@@ -483,7 +526,9 @@ def run_ours(args):
             "warmup": max(3, args.warmup), "ms_per_step": round(step_ms, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "rows": R, "vocab": V, "stride": V, "logits": "N(0, 3^2) f32",
-                       "scale": scale, "step": "ce_grad (gradient + loss rows + argmax) then ce_mean",
+                       "scale": scale,
+                       "step": "ce_grad_step: the fused kernel (gradient + loss rows + argmax) and the "
+                               "f64 mean as its programmatic dependent",
                        "l2": "no flush: inputs (4.2 GB) larger than L2", "parallelism": f"replicas x{ws}",
                        "plan": plan},
             "percent_of_hbm_peak": round(100 * value / ws / peak, 2),
@@ -500,15 +545,25 @@ def run_ours(args):
                        "ms": round(arg_ms, 5), "ms_min": round(min(arg_all), 5),
                        "GB/s": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9, 1),
                        "frac": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9 / peak, 4),
-                       "l2": "flushed before each launch"},
+                       "l2": "flushed before each launch",
+                       "plain_read": {"what": "torch.sum of the same padded buffer, same flush",
+                                      "bytes": read_bytes, "ms": round(read_ms, 5),
+                                      "ms_min": round(min(read_all), 5),
+                                      "GB/s": round(read_bytes / (read_ms * 1e-3) / 1e9, 1),
+                                      "argmax_over_read": round(arg_ms / read_ms, 4)}},
             "candidates": {"workload": wd.name, "rows_per_s": round(ws * wd.rows / (cand_ms * 1e-3), 1),
                            "ms": round(cand_ms, 5), "ms_min": round(min(cand_all), 5),
                            "GB/s": round(cand_bytes / (cand_ms * 1e-3) / 1e9, 1),
                            "frac": round(cand_bytes / (cand_ms * 1e-3) / 1e9 / peak, 4),
                            "l2": "flushed before each launch"},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+                    "host_link": {"what": "one pinned host-to-device copy of the logits, best of 3",
+                                  "bytes": xh_bytes, "ms": round(link_best, 3), "GB/s": round(link_gbs, 1),
+                                  "e2e_step_over_copy": round(e2e_ms / link_best, 4)}},
             "gpu_launches": 2 * K,
+            "gpu_launches_note": "the steps' region: k_grad_staged + k_mean per step; the fused "
+                                 "kernel's own loop adds K more launches of k_grad_staged",
             "cpu_baseline": cpu,
             "clocks": clk,
         }

@@ -86,8 +86,12 @@ CE_API int ce_rows(const float *logits, int64_t rows, int64_t vocab, int64_t str
  * The mean step of crossEntropyLoss (gizml:netops, Functions): the mean of
  * `rows` f32 row losses, accumulated in f64, written as one double to
  * *loss_mean (a device pointer; the value stays on the device, so a
- * recorded step never waits for it). The sum is a fixed-shape tree: the
- * same inputs give the same bits on every run.
+ * recorded step never waits for it). The sum is a fixed-shape tree over a
+ * cluster of CTAs that does not depend on the device: the same inputs give
+ * the same bits on every run. The kernel is launched as a programmatic
+ * dependent of the kernel before it on `stream` (it waits for that kernel to
+ * complete before reading anything), so after this library's row kernels it
+ * starts without a launch gap.
  *   loss_rows: [rows] f32, read only.   loss_mean: 1 double, written.
  */
 CE_API int ce_mean(const float *loss_rows, int64_t rows, double *loss_mean, ce_stream_t stream);
@@ -106,17 +110,31 @@ CE_API int ce_loss(const float *logits, int64_t rows, int64_t vocab, int64_t str
  *     softmax_ij = exp(x_ij - m_i) * f32(1 / sum_i),
  * with `scale` (e.g. 1/rows, the gradient of the mean over rows) rounded to
  * f32. One kernel reads each logit once from HBM and writes each gradient
- * once; it can also write, from the same read, each row's loss (as ce_rows)
- * and each row's argmax token as f32 (as argmax_rows).
+ * once; from the same read it can also write each row's loss (as ce_rows).
  *   logits:    [rows, stride] f32, read only, unless grad == logits.
  *   labels:    [rows] int64, read only.
  *   grad:      [rows, vocab] f32 dense, written. grad == logits (in place)
  *              is allowed when stride == vocab; any other overlap is not.
- *   loss_rows: [rows] f32 or NULL.   top: [rows] f32 or NULL.
+ *   loss_rows: [rows] f32, or NULL.
  */
 CE_API int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
-            const int64_t *labels, double scale, float *grad, float *loss_rows, float *top,
-            ce_stream_t stream);
+            const int64_t *labels, double scale, float *grad, float *loss_rows, ce_stream_t stream);
+
+/*
+ * The whole training-step path from one read of the logits: ce_grad's
+ * gradient and row losses, each row's argmax token (argmaxInto's rule, as
+ * argmax_rows writes it) and the mean loss (crossEntropyLoss, as ce_mean
+ * writes it). Arguments as ce_grad, and:
+ *   top:       [rows] f32, or NULL.
+ *   loss_mean: 1 double on the device, or NULL; needs loss_rows (CE_EINVAL
+ *              otherwise). The mean kernel is launched as a programmatic
+ *              dependent of the fused kernel: it is scheduled while the fused
+ *              kernel finishes and reads the row losses only once that kernel
+ *              has completed, so the step costs no separate launch gap.
+ */
+CE_API int ce_grad_step(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
+                        const int64_t *labels, double scale, float *grad, float *loss_rows, float *top,
+                        double *loss_mean, ce_stream_t stream);
 
 /*
  * crossEntropyGrad and crossEntropyLoss of a batch that is in HOST memory:
@@ -158,21 +176,9 @@ CE_API int ce_grad_host(const float *logits_h, int64_t rows, int64_t vocab, int6
  * into top[rows]. The direct form (rows at logits + i * stride); for rows
  * given by a table of addresses see argmax_rows_indirect.
  *   logits:    [rows, stride] f32, read only.   top: [rows] f32, written.
- *   workspace: NULL, or workspace_bytes of device memory (8-byte aligned,
- *              any contents, owned by the caller, not read by the host) that
- *              lets few long rows be split evenly over the whole GPU: a call
- *              given at least argmax_workspace_bytes(rows, vocab, stride)
- *              bytes may use it; with less it runs without. Two calls that
- *              may run at once on the GPU need separate workspaces.
  */
 CE_API int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top,
-                       void *workspace, int64_t workspace_bytes, ce_stream_t stream);
-
-/*
- * Bytes of workspace argmax_rows can use for this shape on the current
- * device (0: none would be used). Host only; launches nothing.
- */
-CE_API int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t stride);
+                       ce_stream_t stream);
 
 /*
  * argmax_rows_noalloc -- the tokens of argmax_rows (same rule, same f32
@@ -265,7 +271,7 @@ CE_API int candidates_rows(const float *logits, int64_t rows, int64_t vocab, int
  *   top:  [rows] f32, written.   cand: [rows, 2048] f32, written.
  * An address that is null or not 4-byte aligned is detected on the device and
  * never read: that row's token is NaN, its candidates all (-inf, -1). The
- * outputs must not overlap any row. A forced even split (path 5) is refused.
+ * outputs must not overlap any row.
  */
 CE_API int argmax_rows_indirect(const uint64_t *row_addrs, int64_t rows, int64_t vocab, float *top,
                                 ce_stream_t stream);
@@ -349,22 +355,27 @@ CE_API int ce_version(void);
 CE_API int ce_last_cuda_error(void);
 
 /*
- * Device-side error counters of the current device, for tests and
- * diagnostics: counts[0] = rows seen with a label outside [0, vocab);
- * counts[1] = waits on an asynchronous copy that gave up after their time
- * limit (the output of that call is then undefined). This call WAITS for
- * `stream` to finish. ce_device_error_reset zeroes both counters (enqueued
- * on `stream`).
+ * Device-side error counter of the current device, for tests and
+ * diagnostics: *out = rows seen with a label outside [0, vocab) since the
+ * last reset. This call WAITS for `stream` to finish.
  */
-CE_API int ce_device_error_count(ce_stream_t stream, uint64_t counts[2]);
+CE_API int ce_device_error_count(ce_stream_t stream, int64_t *out);
+
+/*
+ * The second device counter: waits on an asynchronous copy or a peer CTA
+ * that gave up after their time limit (the output of such a call is then
+ * undefined; the kernel still ran to its end). WAITS for `stream`.
+ * ce_device_error_reset zeroes both counters (enqueued on `stream`).
+ */
+CE_API int ce_device_wait_timeouts(ce_stream_t stream, int64_t *out);
 CE_API int ce_device_error_reset(ce_stream_t stream);
 
 /*
  * Launch-plan override, for tests and tuning: forces the kernel family
  * (path: 0 automatic, 1 shared-memory-staged (persistent), 2 streaming from
  * global, 3 refused (formerly a ring-of-copies kernel), 4
- * shared-memory-staged with one row per cluster, 5 argmax split evenly over
- * the GPU -- needs a workspace, 6 one warp per row -- ce_rows, ce_loss,
+ * shared-memory-staged with one row per cluster, 5 refused (the argmax split
+ * evenly over the GPU is argmax_rows_noalloc's own plan), 6 one warp per row -- ce_rows, ce_loss,
  * argmax_rows and ce_stats only, 7 argmax through a ring of bulk-copied row
  * chunks -- argmax_rows and argmax_rows_indirect only), the CTAs that share
  * one row (cluster: 0 automatic, else 1..16; candidates_rows and path 7 take
@@ -378,7 +389,7 @@ CE_API int ce_debug_force(int path, int cluster, int threads);
 
 /*
  * Grid override, for tests: at most `clusters` clusters (0: no cap) in every
- * later launch of a row kernel (all but the even-split argmax), so that each
+ * later launch of a row kernel (not argmax_rows_noalloc's), so that each
  * cluster loops over several rows even when the rows are few. Results are
  * the same; only the schedule changes. Returns CE_EINVAL for clusters < 0.
  */

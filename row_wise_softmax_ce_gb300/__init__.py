@@ -15,7 +15,10 @@ Functions, and section Methods for the argmax rule):
 - ``ce_mean``      the f64 mean of row losses (the last step of crossEntropyLoss)
 - ``ce_loss``      crossEntropyLoss: ``ce_rows`` then ``ce_mean``
 - ``ce_grad``      crossEntropyGrad: (softmax - onehot) * scale, optionally with
-                   the row losses and argmax tokens from the same read
+                   the row losses (and, through ``ce_grad_step``, the argmax
+                   tokens) from the same read
+- ``ce_grad_step`` the whole step from one read of the logits: gradient, row
+                   losses, argmax tokens and the f64 mean loss
 - ``argmax_rows``  argmaxInto: each row's token (first of equals, NaN never wins) as f32
 - ``candidates_rows``  candidatesInto: each row's 2048-float sampling candidates
                    (256 threads x TOP_EACH = 4 (value, token) pairs)
@@ -73,9 +76,9 @@ def _bind(lib):
         "ce_rows": [vp, i64, i64, i64, vp, vp, vp],
         "ce_mean": [vp, i64, vp, vp],
         "ce_loss": [vp, i64, i64, i64, vp, vp, vp, vp],
-        "ce_grad": [vp, i64, i64, i64, vp, ctypes.c_double, vp, vp, vp, vp],
-        "argmax_rows": [vp, i64, i64, i64, vp, vp, i64, vp],
-        "argmax_workspace_bytes": [i64, i64, i64],
+        "ce_grad": [vp, i64, i64, i64, vp, ctypes.c_double, vp, vp, vp],
+        "ce_grad_step": [vp, i64, i64, i64, vp, ctypes.c_double, vp, vp, vp, vp, vp],
+        "argmax_rows": [vp, i64, i64, i64, vp, vp],
         "argmax_rows_noalloc": [vp, i64, i64, i64, vp, vp],
         "softmax_rows": [vp, i64, i64, i64, vp, vp],
         "log_softmax_rows": [vp, i64, i64, i64, vp, vp],
@@ -88,7 +91,8 @@ def _bind(lib):
         "ce_grad_from_stats": [vp, i64, i64, i64, i64, vp, vp, ctypes.c_double, vp, vp],
         "ce_version": [],
         "ce_last_cuda_error": [],
-        "ce_device_error_count": [vp, ctypes.POINTER(ctypes.c_uint64)],
+        "ce_device_error_count": [vp, ctypes.POINTER(ctypes.c_int64)],
+        "ce_device_wait_timeouts": [vp, ctypes.POINTER(ctypes.c_int64)],
         "ce_device_error_reset": [vp],
         "ce_debug_force": [i32, i32, i32],
         "ce_debug_grid_cap": [i64],
@@ -98,7 +102,7 @@ def _bind(lib):
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
-        fn.restype = i64 if name == "argmax_workspace_bytes" else i32
+        fn.restype = i32
     lib.ce_status_string.argtypes = [i32]
     lib.ce_status_string.restype = ctypes.c_char_p
     return lib
@@ -215,7 +219,8 @@ def ce_grad(logits: torch.Tensor, labels: torch.Tensor, scale: float, vocab: int
 
     ``grad`` may be ``logits`` itself (in place) when the logits are dense.
     With ``loss_rows`` / ``top`` (True or a tensor) the same kernel also
-    writes each row's loss and argmax token; the result is then a tuple
+    writes each row's loss and argmax token (``top`` goes through the C entry
+    point ``ce_grad_step``, without its mean); the result is then a tuple
     ``(grad, loss_rows, top)`` with None for what was not asked.
     """
     rows, vocab, stride = _logits_view(logits, vocab)
@@ -225,14 +230,39 @@ def ce_grad(logits: torch.Tensor, labels: torch.Tensor, scale: float, vocab: int
     lr = None if loss_rows is False else _out(None if loss_rows is True else loss_rows,
                                               (rows,), torch.float32, dev, "loss_rows")
     tp = None if top is False else _out(None if top is True else top, (rows,), torch.float32, dev, "top")
+    ptr = lambda t: t.data_ptr() if t is not None else None
     with torch.cuda.device(dev):
-        _check("ce_grad", lib().ce_grad(
-            logits.data_ptr(), rows, vocab, stride, labels.data_ptr(), float(scale), grad.data_ptr(),
-            lr.data_ptr() if lr is not None else None, tp.data_ptr() if tp is not None else None,
-            _stream(dev)))
+        if tp is None:
+            _check("ce_grad", lib().ce_grad(logits.data_ptr(), rows, vocab, stride, labels.data_ptr(),
+                                             float(scale), grad.data_ptr(), ptr(lr), _stream(dev)))
+        else:
+            _check("ce_grad_step", lib().ce_grad_step(logits.data_ptr(), rows, vocab, stride, labels.data_ptr(),
+                                                       float(scale), grad.data_ptr(), ptr(lr), ptr(tp), None,
+                                                       _stream(dev)))
     if loss_rows is False and top is False:
         return grad
     return grad, lr, tp
+
+
+def ce_grad_step(logits: torch.Tensor, labels: torch.Tensor, scale: float, vocab: int | None = None,
+                 grad: torch.Tensor | None = None, loss_rows: torch.Tensor | None = None,
+                 top: torch.Tensor | None = None, mean: torch.Tensor | None = None):
+    """The training step's whole path from one read of the logits: returns
+    ``(grad, loss_rows, top, mean)`` -- the gradient (dense f32 ``[rows,
+    vocab]``), each row's loss and argmax token (f32 ``[rows]``) and the mean
+    loss (0-d float64 on the device). Outputs not given are allocated."""
+    rows, vocab, stride = _logits_view(logits, vocab)
+    dev = logits.device
+    labels = _labels(labels, rows, dev)
+    grad = _out(grad, (rows, vocab), torch.float32, dev, "grad")
+    loss_rows = _out(loss_rows, (rows,), torch.float32, dev, "loss_rows")
+    top = _out(top, (rows,), torch.float32, dev, "top")
+    mean = _out(mean, (), torch.float64, dev, "mean")
+    with torch.cuda.device(dev):
+        _check("ce_grad_step", lib().ce_grad_step(logits.data_ptr(), rows, vocab, stride, labels.data_ptr(),
+                                                   float(scale), grad.data_ptr(), loss_rows.data_ptr(),
+                                                   top.data_ptr(), mean.data_ptr(), _stream(dev)))
+    return grad, loss_rows, top, mean
 
 
 class HostStep:
@@ -285,21 +315,13 @@ def ce_grad_host(logits_h: torch.Tensor, labels_h: torch.Tensor, scale: float, s
 
 def argmax_rows(logits: torch.Tensor, vocab: int | None = None,
                 out: torch.Tensor | None = None) -> torch.Tensor:
-    """argmaxInto: each row's token as f32 ``[rows]`` (first of equals; NaN never wins).
-
-    When the library can split few long rows over the whole GPU it asks for a
-    small workspace, allocated here from PyTorch's allocator on the current
-    stream."""
+    """argmaxInto: each row's token as f32 ``[rows]`` (first of equals; NaN never wins)."""
     rows, vocab, stride = _logits_view(logits, vocab)
     dev = logits.device
     out = _out(out, (rows,), torch.float32, dev, "out")
     with torch.cuda.device(dev):
-        L = lib()
-        ws_bytes = int(L.argmax_workspace_bytes(rows, vocab, stride)) if rows > 0 else 0
-        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes > 0 else None
-        _check("argmax_rows", L.argmax_rows(logits.data_ptr(), rows, vocab, stride, out.data_ptr(),
-                                            ws.data_ptr() if ws is not None else None, ws_bytes,
-                                            _stream(dev)))
+        _check("argmax_rows", lib().argmax_rows(logits.data_ptr(), rows, vocab, stride, out.data_ptr(),
+                                                _stream(dev)))
     return out
 
 
@@ -495,12 +517,15 @@ def status_string(status: int) -> str:
 
 
 def device_error_count(device=None) -> tuple[int, int]:
-    """(rows seen with a bad label, waits that gave up) on the device; waits for its stream."""
+    """(rows seen with a bad label, waits that gave up) on the device, from
+    ce_device_error_count and ce_device_wait_timeouts; waits for its stream."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    counts = (ctypes.c_uint64 * 2)()
+    bad, waits = ctypes.c_int64(0), ctypes.c_int64(0)
     with torch.cuda.device(dev):
-        _check("ce_device_error_count", lib().ce_device_error_count(_stream(dev), counts))
-    return int(counts[0]), int(counts[1])
+        L = lib()
+        _check("ce_device_error_count", L.ce_device_error_count(_stream(dev), ctypes.byref(bad)))
+        _check("ce_device_wait_timeouts", L.ce_device_wait_timeouts(_stream(dev), ctypes.byref(waits)))
+    return int(bad.value), int(waits.value)
 
 
 def device_error_reset(device=None) -> None:

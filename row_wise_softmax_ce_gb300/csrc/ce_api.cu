@@ -189,18 +189,6 @@ bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &
     return true;
 }
 
-// The even split of few long rows (argmax only): two 512-thread CTAs per SM,
-// each CTA at least 8192 elements. Taken only when forced (path 5): measured
-// on GB300 it is not yet ahead of the cluster split (256 x 151936, L2
-// flushed: 42.0 us with its combine launch, against 32.8 us).
-bool flat_applies(int64_t rows, int64_t vocab, const DeviceInfo &dev, bool forced) {
-    const int64_t ctas = 2 * static_cast<int64_t>(dev.sms);
-    if (rows * vocab < ctas * 8192) return false;
-    return forced;
-}
-
-int64_t flat_workspace_bytes(int64_t rows, const DeviceInfo &dev) { return 8 * (2 * static_cast<int64_t>(dev.sms) + rows); }
-
 // Launch shape of the candidates kernel: 256 threads (the pages' workgroup);
 // a row split over C = 2 x SMs / rows CTAs (about two per SM), 1 <= C <= 8,
 // each with at least 2048 columns. Measured on GB300, rows x 151936, L2
@@ -278,14 +266,10 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
         if (op != kOpArgmax || (f.threads && f.threads != kCandThreads) || f.cluster > kCandMaxCluster)
             return CE_EINVAL;
         plan_argmax_ring(p, rows, vocab, dev, f.cluster);
-    } else if (op == kOpArgmax && (f.path == kPathFlat || (f.path == kPathAuto && f.cluster == 0 && f.threads == 0)) &&
-               flat_applies(rows, vocab, dev, f.path == kPathFlat)) {
-        p.path = kPathFlat;
-        p.cluster = 1;
-        p.threads = 512;
-        p.smem = 0;
-        p.cols = static_cast<int>(vocab);
-        p.clusters = 2 * static_cast<int64_t>(dev.sms);
+    } else if (f.path == kPathFlat) {
+        // the even split needs scratch for its per-segment keys: only
+        // argmax_rows_noalloc, which owns a fixed array, runs it
+        return CE_EINVAL;
     } else if (f.path == kPathWarp) {
         if ((f.threads && f.threads != 256) || f.cluster > 1 || !plan_warp(p, op, rows)) return CE_EINVAL;
     } else if (f.path == kPathAuto && f.cluster == 0 && f.threads == 0 && warp_applies(op, rows, vocab, dev) &&
@@ -299,9 +283,9 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
     }
     if (p.cluster < 1 || p.cluster > kMaxCluster) return CE_EINVAL;
     if (p.path == kPathStream && p.threads > kStreamMaxThreads) return CE_EINVAL;
-    // every row kernel but the even split loops over rows with a stride of
-    // the cluster count, so a smaller grid only gives each cluster more rows
-    if (f.grid_cap > 0 && p.path != kPathFlat) p.clusters = std::min(p.clusters, f.grid_cap);
+    // every row kernel loops over rows with a stride of the cluster count, so
+    // a smaller grid only gives each cluster more rows
+    if (f.grid_cap > 0) p.clusters = std::min(p.clusters, f.grid_cap);
     *out = p;
     return CE_OK;
 }
@@ -359,6 +343,35 @@ Args make_args(const float *logits, int64_t rows, int64_t vocab, int64_t stride,
     return a;
 }
 
+// The checks and the fused launch behind ce_grad and ce_grad_step.
+int grad_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, const int64_t *labels,
+              double scale, float *grad, float *loss_rows, float *top, ce_stream_t stream) {
+    int st = check_logits(logits, rows, vocab, stride);
+    if (st) return st;
+    if (!std::isfinite(scale)) return CE_EINVAL;
+    if (rows > 0 && (labels == nullptr || grad == nullptr)) return CE_EINVAL;
+    if (misaligned(labels, 8) || misaligned(grad, 4) || misaligned(loss_rows, 4) || misaligned(top, 4))
+        return CE_EALIGN;
+    if (rows == 0) return CE_OK;
+    const int64_t in_bytes = ((rows - 1) * stride + vocab) * 4;
+    const int64_t out_bytes = rows * vocab * 4;
+    if (grad == logits) {
+        if (stride != vocab) return CE_EINVAL;  // in place needs the same layout
+    } else if (ranges_overlap(grad, out_bytes, logits, in_bytes)) {
+        return CE_EINVAL;
+    }
+    DeviceInfo dev;
+    if ((st = current_device(&dev))) return st;
+    Plan p;
+    if ((st = make_plan(kOpGrad, rows, vocab, dev, &p))) return st;
+    Args a = make_args(logits, rows, vocab, stride, labels);
+    a.scale = static_cast<float>(scale);
+    a.grad = grad;
+    a.loss = loss_rows;
+    a.top = top;
+    return cuda_status(launch_fused(p, kOpGrad, a, stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -399,31 +412,18 @@ int ce_loss(const float *logits, int64_t rows, int64_t vocab, int64_t stride, co
 }
 
 int ce_grad(const float *logits, int64_t rows, int64_t vocab, int64_t stride, const int64_t *labels,
-            double scale, float *grad, float *loss_rows, float *top, ce_stream_t stream) {
-    int st = check_logits(logits, rows, vocab, stride);
-    if (st) return st;
-    if (!std::isfinite(scale)) return CE_EINVAL;
-    if (rows > 0 && (labels == nullptr || grad == nullptr)) return CE_EINVAL;
-    if (misaligned(labels, 8) || misaligned(grad, 4) || misaligned(loss_rows, 4) || misaligned(top, 4))
-        return CE_EALIGN;
-    if (rows == 0) return CE_OK;
-    const int64_t in_bytes = ((rows - 1) * stride + vocab) * 4;
-    const int64_t out_bytes = rows * vocab * 4;
-    if (grad == logits) {
-        if (stride != vocab) return CE_EINVAL;  // in place needs the same layout
-    } else if (ranges_overlap(grad, out_bytes, logits, in_bytes)) {
-        return CE_EINVAL;
-    }
-    DeviceInfo dev;
-    if ((st = current_device(&dev))) return st;
-    Plan p;
-    if ((st = make_plan(kOpGrad, rows, vocab, dev, &p))) return st;
-    Args a = make_args(logits, rows, vocab, stride, labels);
-    a.scale = static_cast<float>(scale);
-    a.grad = grad;
-    a.loss = loss_rows;
-    a.top = top;
-    return cuda_status(launch_fused(p, kOpGrad, a, stream));
+            double scale, float *grad, float *loss_rows, ce_stream_t stream) {
+    return grad_rows(logits, rows, vocab, stride, labels, scale, grad, loss_rows, nullptr, stream);
+}
+
+int ce_grad_step(const float *logits, int64_t rows, int64_t vocab, int64_t stride, const int64_t *labels,
+                 double scale, float *grad, float *loss_rows, float *top, double *loss_mean, ce_stream_t stream) {
+    // the mean reads the row losses: asking for it needs somewhere to put them
+    if (loss_mean != nullptr && rows > 0 && loss_rows == nullptr) return CE_EINVAL;
+    if (misaligned(loss_mean, 8)) return CE_EALIGN;
+    int st = grad_rows(logits, rows, vocab, stride, labels, scale, grad, loss_rows, top, stream);
+    if (st || loss_mean == nullptr) return st;
+    return ce_mean(loss_rows, rows, loss_mean, stream);
 }
 
 // softmax_rows and log_softmax_rows: the fused kernels without labels.
@@ -512,7 +512,6 @@ int argmax_rows_indirect(const uint64_t *row_addrs, int64_t rows, int64_t vocab,
     if ((st = current_device(&dev))) return st;
     Plan p;
     if ((st = make_plan(kOpArgmax, rows, vocab, dev, &p))) return st;
-    if (p.path == kPathFlat) return CE_EINVAL;  // forced even split: needs strided rows
     Args a = make_args(nullptr, rows, vocab, vocab, nullptr);
     a.row_at = row_addrs;
     a.top = top;
@@ -595,22 +594,11 @@ int ce_grad_from_stats(const float *logits, int64_t rows, int64_t vocab, int64_t
     return cuda_status(launch_grad_from_stats(a, combined, dev.sms, stream));
 }
 
-int64_t argmax_workspace_bytes(int64_t rows, int64_t vocab, int64_t stride) {
-    if (rows < 1 || vocab < 1 || vocab > kMaxVocab || stride < vocab) return 0;
-    DeviceInfo dev;
-    if (current_device(&dev)) return 0;
-    Plan p;
-    if (make_plan(kOpArgmax, rows, vocab, dev, &p) || p.path != kPathFlat) return 0;
-    return flat_workspace_bytes(rows, dev);
-}
-
-int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top, void *workspace,
-                int64_t workspace_bytes, ce_stream_t stream) {
+int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride, float *top, ce_stream_t stream) {
     int st = check_logits(logits, rows, vocab, stride);
     if (st) return st;
     if (rows > 0 && top == nullptr) return CE_EINVAL;
-    if (workspace_bytes < 0 || (workspace_bytes > 0 && workspace == nullptr)) return CE_EINVAL;
-    if (misaligned(top, 4) || misaligned(workspace, 8)) return CE_EALIGN;
+    if (misaligned(top, 4)) return CE_EALIGN;
     if (rows == 0) return CE_OK;
     DeviceInfo dev;
     if ((st = current_device(&dev))) return st;
@@ -618,17 +606,6 @@ int argmax_rows(const float *logits, int64_t rows, int64_t vocab, int64_t stride
     if ((st = make_plan(kOpArgmax, rows, vocab, dev, &p))) return st;
     Args a = make_args(logits, rows, vocab, stride, nullptr);
     a.top = top;
-    if (p.path == kPathFlat) {
-        if (workspace != nullptr && workspace_bytes >= flat_workspace_bytes(rows, dev))
-            return cuda_status(launch_argmax_flat(a, static_cast<int>(p.clusters), workspace, stream));
-        Force f;
-        {
-            std::lock_guard<std::mutex> lock(g_mu);
-            f = g_force;
-        }
-        if (f.path == kPathFlat) return CE_EINVAL;  // forced, but no room for it
-        plan_stream(p, kOpArgmax, rows, vocab, dev, 0, 0);
-    }
     return cuda_status(launch_rows_stream(p, a, false, stream));
 }
 
@@ -726,8 +703,8 @@ int ce_grad_host(const float *logits_h, int64_t rows, int64_t vocab, int64_t str
         for (int64_t c = 0; c < n; ++c) {
             const int64_t r0 = c * chunk, r1 = std::min(rows, r0 + chunk);
             if ((e = cudaStreamWaitEvent(stream, h.chunk[c], 0)) != cudaSuccess) return cuda_status(e);
-            st = ce_grad(logits_d + r0 * vocab, r1 - r0, vocab, vocab, labels_d + r0, scale, grad + r0 * vocab,
-                         loss_rows + r0, top ? top + r0 : nullptr, stream);
+            st = grad_rows(logits_d + r0 * vocab, r1 - r0, vocab, vocab, labels_d + r0, scale, grad + r0 * vocab,
+                           loss_rows + r0, top ? top + r0 : nullptr, stream);
             if (st) return st;
         }
     }
@@ -745,17 +722,21 @@ int ce_version(void) { return kVersion; }
 
 int ce_last_cuda_error(void) { return t_last_cuda_error; }
 
-int ce_device_error_count(ce_stream_t stream, uint64_t counts[2]) {
-    if (counts == nullptr) return CE_EINVAL;
+// Reads device counter `which` (0 bad labels, 1 waits that gave up); waits for `stream`.
+static int read_counter(ce_stream_t stream, int which, int64_t *out) {
+    if (out == nullptr) return CE_EINVAL;
     DeviceInfo dev;
     int st = current_device(&dev);
     if (st) return st;
     unsigned long long v[2] = {0ull, 0ull};
     if ((st = cuda_status(read_status(v, stream)))) return st;
-    counts[0] = v[0];
-    counts[1] = v[1];
+    *out = static_cast<int64_t>(v[which]);
     return CE_OK;
 }
+
+int ce_device_error_count(ce_stream_t stream, int64_t *out) { return read_counter(stream, 0, out); }
+
+int ce_device_wait_timeouts(ce_stream_t stream, int64_t *out) { return read_counter(stream, 1, out); }
 
 int ce_device_error_reset(ce_stream_t stream) {
     DeviceInfo dev;

@@ -132,6 +132,19 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+// An arrive that releases this thread's earlier writes (shared memory of
+// peers included) to the threads that pass the matching cluster_wait.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// Programmatic dependent launch. launch_dependents: the next kernel on the
+// stream, if launched with programmatic stream serialization, may be
+// scheduled once every CTA of this grid has called it (or exited).
+// wait_prerequisites: block until the grids this one depends on have
+// completed and their memory is visible; a no-op without such a dependency.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // address of the same shared variable in CTA `rank` of the cluster
 __device__ __forceinline__ uint32_t peer_smem(const void *p, uint32_t rank) {
     uint32_t r;
@@ -145,6 +158,12 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
                  : "r"(addr)
                  : "memory");
     return v;
+}
+
+// 8-byte store into the shared memory of a CTA of the cluster (a
+// shared::cluster address from peer_smem).
+__device__ __forceinline__ void st_dsmem_f64(uint32_t addr, double v) {
+    asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(addr), "d"(v) : "memory");
 }
 
 // 16-byte store into the shared memory of a CTA of the cluster (a
@@ -271,8 +290,9 @@ __device__ __forceinline__ float4 sub2_4(float4 v, float m, float l) {
 // running max m (and m is above -inf), so each adds exp(x - m) -- a tie adds
 // exactly 1 and keeps the first index, a NaN makes t NaN. Otherwise (a new
 // max, or no finite value yet, or all four NaN) the exact scalar update runs.
-// exp is CUDA's __expf intrinsic (documented error 2 + 1.2|x| ulp, so below
-// 1.3e-7 absolute on any exp(x - m) <= 1).
+// The common case takes exp_le0 (ex2.approx of d * log2(e), above: below
+// about 2.5e-7 relative and 2.2e-8 absolute for the rounding of the
+// product); the exact update calls CUDA's expf.
 template <bool kStats>
 __device__ __forceinline__ void push_vec(RowState &s, float4 v, int j) {
     const float mv = max4(v);

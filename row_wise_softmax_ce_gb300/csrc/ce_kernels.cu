@@ -31,7 +31,9 @@
 //                   bulk-copied into a shared-memory ring.
 //   k_split_sum     split sums in one resident wave.
 //   k_stats_combine / k_grad_from_stats  the vocab-sharded loss and gradient.
-//   k_mean          the mean of the row losses, an f64 fixed-shape tree.
+//   k_mean          the mean of the row losses, an f64 fixed-shape tree over a
+//                   cluster, launched as a programmatic dependent of the row
+//                   kernel that wrote them.
 //
 // The row kernels loop over rows (row = cluster id, + number of clusters), so
 // any row count fits one launch.
@@ -192,6 +194,7 @@ template <bool kStats>
 __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, int cols) {
     __shared__ RowState red[32];
     __shared__ PushXchg xg;
+    launch_dependents();  // a mean of the row losses may be scheduled now; it waits for this grid's end
     const uint32_t rank = cluster_rank(), C = cluster_size();
     const int tid = threadIdx.x;
     const int c0 = static_cast<int>(rank) * cols;
@@ -250,6 +253,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
 // and ending.
 template <bool kStats>
 __global__ void __launch_bounds__(256) k_rows_warp(Args a) {
+    launch_dependents();  // a mean of the row losses may be scheduled now; it waits for this grid's end
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t row = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; row < a.rows;
@@ -312,6 +316,7 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
     constexpr bool kCE = kMode == kModeGrad;
     constexpr bool kLog = kMode == kModeLogSoftmax;
     extern __shared__ __align__(128) unsigned char smem[];
+    launch_dependents();  // a mean of the row losses may be scheduled now; it waits for this grid's end
     StagedHeader &h = *reinterpret_cast<StagedHeader *>(smem);
     float *buf = reinterpret_cast<float *>(smem + kStagedHeaderBytes);
     float4 *buf4 = reinterpret_cast<float4 *>(buf);
@@ -508,6 +513,7 @@ template <int kMode>
 __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, int cols) {
     constexpr bool kCE = kMode == kModeGrad;
     constexpr bool kLog = kMode == kModeLogSoftmax;
+    launch_dependents();  // a mean of the row losses may be scheduled now; it waits for this grid's end
     __shared__ RowState red[32];
     __shared__ PushXchg xg;
     __shared__ float bc[2];
@@ -1231,20 +1237,43 @@ __global__ void __launch_bounds__(256) k_grad_from_stats(Args a, const float4 *_
 }
 
 // ---------------------------------------------------------------------------
-// k_mean: one CTA. Thread k sums rows k, k + T, ... in f64; a butterfly over
-// each warp, then over the warps' sums. Fixed shape: same bits every run.
-__global__ void __launch_bounds__(1024) k_mean(const float *__restrict__ loss, int64_t rows,
-                                               double *__restrict__ out) {
-    __shared__ double part[32];
+// k_mean: one cluster of kMeanCtas CTAs, launched as a programmatic dependent
+// of the row kernel before it on the stream (so it is already resident when
+// that kernel ends). Thread g of the cluster's kMeanCtas * kMeanThreads sums
+// rows g, g + kMeanCtas * kMeanThreads, ... in f64; a butterfly over each
+// warp, then over the CTA's warps; the CTAs' sums meet in CTA 0's shared
+// memory (distributed shared memory) and are added by a butterfly in rank
+// order. The shape does not depend on the device: the same bits every run.
+constexpr int kMeanCtas = 8;
+constexpr int kMeanThreads = 512;
+
+__global__ void __launch_bounds__(kMeanThreads) k_mean(const float *__restrict__ loss, int64_t rows,
+                                                       double *__restrict__ out) {
+    __shared__ double warp_sum[kMeanThreads / 32];
+    __shared__ double cta_sum[kMeanCtas];
+    cluster_arrive();      // every CTA has started before CTA 0's shared memory is written
+    wait_prerequisites();  // the row losses are complete and visible
+    const uint32_t rank = cluster_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int64_t kAll = static_cast<int64_t>(kMeanCtas) * kMeanThreads;
     double s = 0.0;
-    for (int64_t i = threadIdx.x; i < rows; i += blockDim.x) s += static_cast<double>(loss[i]);
+    for (int64_t i = static_cast<int64_t>(rank) * kMeanThreads + tid; i < rows; i += kAll)
+        s += static_cast<double>(loss[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFullMask, s, o);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    if (lane == 0) part[warp] = s;
+    if (lane == 0) warp_sum[warp] = s;
     __syncthreads();
+    cluster_wait();
     if (warp == 0) {
-        double r = lane < nwarps ? part[lane] : 0.0;
+        double r = lane < kMeanThreads / 32 ? warp_sum[lane] : 0.0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(kFullMask, r, o);
+        if (lane == 0) st_dsmem_f64(peer_smem(&cta_sum[rank], 0), r);
+    }
+    cluster_arrive_release();
+    cluster_wait();
+    if (rank == 0 && warp == 0) {
+        double r = lane < kMeanCtas ? cta_sum[lane] : 0.0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) r += __shfl_xor_sync(kFullMask, r, o);
         if (lane == 0) *out = r / static_cast<double>(rows);
@@ -1416,8 +1445,20 @@ cudaError_t launch_grad_from_stats(const Args &a, const float *combined, int sms
 }
 
 cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream_t s) {
-    k_mean<<<1, 1024, 0, s>>>(loss, rows, out);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMeanCtas, 1, 1);
+    cfg.blockDim = dim3(kMeanThreads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kMeanCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_mean, loss, rows, out);
 }
 
 cudaError_t read_status(unsigned long long out[2], cudaStream_t s) {

@@ -26,11 +26,17 @@ int main(void)
     expect(strlen(ce_status_string(CE_EINVAL)) > 0, "status text");
     /* argument checks run on the host before any device is touched */
     expect(ce_rows(NULL, 4, 10, 10, NULL, NULL, NULL) == CE_EINVAL, "ce_rows: null logits");
-    expect(ce_grad((const float *)256, 4, 10, 9, (const int64_t *)512, 1.0, (float *)4096, NULL, NULL, NULL) ==
-               CE_EINVAL,
+    expect(ce_grad((const float *)256, 4, 10, 9, (const int64_t *)512, 1.0, (float *)4096, NULL, NULL) == CE_EINVAL,
            "ce_grad: stride < vocab");
-    expect(argmax_rows((const float *)258, 4, 10, 10, (float *)1024, NULL, 0, NULL) == CE_EALIGN,
+    expect(ce_loss((const float *)256, 4, 10, 10, (const int64_t *)512, (float *)1024, NULL, NULL) == CE_EINVAL,
+           "ce_loss: no mean");
+    expect(ce_grad_step((const float *)256, 4, 10, 10, (const int64_t *)512, 1.0, (float *)4096, NULL, NULL,
+                        (double *)8192, NULL) == CE_EINVAL,
+           "ce_grad_step: a mean without row losses");
+    expect(argmax_rows((const float *)258, 4, 10, 10, (float *)1024, NULL) == CE_EALIGN,
            "argmax_rows: misaligned logits");
+    expect(ce_device_error_count(NULL, NULL) == CE_EINVAL, "ce_device_error_count: no output");
+    expect(ce_device_wait_timeouts(NULL, NULL) == CE_EINVAL, "ce_device_wait_timeouts: no output");
     expect(split_sum((float *)256, (const float *)4096, 10, 0, 0, NULL) == CE_EINVAL, "split_sum: no parts");
     expect(candidates_rows((const float *)256, 4, 0, 10, (float *)8192, NULL) == CE_EINVAL,
            "candidates_rows: vocab < 1");
@@ -38,6 +44,8 @@ int main(void)
     /* zero rows: nothing to do, nothing launched */
     expect(ce_rows(NULL, 0, 10, 10, NULL, NULL, NULL) == CE_OK, "ce_rows: zero rows");
     expect(softmax_rows(NULL, 0, 10, 10, NULL, NULL) == CE_OK, "softmax_rows: zero rows");
+    expect(argmax_rows(NULL, 0, 10, 10, NULL, NULL) == CE_OK, "argmax_rows: zero rows");
+    expect(ce_grad(NULL, 0, 10, 10, NULL, 1.0, NULL, NULL, NULL) == CE_OK, "ce_grad: zero rows");
     expect(ce_debug_force(0, 0, 0) == CE_OK, "debug_force reset");
     expect(ce_debug_force(7, 2, 0) == CE_OK && ce_debug_force(0, 0, 0) == CE_OK, "debug_force: the ring path");
     expect(ce_debug_grid_cap(-1) == CE_EINVAL, "grid cap: negative");

@@ -3,12 +3,15 @@
 Tolerances (element by element, CUDA path vs the f64 CPU oracle):
   per-row loss   relative 2e-5 (absolute 2^-126 below the f32 normal range,
                  where f32 has no relative precision left)
-  mean loss      relative 1e-6, plus, for each row whose loss is below 1e-4,
-                 that row's own 2e-5 allowance weighted by its share of the
-                 mean: such a loss is a sum of exponentials of logits far below
-                 a labelled max, each carrying up to |x - m| 2^-23 relative
-                 error from f32 arguments, and the mean of few such rows
-                 cannot be better than the rows themselves
+  mean loss      relative 1e-6. Every workload and every fixed case meets it
+                 as it stands. One documented deviation, used by the seeded
+                 random soak alone (its drawn rows may be nothing but tiny
+                 losses): assert_mean(..., tiny_loss_rows=l) adds, for each
+                 row whose loss is below 1e-4, that row's own 2e-5 allowance
+                 weighted by its share of the mean. Such a loss is a sum of
+                 exponentials of logits far below a labelled max, each carrying
+                 up to |x - m| 2^-23 relative error from f32 arguments, and the
+                 mean of few such rows cannot be better than the rows themselves
   gradient       absolute 1e-6
   argmax token   exact
   softmax row    absolute 1e-6 (the gradient's: the same kernel and arithmetic)
@@ -63,9 +66,10 @@ def assert_loss(got, ref, what="loss"):
 TINY_LOSS = 1e-4
 
 
-def assert_mean(got, ref, what="mean", loss_rows=None):
-    """The mean loss; ``loss_rows`` (the oracle's row losses) adds the allowance
-    of rows below TINY_LOSS (see the module docstring)."""
+def assert_mean(got, ref, what="mean", tiny_loss_rows=None):
+    """The mean loss within 1e-6 relative. ``tiny_loss_rows`` (the oracle's
+    row losses) adds the allowance of rows below TINY_LOSS -- the documented
+    deviation of the random soak only (see the module docstring)."""
     got, ref = float(got), float(ref)
     if np.isnan(ref):
         assert np.isnan(got), f"{what}: {got} != NaN"
@@ -74,8 +78,8 @@ def assert_mean(got, ref, what="mean", loss_rows=None):
         assert got == ref, f"{what}: {got!r} vs {ref!r}"
         return
     tol = MEAN_REL * abs(ref)
-    if loss_rows is not None:
-        l = np.abs(np.asarray(loss_rows, dtype=np.float64))
+    if tiny_loss_rows is not None:
+        l = np.abs(np.asarray(tiny_loss_rows, dtype=np.float64))
         if l.size:
             tol += LOSS_REL * l[l < TINY_LOSS].sum() / l.size
     assert abs(got - ref) <= tol, f"{what}: {got!r} vs {ref!r} (tolerance {tol:.3e})"

@@ -17,9 +17,9 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = ce.declared_functions()
-    assert set(names) >= {"ce_rows", "ce_mean", "ce_loss", "ce_grad", "argmax_rows", "argmax_workspace_bytes",
+    assert set(names) >= {"ce_rows", "ce_mean", "ce_loss", "ce_grad", "ce_grad_step", "argmax_rows",
                           "ce_status_string",
-                          "ce_version", "ce_last_cuda_error", "ce_device_error_count",
+                          "ce_version", "ce_last_cuda_error", "ce_device_error_count", "ce_device_wait_timeouts",
                           "ce_device_error_reset", "ce_debug_force", "ce_debug_grid_cap", "ce_plan", "softmax_rows",
                           "log_softmax_rows", "candidates_rows", "split_sum", "argmax_rows_noalloc",
                           "argmax_rows_indirect", "candidates_rows_indirect"}
@@ -53,8 +53,10 @@ V = ctypes.c_void_p
 def test_bad_sizes_rejected_before_launch(lib, args):
     logits, rows, vocab, stride = args
     assert lib.ce_rows(logits, rows, vocab, stride, V(512), V(1024), None) == ce.CE_EINVAL
-    assert lib.argmax_rows(logits, rows, vocab, stride, V(1024), None, 0, None) == ce.CE_EINVAL
-    assert lib.ce_grad(logits, rows, vocab, stride, V(512), 1.0, V(4096), None, None, None) == ce.CE_EINVAL
+    assert lib.argmax_rows(logits, rows, vocab, stride, V(1024), None) == ce.CE_EINVAL
+    assert lib.ce_grad(logits, rows, vocab, stride, V(512), 1.0, V(4096), None, None) == ce.CE_EINVAL
+    assert lib.ce_grad_step(logits, rows, vocab, stride, V(512), 1.0, V(4096), V(1 << 20), None, V(1 << 21),
+                            None) == ce.CE_EINVAL
     for fn in (lib.softmax_rows, lib.log_softmax_rows, lib.candidates_rows):
         assert fn(logits, rows, vocab, stride, V(1 << 20), None) == ce.CE_EINVAL
 
@@ -62,28 +64,36 @@ def test_bad_sizes_rejected_before_launch(lib, args):
 def test_misaligned_pointers_rejected(lib):
     assert lib.ce_rows(V(258), 4, 10, 10, V(512), V(1024), None) == ce.CE_EALIGN
     assert lib.ce_rows(V(256), 4, 10, 10, V(516), V(1024), None) == ce.CE_EALIGN     # labels need 8 B
-    assert lib.argmax_rows(V(256), 4, 10, 10, V(1026), None, 0, None) == ce.CE_EALIGN
-    assert lib.argmax_rows(V(256), 4, 10, 10, V(1024), V(2052), 64, None) == ce.CE_EALIGN   # workspace 8 B
+    assert lib.argmax_rows(V(256), 4, 10, 10, V(1026), None) == ce.CE_EALIGN
+    assert lib.ce_grad_step(V(256), 4, 10, 10, V(512), 1.0, V(4096), V(1 << 20), V((1 << 21) + 2), None,
+                            None) == ce.CE_EALIGN                                     # tokens 4 B
+    assert lib.ce_grad_step(V(256), 4, 10, 10, V(512), 1.0, V(4096), V(1 << 20), None, V((1 << 21) + 4),
+                            None) == ce.CE_EALIGN                                     # double mean
     assert lib.ce_mean(V(256), 4, V(260), None) == ce.CE_EALIGN                       # double out
 
 
 def test_null_outputs_and_bad_scale_rejected(lib):
     assert lib.ce_rows(V(256), 4, 10, 10, None, V(1024), None) == ce.CE_EINVAL
     assert lib.ce_rows(V(256), 4, 10, 10, V(512), None, None) == ce.CE_EINVAL
-    assert lib.argmax_rows(V(256), 4, 10, 10, None, None, 0, None) == ce.CE_EINVAL
-    assert lib.argmax_rows(V(256), 4, 10, 10, V(1024), None, 64, None) == ce.CE_EINVAL    # bytes, no buffer
-    assert lib.argmax_rows(V(256), 4, 10, 10, V(1024), V(2048), -8, None) == ce.CE_EINVAL
+    assert lib.argmax_rows(V(256), 4, 10, 10, None, None) == ce.CE_EINVAL
     assert lib.ce_mean(V(256), 4, None, None) == ce.CE_EINVAL
     assert lib.ce_loss(V(256), 4, 10, 10, V(512), V(1024), None, None) == ce.CE_EINVAL
     for s in (float("nan"), float("inf")):
-        assert lib.ce_grad(V(256), 4, 10, 10, V(512), s, V(4096), None, None, None) == ce.CE_EINVAL
-    assert lib.ce_grad(V(256), 4, 10, 10, V(512), 1.0, None, None, None, None) == ce.CE_EINVAL
+        assert lib.ce_grad(V(256), 4, 10, 10, V(512), s, V(4096), None, None) == ce.CE_EINVAL
+        assert lib.ce_grad_step(V(256), 4, 10, 10, V(512), s, V(4096), None, None, None, None) == ce.CE_EINVAL
+    assert lib.ce_grad(V(256), 4, 10, 10, V(512), 1.0, None, None, None) == ce.CE_EINVAL
+    # the step's mean reads the row losses: a mean without them is refused
+    assert lib.ce_grad_step(V(256), 4, 10, 10, V(512), 1.0, V(4096), None, None, V(1 << 21), None) == ce.CE_EINVAL
+    # the debug counters need somewhere to write
+    assert lib.ce_device_error_count(None, None) == ce.CE_EINVAL
+    assert lib.ce_device_wait_timeouts(None, None) == ce.CE_EINVAL
 
 
 def test_grad_overlap_rules(lib):
     # in place needs stride == vocab; a partial overlap is rejected
-    assert lib.ce_grad(V(4096), 4, 10, 12, V(512), 1.0, V(4096), None, None, None) == ce.CE_EINVAL
-    assert lib.ce_grad(V(4096), 4, 10, 10, V(512), 1.0, V(4100), None, None, None) == ce.CE_EINVAL
+    assert lib.ce_grad(V(4096), 4, 10, 12, V(512), 1.0, V(4096), None, None) == ce.CE_EINVAL
+    assert lib.ce_grad(V(4096), 4, 10, 10, V(512), 1.0, V(4100), None, None) == ce.CE_EINVAL
+    assert lib.ce_grad_step(V(4096), 4, 10, 10, V(512), 1.0, V(4100), None, None, None, None) == ce.CE_EINVAL
 
 
 def test_rows_beside_the_loss_validation(lib):
@@ -147,9 +157,9 @@ def test_indirect_validation(lib):
 def test_zero_rows_is_a_no_op_without_device(lib):
     # nothing is launched, so no device is needed
     assert lib.ce_rows(None, 0, 10, 10, None, None, None) == ce.CE_OK
-    assert lib.argmax_rows(None, 0, 10, 10, None, None, 0, None) == ce.CE_OK
-    assert lib.argmax_workspace_bytes(0, 10, 10) == 0
-    assert lib.ce_grad(None, 0, 10, 10, None, 1.0, None, None, None, None) == ce.CE_OK
+    assert lib.argmax_rows(None, 0, 10, 10, None, None) == ce.CE_OK
+    assert lib.ce_grad(None, 0, 10, 10, None, 1.0, None, None, None) == ce.CE_OK
+    assert lib.ce_grad_step(None, 0, 10, 10, None, 1.0, None, None, None, None, None) == ce.CE_OK
 
 
 def test_debug_force_validation(lib):

@@ -131,10 +131,11 @@ def test_random_case(orc, seed):
     assert_loss(lr2, l_ref, f"{what}: ce_rows")
     assert_tokens(top2, a_ref, f"{what}: argmax_rows")
     assert_tokens(top3, a_ref, f"{what}: argmax_rows (ring)")
-    assert_mean(mean.item(), orc.ce_mean(l_ref), f"{what}: ce_mean", loss_rows=l_ref)
+    # the documented tiny-loss deviation: drawn rows may hold nothing but tiny losses
+    assert_mean(mean.item(), orc.ce_mean(l_ref), f"{what}: ce_mean", tiny_loss_rows=l_ref)
     assert_softmax(soft, orc.softmax(x, vocab, threads=THREADS), f"{what}: softmax_rows")
     assert_log_softmax(logp, orc.log_softmax(x, vocab, threads=THREADS), f"{what}: log_softmax_rows")
     assert_candidates(cand, orc.candidates(x, vocab, threads=THREADS), f"{what}: candidates_rows")
     assert_grad(hs.grad, g_ref, f"{what}: ce_grad_host grad")
     assert_tokens(hs.top_h, a_ref, f"{what}: ce_grad_host tokens")
-    assert_mean(hs.mean_h.item(), orc.ce_mean(l_ref), f"{what}: ce_grad_host mean", loss_rows=l_ref)
+    assert_mean(hs.mean_h.item(), orc.ce_mean(l_ref), f"{what}: ce_grad_host mean", tiny_loss_rows=l_ref)
