@@ -14,8 +14,8 @@ Printed (one JSON line, rank 0):
               around each launch, right after the steps
   argmax      rows/s of argmax_rows on the decode workload (256 x 151936,
               row stride 152064), L2 flushed before every timed launch, with
-              a plain read of the same buffer beside it (torch.sum, same run,
-              same flush) as the ceiling of a read of that size
+              a plain read of the same buffer beside it (the library's read
+              probe, same run, same flush) as the ceiling of a read of that size
   candidates  rows/s of candidates_rows on the same decode batch, likewise
   e2e         the same metric through ce_grad_host: the inputs copied from
               pinned host memory (in chunks, overlapped with the kernels) and
@@ -431,21 +431,27 @@ def run_ours(args):
     torch.cuda.synchronize()
     arg_all = [a.elapsed_time(c) for a, c in times]
     arg_ms = max_over_ranks(statistics.median(arg_all), ws)
-    # the ceiling of a read of this size on this machine, same run, same flush: a
-    # plain reduction over the same buffer (its padding included, +0.08%)
-    for _ in range(3):
-        torch.sum(bd.logits)
-    times = []
-    for _ in range(n_arg):
-        l2_flush(flush)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        torch.sum(bd.logits)
-        e1.record(stream)
-        times.append((e0, e1))
-    torch.cuda.synchronize()
-    read_all = [a.elapsed_time(c) for a, c in times]
+    # the ceiling of a read of this size on this machine, same run, same flush: the
+    # library's read probe over the same buffer (its padding included, +0.08%),
+    # and torch.sum of it beside
+    def timed_reads(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(n_arg):
+            l2_flush(flush)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(c) for a, c in ts]
+
+    probe_out = torch.zeros((), dtype=torch.int32, device=dev)
+    read_all = timed_reads(lambda: ce.debug_read(bd.logits, out=probe_out))
     read_ms = statistics.median(read_all)
+    sum_all = timed_reads(lambda: torch.sum(bd.logits))
     read_bytes = bd.logits.numel() * 4
     # sampling candidates (candidatesInto) of the same decode batch, L2 flushed too
     cand = torch.empty((wd.rows, ce.CANDIDATE_ROW), dtype=torch.float32, device=dev)
@@ -546,11 +552,13 @@ def run_ours(args):
                        "GB/s": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9, 1),
                        "frac": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9 / peak, 4),
                        "l2": "flushed before each launch",
-                       "plain_read": {"what": "torch.sum of the same padded buffer, same flush",
+                       "plain_read": {"what": "ce_debug_read (16-byte loads, 8 in flight per thread, one "
+                                              "resident wave) of the same padded buffer, same flush",
                                       "bytes": read_bytes, "ms": round(read_ms, 5),
                                       "ms_min": round(min(read_all), 5),
                                       "GB/s": round(read_bytes / (read_ms * 1e-3) / 1e9, 1),
-                                      "argmax_over_read": round(arg_ms / read_ms, 4)}},
+                                      "argmax_over_read": round(arg_ms / read_ms, 4),
+                                      "torch_sum_ms": round(statistics.median(sum_all), 5)}},
             "candidates": {"workload": wd.name, "rows_per_s": round(ws * wd.rows / (cand_ms * 1e-3), 1),
                            "ms": round(cand_ms, 5), "ms_min": round(min(cand_all), 5),
                            "GB/s": round(cand_bytes / (cand_ms * 1e-3) / 1e9, 1),

@@ -396,6 +396,16 @@ CE_API int ce_debug_force(int path, int cluster, int threads);
 CE_API int ce_debug_grid_cap(int64_t clusters);
 
 /*
+ * Read probe, for measurement: reads `bytes` bytes at device address p (16-byte
+ * aligned, bytes a multiple of 16) once, sixteen bytes per load with eight
+ * loads in flight per thread over one resident wave of CTAs, and XORs every
+ * word read into *out (4 bytes on the device, not cleared first). No page
+ * defines it: it gives the ceiling of a plain read of a buffer of that size
+ * on this device, to time beside a row kernel that reads the same bytes.
+ */
+CE_API int ce_debug_read(const void *p, int64_t bytes, uint32_t *out, ce_stream_t stream);
+
+/*
  * The plan the library would pick (host only, launches nothing) for
  * op (0 ce_rows, 1 ce_grad, 2 argmax_rows, 3 softmax_rows, 4
  * log_softmax_rows, 5 candidates_rows) on the current device:

@@ -98,6 +98,7 @@ def _bind(lib):
         "ce_debug_grid_cap": [i64],
         "ce_grad_host": [vp, i64, i64, i64, vp, ctypes.c_double, vp, vp, vp, vp, vp, vp, vp, vp, i64, vp],
         "ce_plan": [i32, i64, i64, i64, ctypes.POINTER(ctypes.c_int64)],
+        "ce_debug_read": [vp, i64, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -542,6 +543,21 @@ def debug_force(path: int = 0, cluster: int = 0, threads: int = 0) -> None:
 def debug_grid_cap(clusters: int = 0) -> None:
     """Cap the grid of later row-kernel launches at `clusters` clusters (0 = no cap); see ce_debug_grid_cap."""
     _check("ce_debug_grid_cap", lib().ce_debug_grid_cap(clusters))
+
+
+def debug_read(t: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Read probe (ce_debug_read): one plain read of the whole of the
+    contiguous CUDA tensor ``t``, its words XORed into ``out`` (a uint32-sized
+    int32 tensor on the device, zeroed when allocated here)."""
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("t must be a contiguous CUDA tensor")
+    nbytes = t.numel() * t.element_size()
+    dev = t.device
+    if out is None:
+        out = torch.zeros((), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check("ce_debug_read", lib().ce_debug_read(t.data_ptr(), nbytes, out.data_ptr(), _stream(dev)))
+    return out
 
 
 def plan(op: int, rows: int, vocab: int, stride: int | None = None) -> dict:

@@ -139,14 +139,13 @@ bool plan_warp(Plan &p, Op op, int64_t rows) {
 // Launch shape of the staged fused kernel: the fewest CTAs per row whose
 // slices are at most kStagedTargetCols columns (at most 16 CTAs).
 // The staged kernel's geometry for `c` CTAs per row: columns per CTA and the
-// shared memory that covers any row misalignment (4 * kChunks * W floats);
+// shared memory that covers any row misalignment ((cols + 9) / 4 vectors);
 // false when it does not fit. *active: the clusters resident at once.
 bool staged_shape(Plan &p, Op op, int64_t vocab, const DeviceInfo &dev, int64_t c, int *active) {
     if (c > kMaxCluster) c = kMaxCluster;
     p.cluster = static_cast<int>(c);
     p.cols = round_up4(ceil_div(vocab, c));
-    const int w = ((p.cols + 9) / 4 + 3) / 4;
-    p.smem = kStagedHeaderBytes + 16 * 4 * w;
+    p.smem = kStagedHeaderBytes + 16 * ((p.cols + 9) / 4);
     if (p.smem > dev.max_smem_optin) return false;
     *active = 0;
     if (max_active_clusters(p, op, active) != cudaSuccess) {
@@ -160,7 +159,8 @@ bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &
                  bool per_row, bool auto_form) {
     p.path = kPathStaged;
     p.threads = threads ? threads : 256;
-    if (p.threads > kStagedMaxThreads) return false;
+    // the kernel maps vectors to threads modulo T: 128 or 256
+    if (p.threads > kStagedMaxThreads || (p.threads & (p.threads - 1)) != 0) return false;
     int active = 0;
     const int64_t c = cluster ? cluster : std::max<int64_t>(1, ceil_div(vocab, kStagedTargetCols));
     if (!staged_shape(p, op, vocab, dev, c, &active)) return false;
@@ -760,6 +760,16 @@ int ce_debug_grid_cap(int64_t clusters) {
     std::lock_guard<std::mutex> lock(g_mu);
     g_force.grid_cap = clusters;
     return CE_OK;
+}
+
+int ce_debug_read(const void *p, int64_t bytes, uint32_t *out, ce_stream_t stream) {
+    if (bytes < 0 || out == nullptr || (bytes > 0 && p == nullptr)) return CE_EINVAL;
+    if (bytes % 16 != 0) return CE_EINVAL;
+    if (misaligned(p, 16) || misaligned(out, 4)) return CE_EALIGN;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st) return st;
+    return cuda_status(launch_read_probe(p, bytes, out, dev.sms, stream));
 }
 
 int ce_plan(int op, int64_t rows, int64_t vocab, int64_t stride, int64_t out[6]) {

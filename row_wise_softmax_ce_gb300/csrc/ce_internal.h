@@ -105,6 +105,9 @@ cudaError_t launch_grad_from_stats(const Args &a, const float *combined, int sms
 // argmax of few long rows split evenly over `ctas` CTAs; ws: 8 * (ctas + rows) bytes
 cudaError_t launch_argmax_flat(const Args &a, int ctas, void *ws, cudaStream_t s);
 
+// a plain read of `bytes` (a multiple of 16, 16-byte aligned) in one resident wave
+cudaError_t launch_read_probe(const void *p, int64_t bytes, uint32_t *out, int sms, cudaStream_t s);
+
 cudaError_t read_status(unsigned long long out[2], cudaStream_t s);
 cudaError_t reset_status(cudaStream_t s);
 

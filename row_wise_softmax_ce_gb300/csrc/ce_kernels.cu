@@ -31,6 +31,7 @@
 //                   bulk-copied into a shared-memory ring.
 //   k_split_sum     split sums in one resident wave.
 //   k_stats_combine / k_grad_from_stats  the vocab-sharded loss and gradient.
+//   k_read_probe    a plain read of a buffer (measurement only).
 //   k_mean          the mean of the row losses, an f64 fixed-shape tree over a
 //                   cluster, launched as a programmatic dependent of the row
 //                   kernel that wrote them.
@@ -51,7 +52,6 @@ __device__ unsigned long long g_status[2];
 
 namespace {
 
-constexpr int kChunks = 4;  // bulk copies (and mbarriers) per staged slice
 constexpr int kUnroll = 4;      // 16-byte loads in flight per thread (streaming)
 // the same for a warp alone on its row (4096 x 32000, L2 flushed: argmax
 // 90 -> 80 us, row losses 97 -> 90 us against 4; 12 for the losses needs 76
@@ -60,7 +60,7 @@ constexpr int kWarpUnroll = 8;
 
 struct alignas(16) StagedHeader {
     PushXchg xg;  // row states pushed by the cluster's CTAs
-    uint64_t bar[kChunks];
+    uint64_t bar;  // the slice's bulk copy
     RowState red[32];
     float bc[4];
 };
@@ -203,8 +203,10 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
     const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;  // rows of this cluster
     if (tid == 0) push_xchg_init(xg, K, C);
     __syncthreads();
-    cluster_arrive();  // every CTA's slot barriers exist before a peer pushes to them
-    cluster_wait();
+    // every CTA's slot barriers exist before a peer pushes to them: the wait
+    // that matches this arrive comes just before the first push, so the
+    // barrier's latency hides under the first row's scan
+    cluster_arrive();
     bool failed = false;
     int64_t k = 0;
     for (int64_t row = cid; row < a.rows; row += G, ++k) {
@@ -221,6 +223,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
         RowState st = empty_state();
         if (n > 0 && rp) st = scan_global<kStats>(rp + c0, c0, n);
         st = block_reduce_w0<kStats>(st, red);
+        if (k == 0) cluster_wait();
         if (tid == 0) push_xchg_publish(xg, k, rank, C, st, 0.0f);
         if (tid < 32) {
             float unused;
@@ -239,6 +242,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
         }
         __syncthreads();  // red is rewritten for the next row
     }
+    if (K == 0) cluster_wait();  // the first arrive's match, for a cluster without rows
     cluster_arrive();  // no CTA leaves while a peer may still push to it
     cluster_wait();
     if (__syncthreads_or(failed) && tid == 0) atomicAdd(&g_status[1], 1ull);
@@ -284,18 +288,16 @@ __global__ void __launch_bounds__(256) k_rows_warp(Args a) {
 
 // ---------------------------------------------------------------------------
 // k_grad_staged: fused loss + gradient (+ token) from shared-memory slices,
-// persistent, with the next row's slice prefetched as this one is written.
+// persistent, each CTA's next slice copied in as soon as this one is written.
 //
 // CTA `rank` of a cluster owns columns [c0, c0 + n), c0 = rank * cols, of the
 // cluster's rows (cluster cid of G takes rows cid, cid + G, ...). A row's
 // slice sits in shared memory on the 16-byte grid of the logits: float i of
 // buf holds column c0 - off + i, off = the slice's start modulo 16 bytes (in
-// floats). The grid is cut into kChunks fixed ranges of W vectors; chunk c of
-// every row lands in range c, whatever that row's off. The aligned body of a
-// range arrives by one bulk copy (mbarrier bar[c], one phase per row); the at
-// most two partial end vectors are loaded by the threads that own them, with
-// -inf outside the slice. Thread t owns, in every pass, the vectors c*W + t +
-// T*i of each range c. Per row:
+// floats). Its aligned body arrives by one bulk copy (mbarrier bar, one phase
+// per row); the at most two partial end vectors are loaded by the threads
+// that own them, with -inf outside the slice. Thread t owns, in every pass,
+// the vectors t + T*i. Per row:
 //   sweep 1  each thread's max m over its vectors, and the first vector
 //            holding it;
 //   sweep 2  t = the sum of exp(x - m) but for the first element holding m
@@ -305,8 +307,11 @@ __global__ void __launch_bounds__(256) k_rows_warp(Args a) {
 //            merges the C states in rank order, so every CTA holds the same
 //            row state -- no cluster barrier per row;
 //   write    grad = exp(x - M) * f32(1/(1 + T)) * scale (the label column
-//            less scale) range by range; as soon as a range is written the
-//            bulk copy of the next row's chunk into it starts.
+//            less scale); once the slice is written, the bulk copy of the
+//            CTA's next row starts. The copy's latency hides behind the other
+//            CTAs of the SM (four per SM): handing the slice over in two or
+//            four ranges, each behind its own CTA barrier, measured slower
+//            (16384 x 50257: 1.010 / 1.024 ms against 0.992 ms).
 //
 // The same kernel writes two other rows of the same statistics (kMode):
 //   kModeSoftmax     out = exp(x - M) * f32(1/(1 + T)): no label, no scale;
@@ -325,36 +330,34 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
     const int c0 = static_cast<int>(rank) * cols;
     const int n = max(0, min(a.vocab, c0 + cols) - c0);
     const float scale = a.scale;
-    const int W = ((cols + 9) / 4 + kChunks - 1) / kChunks;  // vectors per range (covers any off)
     const int64_t G = cluster_count_x();
 
-    // the bulk copy of chunk c (the body of range c) of `row`
-    auto issue = [&](int64_t row, int c, uint64_t policy) {
+    // the bulk copy of the aligned body of `row`'s slice
+    auto issue = [&](int64_t row, uint64_t policy) {
         const float *p = a.logits + row * a.stride + c0;
         const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
         const int head = min(n, (4 - off) & 3);
         const int nvec = (n - head) >> 2;
         const int qa = (off + head) >> 2;
-        const int q0 = max(qa, c * W), q1 = min(qa + nvec, (c + 1) * W);
-        const uint32_t bytes = q1 > q0 ? static_cast<uint32_t>(q1 - q0) * 16u : 0u;
-        mbar_arrive_expect_tx(&h.bar[c], bytes);
-        if (bytes) bulk_copy_g2s(buf4 + q0, p - off + 4 * q0, bytes, &h.bar[c], policy);
+        const uint32_t bytes = static_cast<uint32_t>(nvec) * 16u;
+        mbar_arrive_expect_tx(&h.bar, bytes);
+        if (bytes) bulk_copy_g2s(buf4 + qa, p - off + 4 * qa, bytes, &h.bar, policy);
     };
 
     const int64_t cid = cluster_id_x();
     const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;  // rows of this cluster
     uint64_t policy = 0;
     if (tid == 0) {
-        for (int c = 0; c < kChunks; ++c) mbar_init(&h.bar[c], 1);
+        mbar_init(&h.bar, 1);
         fence_mbar_init();
         push_xchg_init(h.xg, K, C);
         policy = l2_policy_evict_first();
-        if (K > 0)
-            for (int c = 0; c < kChunks; ++c) issue(cid, c, policy);
+        if (K > 0) issue(cid, policy);
     }
     __syncthreads();
-    cluster_arrive();  // every CTA's barriers exist before a peer pushes to them
-    cluster_wait();
+    // every CTA's barriers exist before a peer pushes to them: the matching
+    // wait comes just before the first push, under the first row's sweeps
+    cluster_arrive();
 
     bool failed = false;
     uint32_t parity = 0;
@@ -371,13 +374,14 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         const int jbase = c0 - off;             // column of float 0 of buf
         const bool more = row + G < a.rows;
 
-        // the partial end vectors (at most two), loaded by their owners
+        // the partial end vectors (at most two), loaded by their owners and
+        // stored straight into the buffer: they lie outside the bulk copy's
+        // bytes, and the previous row's reads of them ended at its last barrier
         const int qe0 = qa == 1 ? 0 : -1;
         const int qe1 = qa + nvec < nq ? qa + nvec : -1;
-        auto owner = [&](int q) { return (q - (q / W) * W) % T; };
-        float4 edge0 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), edge1 = edge0;
-        if (qe0 >= 0 && owner(qe0) == tid) edge0 = load_edge(p, off, n, qe0);
-        if (qe1 >= 0 && owner(qe1) == tid) edge1 = load_edge(p, off, n, qe1);
+        auto owner = [&](int q) { return q & (T - 1); };  // T is a power of 2
+        if (qe0 >= 0 && owner(qe0) == tid) buf4[qe0] = load_edge(p, off, n, qe0);
+        if (qe1 >= 0 && owner(qe1) == tid) buf4[qe1] = load_edge(p, off, n, qe1);
         const int64_t label = label_next;
         if (kCE && more) label_next = a.labels[row + G];
         const bool lab_ok = !kCE || label_valid(label, a.vocab);
@@ -388,36 +392,29 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         // sweep 1: max and its first vector
         float m = -INFINITY;
         int qm = -1;
-        for (int c = 0; c < kChunks; ++c) {
-            const int qend = min(nq, (c + 1) * W);
-            if (c * W + tid < qend && !failed) failed = !mbar_wait_bounded(&h.bar[c], parity);
-            for (int q = c * W + tid; q < qend; q += T) {
-                if (q == qe0 || q == qe1) buf4[q] = q == qe0 ? edge0 : edge1;
-                const float mv = max4(buf4[q]);
-                if (mv > m) {
-                    m = mv;
-                    qm = q;
-                }
+        if (tid < nq && !failed) failed = !mbar_wait_bounded(&h.bar, parity);
+        for (int q = tid; q < nq; q += T) {
+            const float mv = max4(buf4[q]);
+            if (mv > m) {
+                m = mv;
+                qm = q;
             }
         }
         // x[label]: read by the thread that owns its vector, before it
         // overwrites anything below (only that thread touches that vector)
         if (lab_q >= 0 && owner(lab_q) == tid) h.bc[2] = buf[lab_f];
 
-        // sweep 2: e = exp(x - m) in place; t sums all but the first element
-        // holding m (masked to -inf for the sweep, then given e = 1)
+        // sweep 2: t sums exp(x - m) over all but the first element holding
+        // m (masked to -inf for the sweep, then restored)
         RowState st;
         if (m != -INFINITY) {
             const float4 vm = buf4[qm];
             const int lm = vm.x == m ? 0 : vm.y == m ? 1 : vm.z == m ? 2 : 3;
             buf[4 * qm + lm] = -INFINITY;
             float2 acc = make_float2(0.0f, 0.0f);
-            for (int c = 0; c < kChunks; ++c) {
-                const int qend = min(nq, (c + 1) * W);
-                for (int q = c * W + tid; q < qend; q += T) {
-                    const float4 e = exp4_sub(buf4[q], m);
-                    acc = __fadd2_rn(acc, __fadd2_rn(make_float2(e.x, e.y), make_float2(e.z, e.w)));
-                }
+            for (int q = tid; q < nq; q += T) {
+                const float4 e = exp4_sub(buf4[q], m);
+                acc = __fadd2_rn(acc, __fadd2_rn(make_float2(e.x, e.y), make_float2(e.z, e.w)));
             }
             const float t = acc.x + acc.y;
             buf[4 * qm + lm] = m;
@@ -426,18 +423,16 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
             // no value above -inf among this thread's columns: the exact
             // update; e is 0 for -inf and NaN for NaN
             st = empty_state();
-            for (int c = 0; c < kChunks; ++c) {
-                const int qend = min(nq, (c + 1) * W);
-                for (int q = c * W + tid; q < qend; q += T) {
-                    for (int l = 0; l < 4; ++l) {
-                        const int i = 4 * q + l;
-                        const float x = buf[i];
-                        if (i >= off && i - off < n) push<true>(st, x, jbase + i);
-                    }
+            for (int q = tid; q < nq; q += T) {
+                for (int l = 0; l < 4; ++l) {
+                    const int i = 4 * q + l;
+                    const float x = buf[i];
+                    if (i >= off && i - off < n) push<true>(st, x, jbase + i);
                 }
             }
         }
         st = block_reduce_w0<true>(st, h.red);
+        if (k == 0) cluster_wait();
 
         // exchange over the cluster: push this CTA's state into slot k % 2 of
         // every CTA (st.async, completing bytes on their slot barrier); warp 0
@@ -462,46 +457,41 @@ __global__ void __launch_bounds__(kStagedMaxThreads, 3) k_grad_staged(Args a, in
         }
         __syncthreads();
 
-        // the output, range by range; each freed range takes the next
-        // row's chunk
+        // the output
         const float M = h.bc[0], rcp = h.bc[1];
         const float cm = rcp * scale;
         float *gp = a.grad + row * static_cast<int64_t>(a.vocab) + c0;  // column c0
         const bool vec_store = ((reinterpret_cast<uintptr_t>(gp) >> 2) & 3) == static_cast<uintptr_t>(off);
-        for (int c = 0; c < kChunks; ++c) {
-            const int qend = min(nq, (c + 1) * W);
-            for (int q = c * W + tid; q < qend; q += T) {
-                const float4 g = kLog ? sub2_4(buf4[q], M, rcp) : mul4(exp4_sub(buf4[q], M), cm);
-                if (vec_store && static_cast<unsigned>(q - qa) < static_cast<unsigned>(nvec)) {
-                    __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
-                } else {
-                    const int i = 4 * q - off;  // column - c0 of lane 0
-                    if (i >= 0 && i < n) __stcs(gp + i, g.x);
-                    if (i + 1 >= 0 && i + 1 < n) __stcs(gp + i + 1, g.y);
-                    if (i + 2 >= 0 && i + 2 < n) __stcs(gp + i + 2, g.z);
-                    if (i + 3 >= 0 && i + 3 < n) __stcs(gp + i + 3, g.w);
-                }
-            }
-            // the label column: its owner stored e * c there above; this
-            // later store by the same thread replaces it
-            if (lab_q >= c * W && lab_q < qend && owner(lab_q) == tid)
-                __stcs(gp + lab_local, (exp_le0(buf[lab_f] - M) * rcp - 1.0f) * scale);
-            if (more) {
-                __syncthreads();  // range c is free
-                if (tid == 0) {
-                    fence_proxy_async_smem();
-                    issue(row + G, c, policy);
-                }
+        for (int q = tid; q < nq; q += T) {
+            const float4 g = kLog ? sub2_4(buf4[q], M, rcp) : mul4(exp4_sub(buf4[q], M), cm);
+            if (vec_store && static_cast<unsigned>(q - qa) < static_cast<unsigned>(nvec)) {
+                __stcs(reinterpret_cast<float4 *>(gp - off) + q, g);
+            } else {
+                const int i = 4 * q - off;  // column - c0 of lane 0
+                if (i >= 0 && i < n) __stcs(gp + i, g.x);
+                if (i + 1 >= 0 && i + 1 < n) __stcs(gp + i + 1, g.y);
+                if (i + 2 >= 0 && i + 2 < n) __stcs(gp + i + 2, g.z);
+                if (i + 3 >= 0 && i + 3 < n) __stcs(gp + i + 3, g.w);
             }
         }
-        __syncthreads();  // edge vectors and bc are rewritten for the next row
+        // the label column: its owner stored e * c there above; this later
+        // store by the same thread replaces it
+        if (lab_q >= 0 && owner(lab_q) == tid) __stcs(gp + lab_local, (exp_le0(buf[lab_f] - M) * rcp - 1.0f) * scale);
+        // the slice, the edge vectors and bc are free: the next row's copy
+        // starts, and they are rewritten for the next row
+        __syncthreads();
+        if (more && tid == 0) {
+            fence_proxy_async_smem();
+            issue(row + G, policy);
+        }
     }
+    if (K == 0) cluster_wait();  // the first arrive's match, for a cluster without rows
     cluster_arrive();  // no CTA leaves while a peer may still push to it
     cluster_wait();
     if (__syncthreads_or(failed) && tid == 0) {
         atomicAdd(&g_status[1], 1ull);
-        // give copies still in flight a last bounded chance to land
-        for (int c = 0; c < kChunks; ++c) (void)mbar_wait_bounded(&h.bar[c], parity ^ 1u, 10000000ull);
+        // give a copy still in flight a last bounded chance to land
+        (void)mbar_wait_bounded(&h.bar, parity ^ 1u, 10000000ull);
     }
 }
 
@@ -526,8 +516,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
     const int64_t K = cid < a.rows ? (a.rows - 1 - cid) / G + 1 : 0;  // rows of this cluster
     if (tid == 0) push_xchg_init(xg, K, C);
     __syncthreads();
-    cluster_arrive();  // every CTA's slot barriers exist before a peer pushes to them
-    cluster_wait();
+    cluster_arrive();  // slot barriers exist before a peer pushes: the wait comes before the first push
     bool failed = false;
     int64_t k = 0;
     for (int64_t row = cid; row < a.rows; row += G, ++k) {
@@ -540,6 +529,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
         RowState st = empty_state();
         if (n > 0) st = scan_global<true>(p, c0, n);
         st = block_reduce_w0<true>(st, red);
+        if (k == 0) cluster_wait();
         if (tid == 0) push_xchg_publish(xg, k, rank, C, st, xl_own);
         if (tid < 32) {
             float xl;
@@ -571,6 +561,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_grad_stream(Args a, in
         }
         __syncthreads();  // bc and red are rewritten for the next row
     }
+    if (K == 0) cluster_wait();  // the first arrive's match, for a cluster without rows
     cluster_arrive();  // no CTA leaves while a peer may still push to it
     cluster_wait();
     if (__syncthreads_or(failed) && tid == 0) atomicAdd(&g_status[1], 1ull);
@@ -714,10 +705,6 @@ __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
     float2 v;
     asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
     return v;
-}
-
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
 // Insert the values whose bits are set in `mask` (bit u: the value of the
@@ -1280,6 +1267,34 @@ __global__ void __launch_bounds__(kMeanThreads) k_mean(const float *__restrict__
     }
 }
 
+// ---------------------------------------------------------------------------
+// k_read_probe: a plain read of n16 16-byte vectors, eight loads in flight per
+// thread in a grid-stride loop, folded by XOR into one word -- the ceiling of a
+// read of that size on this device, for measurement beside the row kernels.
+constexpr int kProbeThreads = 512;
+
+__global__ void __launch_bounds__(kProbeThreads) k_read_probe(const float4 *__restrict__ p, int64_t n16,
+                                                              uint32_t *__restrict__ out) {
+    const int64_t T = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    uint32_t acc = 0;
+    for (; i + 7 * T < n16; i += 8 * T) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = ld_stream_f4(p + i + u * T);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            acc ^= __float_as_uint(v[u].x) ^ __float_as_uint(v[u].y) ^ __float_as_uint(v[u].z) ^
+                   __float_as_uint(v[u].w);
+    }
+    for (; i < n16; i += T) {
+        const float4 v = ld_stream_f4(p + i);
+        acc ^= __float_as_uint(v.x) ^ __float_as_uint(v.y) ^ __float_as_uint(v.z) ^ __float_as_uint(v.w);
+    }
+    acc = __reduce_xor_sync(kFullMask, acc);
+    if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
+}
+
 cudaError_t launch_clustered(const void *fn, const Plan &p, void **args, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.clusters * p.cluster), 1, 1);
@@ -1459,6 +1474,17 @@ cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_mean, loss, rows, out);
+}
+
+cudaError_t launch_read_probe(const void *p, int64_t bytes, uint32_t *out, int sms, cudaStream_t s) {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_read_probe, kProbeThreads, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t n16 = bytes / 16;
+    const int64_t need = (n16 + kProbeThreads - 1) / kProbeThreads;
+    const int ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, int64_t(per_sm) * sms)));
+    k_read_probe<<<ctas, kProbeThreads, 0, s>>>(static_cast<const float4 *>(p), n16, out);
+    return cudaGetLastError();
 }
 
 cudaError_t read_status(unsigned long long out[2], cudaStream_t s) {

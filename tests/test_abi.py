@@ -20,7 +20,7 @@ def test_exports_every_declared_function(lib):
     assert set(names) >= {"ce_rows", "ce_mean", "ce_loss", "ce_grad", "ce_grad_step", "argmax_rows",
                           "ce_status_string",
                           "ce_version", "ce_last_cuda_error", "ce_device_error_count", "ce_device_wait_timeouts",
-                          "ce_device_error_reset", "ce_debug_force", "ce_debug_grid_cap", "ce_plan", "softmax_rows",
+                          "ce_device_error_reset", "ce_debug_force", "ce_debug_grid_cap", "ce_plan", "ce_debug_read", "softmax_rows",
                           "log_softmax_rows", "candidates_rows", "split_sum", "argmax_rows_noalloc",
                           "argmax_rows_indirect", "candidates_rows_indirect"}
     missing = [n for n in names if not hasattr(lib, n)]
@@ -160,6 +160,15 @@ def test_zero_rows_is_a_no_op_without_device(lib):
     assert lib.argmax_rows(None, 0, 10, 10, None, None) == ce.CE_OK
     assert lib.ce_grad(None, 0, 10, 10, None, 1.0, None, None, None) == ce.CE_OK
     assert lib.ce_grad_step(None, 0, 10, 10, None, 1.0, None, None, None, None, None) == ce.CE_OK
+
+
+def test_read_probe_validation(lib):
+    assert lib.ce_debug_read(V(256), 32, None, None) == ce.CE_EINVAL        # no output
+    assert lib.ce_debug_read(V(256), 30, V(4096), None) == ce.CE_EINVAL     # not whole 16-byte vectors
+    assert lib.ce_debug_read(V(256), -16, V(4096), None) == ce.CE_EINVAL
+    assert lib.ce_debug_read(None, 32, V(4096), None) == ce.CE_EINVAL
+    assert lib.ce_debug_read(V(264), 32, V(4096), None) == ce.CE_EALIGN     # 16-byte aligned reads
+    assert lib.ce_debug_read(V(256), 32, V(4098), None) == ce.CE_EALIGN
 
 
 def test_debug_force_validation(lib):

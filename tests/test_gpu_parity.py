@@ -425,3 +425,15 @@ def test_warp_per_row_path(orc, offset):
     finally:
         ce.debug_force(0, 0, 0)
         ce.device_error_reset()
+
+
+@pytest.mark.parametrize("words", [4, 4096, (1 << 20) + 12, 38928384])
+def test_read_probe_reads_every_word(words):
+    """ce_debug_read, the bench's plain-read ceiling, reads every word once:
+    its XOR of the words equals the host's."""
+    g = torch.Generator().manual_seed(words)
+    x = torch.randint(-(2 ** 31), 2 ** 31 - 1, (words,), dtype=torch.int32, generator=g)
+    out = ce.debug_read(x.to(DEV))
+    torch.cuda.synchronize()
+    want = np.bitwise_xor.reduce(x.numpy().view(np.uint32))
+    assert int(out.item()) & 0xFFFFFFFF == int(want)
