@@ -97,11 +97,13 @@ void plan_stream(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &
     if (cluster) {
         p.cluster = cluster;
     } else if (op == kOpArgmax) {
-        // argmax (branch-free scan): split rows until about four CTAs per SM;
-        // none from three rows per SM up. Measured on GB300, rows x 151936, L2
-        // flushed (us, by CTAs per row): 256 rows 36.9 / 30.8 / 28.7 / 34.8 for
-        // 1 / 2 / 3 / 4; 128 rows best at 5 (18.4); 512 rows best at 1 (51.2).
-        int64_t c = rows >= 3 * static_cast<int64_t>(dev.sms) ? 1 : ceil_div(4 * static_cast<int64_t>(dev.sms), rows);
+        // argmax (branch-free scan, eight loads in flight): split rows until
+        // about four and a half CTAs per SM; none from three rows per SM up.
+        // Measured on GB300, rows x 151936, L2 flushed (us, by CTAs per row 1 /
+        // 2 / 3 / 4 / 5 / 6): 256 rows 37.3 / 31.5 / 30.8 / 37.0 / 34.7 / 31.2;
+        // 128 rows 33.1 / 23.2 / 20.9 / 22.4 / 20.8 / 18.9; 512 rows 53.9 /
+        // 59.9 / 53.2 / 59.9 / 57.3 / 56.1.
+        int64_t c = rows >= 3 * static_cast<int64_t>(dev.sms) ? 1 : ceil_div(9 * static_cast<int64_t>(dev.sms), 2 * rows);
         c = std::min<int64_t>(c, std::min<int64_t>(kMaxCluster, ceil_div(vocab, kStreamMinCols)));
         p.cluster = static_cast<int>(std::max<int64_t>(1, c));
     } else {
@@ -206,7 +208,13 @@ void plan_candidates(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev
     }
     p.cluster = static_cast<int>(std::max<int64_t>(1, c));
     p.cols = round_up4(ceil_div(vocab, p.cluster));
-    p.smem = kCandRingBytes + (p.cluster > 1 ? kCandListBytes : 0);
+    // chunks of 32 blocks where the grid has at most two CTAs per SM (their
+    // ring allows two per SM), else of 15 (four per SM). Measured on GB300, L2
+    // flushed (us, 15 / 30 / 36 blocks): 256 x 151936 39.1 / 33.2 / 32.7;
+    // 4096 x 32000 114 / 125 / 127; 16384 x 50257 588 / 711 / 702.
+    p.chunk = rows * static_cast<int64_t>(p.cluster) <= 2 * static_cast<int64_t>(dev.sms) ? kCandChunkLarge
+                                                                                          : kCandChunkSmall;
+    p.smem = cand_ring_bytes(p.chunk) + (p.cluster > 1 ? kCandListBytes : 0);
     p.clusters = std::min<int64_t>(rows, kMaxClusters);
 }
 
@@ -222,7 +230,7 @@ bool ring_argmax_applies(int64_t rows, const DeviceInfo &dev) { return rows >= 4
 void plan_argmax_ring(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int cluster) {
     plan_candidates(p, rows, vocab, dev, cluster);
     p.path = kPathRing;
-    p.smem = kCandRingBytes + (p.cluster > 1 ? kRingArgmaxSlotBytes : 0);
+    p.smem = cand_ring_bytes(p.chunk) + (p.cluster > 1 ? kRingArgmaxSlotBytes : 0);
 }
 
 // Where one warp per row beats a CTA (or cluster) per row, measured on GB300

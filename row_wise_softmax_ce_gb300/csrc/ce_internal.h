@@ -28,22 +28,27 @@ constexpr int kTopEach = 4;
 constexpr int kCandRow = 2 * kCandThreads * kTopEach;
 constexpr int kCandMaxCluster = 8;
 // Shared memory of the candidates kernel: mbarriers and counters, a ring of
-// kCandStages chunks of a row (kCandChunkBlocks blocks of 256 columns on the
-// 16-byte grid of the logits: up to 3 floats before the chunk and 1 after),
-// and, for rows split over a cluster, the lists CTA 0 pulls from the others.
-// 15 blocks keep a split-row CTA at 54 KB: four fit on an SM.
-constexpr int kCandChunkBlocks = 15;
+// kCandStages chunks of a row (B blocks of 256 columns on the 16-byte grid of
+// the logits: up to 3 floats before the chunk and 1 after), and, for rows
+// split over a cluster, the lists CTA 0 pulls from the others. Two chunk
+// sizes: 15 blocks keep a split-row CTA at 54 KB (four per SM) for grids of
+// many CTAs; 32 blocks (104 KB, two per SM) halve the per-chunk overhead where
+// the grid has at most two CTAs per SM (256 decode rows of 151936: 39.1 ->
+// about 33 us).
+constexpr int kCandChunkSmall = 15;
+constexpr int kCandChunkLarge = 32;
 constexpr int kCandStages = 3;
-constexpr int kCandStageFloats = kCandChunkBlocks * kCandThreads + 4;
 constexpr int kCandHeaderBytes = 48;
 constexpr int kCandListBytes = kCandThreads * kTopEach * 8;
-constexpr int kCandRingBytes = kCandHeaderBytes + kCandStages * kCandStageFloats * 4;
-constexpr int kCandMaxSmemBytes = kCandRingBytes + kCandListBytes;
 constexpr int kRingArgmaxSlotBytes = kCandThreads * 8;  // one (value, column) per thread (split rows)
-constexpr int kCandCtasPerSm = 4;  // resident CTAs per SM the shared memory allows
-static_assert(kCandStages * 12 <= kCandHeaderBytes && kCandHeaderBytes % 16 == 0 && kCandStageFloats % 4 == 0 &&
-                  kCandCtasPerSm * (kCandMaxSmemBytes + 1024) <= 228 * 1024,
-              "candidates smem layout");
+constexpr int cand_stage_floats(int blocks) { return blocks * kCandThreads + 4; }
+constexpr int cand_ring_bytes(int blocks) { return kCandHeaderBytes + kCandStages * cand_stage_floats(blocks) * 4; }
+constexpr int cand_max_smem_bytes(int blocks) { return cand_ring_bytes(blocks) + kCandListBytes; }
+static_assert(kCandStages * 12 <= kCandHeaderBytes && kCandHeaderBytes % 16 == 0 &&
+                  cand_stage_floats(kCandChunkSmall) % 4 == 0 && cand_stage_floats(kCandChunkLarge) % 4 == 0 &&
+                  4 * (cand_max_smem_bytes(kCandChunkSmall) + 1024) <= 228 * 1024 &&
+                  2 * (cand_max_smem_bytes(kCandChunkLarge) + 1024) <= 228 * 1024 && kCandChunkLarge <= 32,
+              "candidates smem layout: four small-chunk or two large-chunk CTAs per SM; a 32-bit mark mask");
 constexpr int kSplitThreads = 256;
 
 // Per-CTA shared bytes the staged kernel reserves before its row buffer.
@@ -58,6 +63,7 @@ struct Plan {
     int threads = 256;     // threads per CTA
     int smem = 0;          // dynamic shared bytes per CTA
     int cols = 0;          // columns per CTA (a multiple of 4)
+    int chunk = 0;         // candidates and ring argmax: blocks of 256 columns per ring chunk
     int64_t clusters = 0;  // clusters in the grid (each loops over rows)
 };
 

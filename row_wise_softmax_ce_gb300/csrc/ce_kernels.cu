@@ -41,6 +41,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <utility>
 
 #include "ce_device.cuh"
 #include "ce_internal.h"
@@ -53,6 +54,10 @@ __device__ unsigned long long g_status[2];
 namespace {
 
 constexpr int kUnroll = 4;      // 16-byte loads in flight per thread (streaming)
+// the same for the argmax scan, whose state is two registers: eight in flight
+// (256 x 151936, L2 flushed: 32.9 -> 30.6 us on one box, with a plain read of
+// the same bytes at 28.7 us; clusters of 2: 36.9 -> 32.7 us)
+constexpr int kArgmaxUnroll = 8;
 // the same for a warp alone on its row (4096 x 32000, L2 flushed: argmax
 // 90 -> 80 us, row losses 97 -> 90 us against 4; 12 for the losses needs 76
 // registers and leaves rows unscheduled, 16 for the argmax gains nothing)
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
             if (lab_ok && rp) xl = rp[label];
         }
         RowState st = empty_state();
-        if (n > 0 && rp) st = scan_global<kStats>(rp + c0, c0, n);
+        if (n > 0 && rp) st = scan_global<kStats, kStats ? kUnroll : kArgmaxUnroll>(rp + c0, c0, n);
         st = block_reduce_w0<kStats>(st, red);
         if (k == 0) cluster_wait();
         if (tid == 0) push_xchg_publish(xg, k, rank, C, st, 0.0f);
@@ -712,15 +717,23 @@ __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
 // later in column order than every pair the list holds, as stream_push needs.
 // The warp runs as many steps as its busiest lane has marks; a lane out of
 // marks inserts -inf, which changes nothing (nor does a marked value that is
-// no longer above the list's 4th).
+// no longer above the list's 4th). Each step reads the next marked value
+// before it inserts the current one, so the read's latency overlaps the
+// insertion.
 template <typename Val>
 __device__ __forceinline__ void insert_marked(TopList &L, uint32_t mask, int col0, Val val) {
     const int steps = static_cast<int>(__reduce_max_sync(kFullMask, static_cast<unsigned>(__popc(mask))));
+    int u = __ffs(mask) - 1;  // -1 once the lane's marks are used
+    mask &= mask - 1;
+    float x = u >= 0 ? val(u, col0 + kCandThreads * u) : -INFINITY;
     for (int i = 0; i < steps; ++i) {
-        const int u = __ffs(mask) - 1;  // -1 once the lane's marks are used
-        mask &= mask - 1;
         const int col = col0 + kCandThreads * u;
-        stream_push(L, u >= 0 ? val(u, col) : -INFINITY, col);
+        const int un = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const float xn = un >= 0 ? val(un, col0 + kCandThreads * un) : -INFINITY;
+        stream_push(L, x, col);
+        u = un;
+        x = xn;
     }
 }
 
@@ -728,7 +741,7 @@ __device__ __forceinline__ void insert_marked(TopList &L, uint32_t mask, int col
 
 // ChunkRing: a CTA's even share [jr0, jr1) of the blocks of 256 columns of
 // each of its cluster's rows (cluster cid of G takes rows cid, cid + G, ...),
-// streamed chunk by chunk: kCandChunkBlocks blocks arrive by one bulk copy
+// streamed chunk by chunk: kBlocks blocks arrive by one bulk copy
 // into a ring of kCandStages shared-memory stages (mbarrier full[s]), up to
 // kCandStages chunks ahead, across rows. Each warp counts itself done with a
 // stage (an acq_rel atomic on used[s]); the warp that finishes a chunk last
@@ -741,8 +754,12 @@ struct RowGeom {
     int off, h, e;  // 16-byte phase (floats); columns [0, h) and [e, vocab) outside the copied grid
 };
 
+template <int kBlocks>
 struct ChunkRing {
+    static constexpr int kStageFloats = cand_stage_floats(kBlocks);
     const Args *a;
+    int vocab;     // a->vocab and a->rows, held in registers: read every chunk
+    int64_t rows;
     uint64_t *full;
     uint32_t *used;
     float *stages;
@@ -750,7 +767,8 @@ struct ChunkRing {
     int64_t cid, G;
     uint64_t policy;
 
-    __device__ __forceinline__ ChunkRing(const Args &args, unsigned char *smem) : a(&args) {
+    __device__ __forceinline__ ChunkRing(const Args &args, unsigned char *smem)
+        : a(&args), vocab(args.vocab), rows(args.rows) {
         full = reinterpret_cast<uint64_t *>(smem);
         used = reinterpret_cast<uint32_t *>(full + kCandStages);
         stages = reinterpret_cast<float *>(smem + kCandHeaderBytes);
@@ -758,22 +776,22 @@ struct ChunkRing {
         const int nb = (args.vocab + kCandThreads - 1) / kCandThreads;
         jr0 = static_cast<int>(static_cast<int64_t>(nb) * rank / C);
         jr1 = static_cast<int>(static_cast<int64_t>(nb) * (rank + 1) / C);
-        nk = (jr1 - jr0 + kCandChunkBlocks - 1) / kCandChunkBlocks;
+        nk = (jr1 - jr0 + kBlocks - 1) / kBlocks;
         cid = cluster_id_x();
         G = cluster_count_x();
         policy = l2_policy_evict_first();
     }
     __device__ __forceinline__ RowGeom geom(const float *p) const {
         const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
-        const int h = min(a->vocab, (4 - off) & 3);
-        return RowGeom{off, h, h + ((a->vocab - h) & ~3)};
+        const int h = min(vocab, (4 - off) & 3);
+        return RowGeom{off, h, h + ((vocab - h) & ~3)};
     }
     // the columns [cs, ce) of chunk k
-    __device__ __forceinline__ int chunk_begin(int k) const { return kCandThreads * (jr0 + kCandChunkBlocks * k); }
+    __device__ __forceinline__ int chunk_begin(int k) const { return kCandThreads * (jr0 + kBlocks * k); }
     __device__ __forceinline__ int chunk_end(int k) const {
-        return min(a->vocab, kCandThreads * min(jr0 + kCandChunkBlocks * (k + 1), jr1));
+        return min(vocab, kCandThreads * min(jr0 + kBlocks * (k + 1), jr1));
     }
-    __device__ __forceinline__ float *stage(int s) const { return stages + s * kCandStageFloats; }
+    __device__ __forceinline__ float *stage(int s) const { return stages + s * kStageFloats; }
     // chunk k of `row` into stage s: the grid-aligned body of its columns
     __device__ __forceinline__ void issue(int64_t row, int k, int s) const {
         const float *p = row_start(*a, row);
@@ -800,7 +818,7 @@ struct ChunkRing {
         }
         fence_mbar_init();
         int64_t row = cid;
-        for (int k = 0, s = 0; s < kCandStages && row < a->rows && nk > 0; ++s) {
+        for (int k = 0, s = 0; s < kCandStages && row < rows && nk > 0; ++s) {
             issue(row, k, s);
             if (++k == nk) k = 0, row += G;
         }
@@ -813,12 +831,12 @@ struct ChunkRing {
         int64_t rn = row;
         while (kn >= nk) kn -= nk, rn += G;
         __syncwarp();
-        if (lane == 0 && rn < a->rows && atom_add_acq_rel_smem(&used[s], 1u) % kWarps == kWarps - 1)
+        if (lane == 0 && rn < rows && atom_add_acq_rel_smem(&used[s], 1u) % kWarps == kWarps - 1)
             issue(rn, kn, s);
     }
     // after a wait gave up: a last bounded wait for the copies still in flight
     __device__ __forceinline__ void settle() const {
-        const int64_t K = cid < a->rows ? (a->rows - 1 - cid) / G + 1 : 0;
+        const int64_t K = cid < rows ? (rows - 1 - cid) / G + 1 : 0;
         const int64_t total = K * nk;
         for (int64_t gl = total > kCandStages ? total - kCandStages : 0; gl < total; ++gl)
             (void)mbar_wait_bounded(&full[gl % kCandStages], static_cast<uint32_t>(gl / kCandStages) & 1u,
@@ -835,15 +853,16 @@ struct ChunkRing {
 // insertion once per value that some lane keeps, not once per value read.
 // For C > 1, CTAs 1..C-1 leave their lists in shared memory and CTA 0 pulls
 // and merges them through distributed shared memory and writes the row.
+template <int kBlocks>
 __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *__restrict__ out) {
     using namespace cand;
     extern __shared__ __align__(128) unsigned char smem[];
-    const ChunkRing R(a, smem);
-    float2 *lt = reinterpret_cast<float2 *>(smem + kCandRingBytes) + threadIdx.x;  // list slots (split rows)
+    const ChunkRing<kBlocks> R(a, smem);
+    float2 *lt = reinterpret_cast<float2 *>(smem + cand_ring_bytes(kBlocks)) + threadIdx.x;  // list slots (split rows)
     const int t = threadIdx.x, lane = t & 31;
     const uint32_t rank = cluster_rank(), C = cluster_size();
     const bool vec_out = (reinterpret_cast<uintptr_t>(out) & 15) == 0;
-    constexpr int kChunkCols = kCandChunkBlocks * kCandThreads;
+    constexpr int kChunkCols = kBlocks * kCandThreads;
     if (t == 0) R.start();
     __syncthreads();
 
@@ -868,7 +887,7 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
                 uint32_t mask = 0;
                 if (ce - cs == kChunkCols && cs >= r.h && ce <= r.e) {
 #pragma unroll
-                    for (int u = 0; u < kCandChunkBlocks; ++u) mask |= sv[kCandThreads * u] > thr ? 1u << u : 0u;
+                    for (int u = 0; u < kBlocks; ++u) mask |= sv[kCandThreads * u] > thr ? 1u << u : 0u;
                     insert_marked(L, mask, cs + t, [&](int u, int) { return sv[kCandThreads * u]; });
                 } else {
                     // a chunk at the row's ends or cut short: columns past ce
@@ -877,7 +896,7 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
                         return (col >= r.h && col < r.e) ? sv[kCandThreads * u] : ld_stream_f1(p + col);
                     };
 #pragma unroll 4
-                    for (int u = 0; u < kCandChunkBlocks; ++u) {
+                    for (int u = 0; u < kBlocks; ++u) {
                         const int col = cs + t + kCandThreads * u;
                         if (col < ce && val(u, col) > thr) mask |= 1u << u;
                     }
@@ -953,15 +972,16 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
 // thread-t states over distributed shared memory, then reduces its 256
 // states (larger value, then lower column) and writes the token, 0 for a row
 // of NaN only.
+template <int kBlocks>
 __global__ void __launch_bounds__(kCandThreads, 4) k_argmax_ring(Args a) {
     using namespace cand;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float2 red[kCandThreads / 32];
-    const ChunkRing R(a, smem);
-    float2 *lt = reinterpret_cast<float2 *>(smem + kCandRingBytes) + threadIdx.x;  // state slot (split rows)
+    const ChunkRing<kBlocks> R(a, smem);
+    float2 *lt = reinterpret_cast<float2 *>(smem + cand_ring_bytes(kBlocks)) + threadIdx.x;  // state slot (split rows)
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const uint32_t rank = cluster_rank(), C = cluster_size();
-    constexpr int kChunkCols = kCandChunkBlocks * kCandThreads;
+    constexpr int kChunkCols = kBlocks * kCandThreads;
     if (t == 0) R.start();
     __syncthreads();
 
@@ -981,7 +1001,7 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_argmax_ring(Args a) {
                 const float *sv = R.stage(s) + r.off + t;
                 if (ce - cs == kChunkCols && cs >= r.h && ce <= r.e) {
 #pragma unroll
-                    for (int u = 0; u < kCandChunkBlocks; ++u) {
+                    for (int u = 0; u < kBlocks; ++u) {
                         const float x = sv[kCandThreads * u];
                         const bool gt = x > best;
                         best = gt ? x : best;
@@ -989,7 +1009,7 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_argmax_ring(Args a) {
                     }
                 } else {
 #pragma unroll 4
-                    for (int u = 0; u < kCandChunkBlocks; ++u) {
+                    for (int u = 0; u < kBlocks; ++u) {
                         const int col = cs + t + kCandThreads * u;
                         if (col < ce) {
                             const float x = (col >= r.h && col < r.e) ? sv[kCandThreads * u] : ld_stream_f1(p + col);
@@ -1323,8 +1343,12 @@ const void *kernel_of(const Plan &p, Op op) {
     }
     if (op == kOpSoftmax) return fused_kernel<kModeSoftmax>(p.path);
     if (op == kOpLogSoftmax) return fused_kernel<kModeLogSoftmax>(p.path);
-    if (op == kOpCandidates) return reinterpret_cast<const void *>(&k_candidates);
-    if (p.path == kPathRing) return reinterpret_cast<const void *>(&k_argmax_ring);
+    if (op == kOpCandidates)
+        return p.chunk == kCandChunkLarge ? reinterpret_cast<const void *>(&k_candidates<kCandChunkLarge>)
+                                          : reinterpret_cast<const void *>(&k_candidates<kCandChunkSmall>);
+    if (p.path == kPathRing)
+        return p.chunk == kCandChunkLarge ? reinterpret_cast<const void *>(&k_argmax_ring<kCandChunkLarge>)
+                                          : reinterpret_cast<const void *>(&k_argmax_ring<kCandChunkSmall>);
     if (p.path == kPathWarp)
         return op == kOpRows ? reinterpret_cast<const void *>(&k_rows_warp<true>)
                              : reinterpret_cast<const void *>(&k_rows_warp<false>);
@@ -1343,8 +1367,10 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
                          reinterpret_cast<const void *>(&k_grad_stream<kModeGrad>),
                          reinterpret_cast<const void *>(&k_grad_stream<kModeSoftmax>),
                          reinterpret_cast<const void *>(&k_grad_stream<kModeLogSoftmax>),
-                         reinterpret_cast<const void *>(&k_candidates),
-                         reinterpret_cast<const void *>(&k_argmax_ring)};
+                         reinterpret_cast<const void *>(&k_candidates<kCandChunkSmall>),
+                         reinterpret_cast<const void *>(&k_candidates<kCandChunkLarge>),
+                         reinterpret_cast<const void *>(&k_argmax_ring<kCandChunkSmall>),
+                         reinterpret_cast<const void *>(&k_argmax_ring<kCandChunkLarge>)};
     for (const void *f : fns) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -1356,11 +1382,16 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
         cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
         if (e != cudaSuccess) return e;
     }
-    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_candidates),
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kCandMaxSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_argmax_ring),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kCandMaxSmemBytes);
+    const std::pair<const void *, int> rings[] = {
+        {reinterpret_cast<const void *>(&k_candidates<kCandChunkSmall>), cand_max_smem_bytes(kCandChunkSmall)},
+        {reinterpret_cast<const void *>(&k_candidates<kCandChunkLarge>), cand_max_smem_bytes(kCandChunkLarge)},
+        {reinterpret_cast<const void *>(&k_argmax_ring<kCandChunkSmall>), cand_max_smem_bytes(kCandChunkSmall)},
+        {reinterpret_cast<const void *>(&k_argmax_ring<kCandChunkLarge>), cand_max_smem_bytes(kCandChunkLarge)}};
+    for (const auto &r : rings) {
+        cudaError_t e = cudaFuncSetAttribute(r.first, cudaFuncAttributeMaxDynamicSharedMemorySize, r.second);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t max_active_clusters(const Plan &p, Op op, int *n) {
@@ -1383,7 +1414,7 @@ cudaError_t launch_rows_stream(const Plan &p, const Args &a, bool stats, cudaStr
         if (stats) return cudaErrorInvalidValue;  // the ring serves the argmax only
         Args aa = a;
         void *args[] = {&aa};
-        return launch_clustered(reinterpret_cast<const void *>(&k_argmax_ring), p, args, s);
+        return launch_clustered(kernel_of(p, kOpArgmax), p, args, s);
     }
     if (p.path == kPathWarp) {
         if (stats)

@@ -279,14 +279,39 @@ def test_candidates_more_rows_than_clusters(orc):
     assert_candidates(cand[pick.to(DEV)], orc.candidates(xs, V), "rows past the grid")
 
 
-def test_candidates_full_size_sampled_rows(orc):
+def test_candidates_full_size_every_row(orc):
+    """8192 x 128256 against the oracle on every row, in chunks of rows."""
     w = W.WORKLOADS[W.HEADLINE]
     b = W.generate(w, device=DEV)
     cand = ce.candidates_rows(b.logits)
-    idx = torch.unique(torch.cat([torch.randint(0, w.rows, (24,), generator=torch.Generator().manual_seed(5)),
-                                  torch.tensor([0, w.rows - 1])])).to(DEV)
-    ref = orc.candidates(b.logits[idx].cpu().numpy(), w.vocab, threads=THREADS)
-    assert_candidates(cand[idx], ref, "full-size candidates (sampled)")
+    torch.cuda.synchronize()
+    for a in range(0, w.rows, 1024):
+        c = min(w.rows, a + 1024)
+        ref = orc.candidates(b.logits[a:c].cpu().numpy(), w.vocab, threads=THREADS)
+        assert_candidates(cand[a:c], ref, f"full-size candidates rows {a}..{c - 1}")
+
+
+# the ring's two chunk sizes (blocks of 256 columns per bulk copy): 32 where
+# the grid has at most two CTAs per SM, else 15
+def _ring_smem(chunk_blocks, split):
+    return 48 + 3 * (chunk_blocks * 256 + 4) * 4 + ((256 * 4 * 8) if split else 0)
+
+
+@pytest.mark.parametrize("extra", [0, 1], ids=["large-chunks", "small-chunks"])
+def test_candidates_both_chunk_sizes(orc, extra):
+    """Rows just at and just past two CTAs per SM: the same rows' candidates
+    through each chunk size, exact against the oracle (odd vocab: every row
+    at another 16-byte phase, ties, NaN and -inf runs inside the chunks)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, V = 2 * sms + extra, 20011
+    p = ce.plan(ce.OP_CANDIDATES, rows, V, V + 2)
+    assert p["cluster"] == 1 and p["smem"] == _ring_smem(15 if extra else 32, False), p
+    x, _ = W.random_logits(rows, V, stride=V + 2, sigma=2.0, seed=17 + extra, pad_value=1e30)
+    x[1, ::7] = float("nan")
+    x[2, 100:9000] = -float("inf")
+    x[3] = torch.randint(0, 3, (V + 2,), generator=torch.Generator().manual_seed(3)).float()
+    cand = ce.candidates_rows(x.to(DEV), vocab=V)
+    assert_candidates(cand, orc.candidates(x.numpy(), V, threads=THREADS), f"{rows} x {V}")
 
 
 def test_candidates_zero_rows():

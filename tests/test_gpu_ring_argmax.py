@@ -93,6 +93,26 @@ def test_decode_workload_full_size(orc):
         assert (top[b.tie_rows.to(DEV)].long() == b.tie_cols[:, 0].to(DEV)).all()
 
 
+@pytest.mark.parametrize("extra", [0, 1], ids=["large-chunks", "small-chunks"])
+def test_both_chunk_sizes(orc, extra):
+    """Rows just at and just past two CTAs per SM: the ring's 32-block and
+    15-block chunks on the same kind of rows (odd vocab: every row phase)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, V = 2 * sms + extra, 20011
+    x, _ = W.random_logits(rows, V, stride=V + 2, sigma=2.0, seed=31 + extra, pad_value=1e30)
+    x[1, 4000] = x[1, 12000] = 40.0            # a tie across chunks: the lower column
+    x[2, :V] = float("nan")
+    x[3, :V] = -float("inf")
+    ce.debug_force(ce.PATH_RING, 1, 0)
+    try:
+        p = ce.plan(ce.OP_ARGMAX, rows, V, V + 2)
+        assert p["smem"] == 48 + 3 * ((15 if extra else 32) * 256 + 4) * 4, p
+    finally:
+        ce.debug_force(0, 0, 0)
+    top = ring_argmax(x.to(DEV), V, 1)
+    assert_tokens(top, orc.argmax(x.numpy(), V), f"ring {rows} x {V}")
+
+
 def test_other_operations_refuse_the_ring():
     x, y = W.random_logits(4, 1000, seed=1)
     xd, yd = x.to(DEV), y.to(DEV)
