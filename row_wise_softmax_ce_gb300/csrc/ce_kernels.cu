@@ -883,20 +883,46 @@ __global__ void __launch_bounds__(kCandThreads, 4) k_candidates(Args a, float *_
             if (p) {
                 const int cs = R.chunk_begin(k), ce = R.chunk_end(k);
                 const float *sv = R.stage(s) + r.off + t;  // sv[256 u]: column cs + t + 256 u
-                const float thr = L.v[3];
-                uint32_t mask = 0;
+                auto fast = [&](int u, int) { return sv[kCandThreads * u]; };
                 if (ce - cs == kChunkCols && cs >= r.h && ce <= r.e) {
+                    if (k == 0) {
+                        // the list starts empty: mark in groups of 8 blocks, each
+                        // against the list's 4th value after the group before, so
+                        // fewer of the chunk's values reach an insertion step
 #pragma unroll
-                    for (int u = 0; u < kBlocks; ++u) mask |= sv[kCandThreads * u] > thr ? 1u << u : 0u;
-                    insert_marked(L, mask, cs + t, [&](int u, int) { return sv[kCandThreads * u]; });
+                        for (int u0 = 0; u0 < kBlocks; u0 += 8) {
+                            const float thr = L.v[3];
+                            uint32_t mask = 0;
+#pragma unroll
+                            for (int u = u0; u < u0 + 8 && u < kBlocks; ++u)
+                                mask |= sv[kCandThreads * u] > thr ? 1u << u : 0u;
+                            insert_marked(L, mask, cs + t, fast);
+                        }
+                    } else {
+                        const float thr = L.v[3];
+                        uint32_t mask = 0;
+#pragma unroll
+                        for (int u = 0; u < kBlocks; ++u) mask |= sv[kCandThreads * u] > thr ? 1u << u : 0u;
+                        insert_marked(L, mask, cs + t, fast);
+                    }
                 } else {
-                    // a chunk at the row's ends or cut short: columns past ce
-                    // are skipped, those outside the grid body read from global
+                    // a chunk at the row's ends or cut short: its whole blocks
+                    // inside the 16-byte grid body [h, e) are read from the
+                    // stage as above; the at most two others column by column
+                    // (columns past ce skipped, those outside the body read
+                    // from global memory)
                     auto val = [&](int u, int col) {
                         return (col >= r.h && col < r.e) ? sv[kCandThreads * u] : ld_stream_f1(p + col);
                     };
-#pragma unroll 4
-                    for (int u = 0; u < kBlocks; ++u) {
+                    const int u_lo = cs < r.h ? 1 : 0;                                 // block 0 of a misaligned row
+                    const int u_hi = max(u_lo, (min(ce, r.e) - cs) / kCandThreads);    // whole blocks in [h, e)
+                    const int u_end = (ce - cs + kCandThreads - 1) / kCandThreads;     // blocks with columns
+                    const float thr = L.v[3];
+                    uint32_t mask = 0;
+#pragma unroll 8
+                    for (int u = u_lo; u < u_hi; ++u) mask |= sv[kCandThreads * u] > thr ? 1u << u : 0u;
+                    for (int u = 0; u < u_end; ++u) {
+                        if (u >= u_lo && u < u_hi) continue;
                         const int col = cs + t + kCandThreads * u;
                         if (col < ce && val(u, col) > thr) mask |= 1u << u;
                     }
