@@ -31,11 +31,12 @@
  *      CE_EALIGN: a pointer is not aligned to its element size;
  *      CE_ECUDA:  the CUDA runtime reported an error at launch
  *                 (ce_last_cuda_error() gives its code).
- *  - rows == 0 is valid and launches nothing, except that ce_loss and
- *    ce_mean still write their mean (NaN: the mean of no rows).
+ *  - rows == 0 is valid and launches nothing, except that ce_loss, ce_mean
+ *    and ce_grad_step (given a loss_mean) still write their mean (NaN: the
+ *    mean of no rows).
  *  - A label outside [0, vocab) is found on the device: that row's loss
  *    is NaN, its gradient row gets no one-hot term, and a device counter
- *    (ce_device_error_count) is incremented. Nothing traps.
+ *    (read by ce_device_error_count) is incremented. Nothing traps.
  *  - A row holding a NaN or +inf, or whose entries are all -inf, has a NaN
  *    loss and a NaN gradient row (the IEEE value of the definition). Its
  *    argmax still follows Tensor.argmax: NaN never wins, first of equals.
@@ -141,10 +142,10 @@ CE_API int ce_grad_step(const float *logits, int64_t rows, int64_t vocab, int64_
  * the training step fed from the host, with the host-to-device copy
  * overlapped with the kernels. The labels, then the logits in chunks of
  * rows, are copied into caller-owned device buffers on a copy stream the
- * library keeps per device; the fused kernel (as ce_grad) runs on each chunk
- * on `stream` as soon as that chunk has landed, so chunk c is computed while
- * chunk c + 1 is copied. Then ce_mean, and the mean and tokens back to the
- * host. Everything is enqueued: the call returns at once, and the host and
+ * library keeps per device; the fused kernel (as ce_grad_step, with the
+ * tokens) runs on each chunk on `stream` as soon as that chunk has landed, so
+ * chunk c is computed while chunk c + 1 is copied. Then ce_mean over all the
+ * rows, and the mean and tokens back to the host. Everything is enqueued: the call returns at once, and the host and
  * device buffers must stay valid, and the host outputs unread, until
  * `stream` has reached this point. Host inputs in page-locked memory copy
  * asynchronously; pageable ones work but the copies may block the caller.

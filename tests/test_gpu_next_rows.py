@@ -428,6 +428,52 @@ def test_step_replayed_from_a_cuda_graph(orc):
         assert_mean(m.item(), orc.ce_mean(orc.ce_rows(x.numpy(), V, y.numpy())), "graph mean")
 
 
+@pytest.mark.parametrize("shape", [(64, 5003), (8192, 2000)], ids=["64x5003", "8192x2000"])
+def test_grad_step_replayed_from_a_cuda_graph(orc, shape):
+    """ce_grad_step (the fused kernel and its mean as a programmatic dependent)
+    and ce_loss captured in one CUDA graph: the dependent launches become graph
+    edges; replays on new batches give the oracle's results, and the means stay
+    on the device."""
+    R, V = shape
+    sx = torch.zeros((R, V), device=DEV)
+    sy = torch.zeros((R,), dtype=torch.int64, device=DEV)
+    grad = torch.empty((R, V), device=DEV)
+    lr, top, lr2 = (torch.empty((R,), device=DEV) for _ in range(3))
+    mean, mean2 = (torch.empty((), dtype=torch.float64, device=DEV) for _ in range(2))
+
+    def step():
+        ce.ce_grad_step(sx, sy, 1.0 / R, grad=grad, loss_rows=lr, top=top, mean=mean)
+        ce.ce_loss(sx, sy, loss_rows=lr2, out=mean2)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    batches = [W.random_logits(R, V, sigma=s_, seed=200 + i) for i, s_ in enumerate((1.0, 4.0))]
+    means = []
+    for x, y in batches:
+        sx.copy_(x.to(DEV))
+        sy.copy_(y.to(DEV))
+        graph.replay()
+        means.append((mean.clone(), mean2.clone()))
+    torch.cuda.synchronize()
+    x, y = batches[-1]
+    g_ref, l_ref = orc.ce_grad(x.numpy(), V, y.numpy(), 1.0 / R, threads=THREADS)
+    assert_grad(grad, g_ref, "graph step grad")
+    assert_loss(lr, l_ref, "graph step loss rows")
+    assert_loss(lr2, l_ref, "graph ce_loss rows")
+    assert_tokens(top, orc.argmax(x.numpy(), V, threads=THREADS), "graph step tokens")
+    for (m, m2), (x, y) in zip(means, batches):
+        m_ref = orc.ce_mean(orc.ce_rows(x.numpy(), V, y.numpy(), threads=THREADS))
+        assert_mean(m.item(), m_ref, "graph step mean")
+        assert_mean(m2.item(), m_ref, "graph ce_loss mean")
+
+
 def test_every_row_family_gives_the_same_bits_every_run():
     """Fixed-shape reductions and merges: five runs, identical bits (a race in a
     split-row combine or an exchange would show as a difference)."""

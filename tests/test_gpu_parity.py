@@ -300,8 +300,10 @@ def test_zero_rows():
     mean, lr = ce.ce_loss(x, y)
     g = ce.ce_grad(x, y, 1.0)
     t = ce.argmax_rows(x)
+    g2, lr2, t2, mean2 = ce.ce_grad_step(x, y, 1.0)
     torch.cuda.synchronize()
     assert np.isnan(mean.item()) and lr.numel() == 0 and g.shape == (0, 100) and t.numel() == 0
+    assert np.isnan(mean2.item()) and lr2.numel() == 0 and g2.shape == (0, 100) and t2.numel() == 0
 
 
 def test_max_vocab_and_beyond(orc):
