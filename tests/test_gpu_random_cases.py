@@ -110,6 +110,8 @@ def test_random_case(orc, seed):
     ce.debug_grid_cap(plans["grid_cap"])
     try:
         grad, lr, top = fused(ce.ce_grad, dx, dy, scale, vocab=vocab, loss_rows=True, top=True)
+        # the whole step: the same fused kernel, then its mean as a programmatic dependent
+        grad_s, lr_s, top_s, mean_s = fused(ce.ce_grad_step, dx, dy, scale, vocab=vocab)
         soft = fused(ce.softmax_rows, dx, vocab=vocab)
         logp = fused(ce.log_softmax_rows, dx, vocab=vocab)
         lr2 = forced_call(plans["rows"], ce.ce_rows, dx, dy, vocab=vocab)
@@ -133,6 +135,10 @@ def test_random_case(orc, seed):
     assert_tokens(top3, a_ref, f"{what}: argmax_rows (ring)")
     # the documented tiny-loss deviation: drawn rows may hold nothing but tiny losses
     assert_mean(mean.item(), orc.ce_mean(l_ref), f"{what}: ce_mean", tiny_loss_rows=l_ref)
+    assert_grad(grad_s, g_ref, f"{what}: ce_grad_step")
+    assert_loss(lr_s, l_ref, f"{what}: ce_grad_step loss")
+    assert_tokens(top_s, a_ref, f"{what}: ce_grad_step tokens")
+    assert_mean(mean_s.item(), orc.ce_mean(l_ref), f"{what}: ce_grad_step mean", tiny_loss_rows=l_ref)
     assert_softmax(soft, orc.softmax(x, vocab, threads=THREADS), f"{what}: softmax_rows")
     assert_log_softmax(logp, orc.log_softmax(x, vocab, threads=THREADS), f"{what}: log_softmax_rows")
     assert_candidates(cand, orc.candidates(x, vocab, threads=THREADS), f"{what}: candidates_rows")
