@@ -198,6 +198,19 @@ __device__ __forceinline__ float ld_stream_f1(const float *p) {
     return v;
 }
 
+// exp(d) for d <= 0 by the change of base exp(d) = 2^(d * log2(e)), with the
+// hardware base-2 exponential ex2.approx.ftz.f32 (relative error below 2^-22;
+// results below 2^-126 flush to 0, i.e. an absolute error below 1.2e-38).
+// Rounding the product d * log2(e) adds a relative error of about
+// |d| * 2^-24 to the result -- at most 2.2e-8 absolute, since |d| * exp(d)
+// <= 1/e for d <= 0.
+__device__ __forceinline__ float ex2_ftz(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+__device__ __forceinline__ float exp_le0(float d) { return ex2_ftz(d * 1.4426950408889634f); }
+
 // ---------------------------------------------------------------------------
 // Online row state.
 //
@@ -212,7 +225,10 @@ __device__ __forceinline__ float ld_stream_f1(const float *p) {
 //   x == m:  t <- t + 1                  (a tie; idx keeps the first)
 //   else:    t <- t + exp(x - m)         (NaN x makes t NaN, and it stays NaN)
 // x == m also covers -inf == -inf and +inf == +inf, where x - m is NaN.
-// In the first two cases exp takes -|x - m|, so one exp serves both.
+// In the first two cases exp takes -|x - m|, so one exp serves both; it is
+// exp_le0 (above), as in the common path. (CUDA's expf on this path -- the
+// one a warp takes whenever one of its lanes meets a new max -- cost 9% of
+// ce_rows on 4096 x 32000 and 18% on 256 x 151936.)
 //
 // Merge two states: the winner has the larger m (ties: smaller idx); then
 //   t <- t_w + (1 + t_l) * exp(m_l - m_w).
@@ -231,7 +247,7 @@ __device__ __forceinline__ void push(RowState &s, float x, int j) {
     const bool gt = x > s.m;
     const bool eq = x == s.m;
     if (kStats) {
-        const float e = eq ? 1.0f : expf(-fabsf(x - s.m));
+        const float e = eq ? 1.0f : exp_le0(-fabsf(x - s.m));
         s.t = gt ? fmaf(s.t, e, e) : s.t + e;
     }
     s.idx = gt ? j : (eq ? min(s.idx, j) : s.idx);
@@ -247,19 +263,6 @@ __device__ __forceinline__ void push4(RowState &s, float4 v, int j) {
 }
 
 __device__ __forceinline__ float max4(float4 v) { return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)); }
-
-// exp(d) for d <= 0 by the change of base exp(d) = 2^(d * log2(e)), with the
-// hardware base-2 exponential ex2.approx.ftz.f32 (relative error below 2^-22;
-// results below 2^-126 flush to 0, i.e. an absolute error below 1.2e-38).
-// Rounding the product d * log2(e) adds a relative error of about
-// |d| * 2^-24 to the result -- at most 2.2e-8 absolute, since |d| * exp(d)
-// <= 1/e for d <= 0.
-__device__ __forceinline__ float ex2_ftz(float y) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
-    return r;
-}
-__device__ __forceinline__ float exp_le0(float d) { return ex2_ftz(d * 1.4426950408889634f); }
 
 // exp(v - m) lane by lane (every lane <= m), the subtraction and the scaling
 // by log2(e) done two lanes per instruction (Blackwell paired f32 ops).
@@ -290,9 +293,8 @@ __device__ __forceinline__ float4 sub2_4(float4 v, float m, float l) {
 // running max m (and m is above -inf), so each adds exp(x - m) -- a tie adds
 // exactly 1 and keeps the first index, a NaN makes t NaN. Otherwise (a new
 // max, or no finite value yet, or all four NaN) the exact scalar update runs.
-// The common case takes exp_le0 (ex2.approx of d * log2(e), above: below
-// about 2.5e-7 relative and 2.2e-8 absolute for the rounding of the
-// product); the exact update calls CUDA's expf.
+// Both take exp_le0 (ex2.approx of d * log2(e), above: below about 2.5e-7
+// relative and 2.2e-8 absolute for the rounding of the product).
 template <bool kStats>
 __device__ __forceinline__ void push_vec(RowState &s, float4 v, int j) {
     const float mv = max4(v);
