@@ -91,26 +91,22 @@ int current_device(DeviceInfo *out) {
 // Launch shape of a streaming kernel (ce_rows, argmax_rows, and the fused
 // path for rows too long to stage): split a row over C CTAs when there are
 // too few rows to give every SM several CTAs.
-void plan_stream(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster) {
+void plan_stream(Plan &p, int64_t rows, int64_t vocab, const DeviceInfo &dev, int threads, int cluster) {
     p.path = kPathStream;
     p.threads = threads ? threads : kStreamMaxThreads;
     if (cluster) {
         p.cluster = cluster;
-    } else if (op == kOpArgmax) {
-        // argmax (branch-free scan, eight loads in flight): split rows until
-        // about four and a half CTAs per SM; none from three rows per SM up.
-        // Measured on GB300, rows x 151936, L2 flushed (us, by CTAs per row 1 /
-        // 2 / 3 / 4 / 5 / 6): 256 rows 37.3 / 31.5 / 30.8 / 37.0 / 34.7 / 31.2;
-        // 128 rows 33.1 / 23.2 / 20.9 / 22.4 / 20.8 / 18.9; 512 rows 53.9 /
-        // 59.9 / 53.2 / 59.9 / 57.3 / 56.1.
-        int64_t c = rows >= 3 * static_cast<int64_t>(dev.sms) ? 1 : ceil_div(9 * static_cast<int64_t>(dev.sms), 2 * rows);
-        c = std::min<int64_t>(c, std::min<int64_t>(kMaxCluster, ceil_div(vocab, kStreamMinCols)));
-        p.cluster = static_cast<int>(std::max<int64_t>(1, c));
     } else {
-        // split a row only when there are fewer rows than about two CTAs per
-        // SM (measured on GB300, 256 x 151936: 2 CTAs per row 32.8 us, 4: 38.9,
-        // 8: 36.9, 16: 43.0)
-        int64_t c = ceil_div(2 * static_cast<int64_t>(dev.sms), rows);
+        // split rows until about four and a half CTAs per SM; none from three
+        // rows per SM up. Measured on GB300, rows x 151936, L2 flushed (us, by
+        // CTAs per row 1 / 2 / 3 / 4 / 5 / 6). Argmax (branch-free scan, eight
+        // loads in flight): 256 rows 37.3 / 31.5 / 30.8 / 37.0 / 34.7 / 31.2;
+        // 128 rows 33.1 / 23.2 / 20.9 / 22.4 / 20.8 / 18.9; 512 rows 53.9 /
+        // 59.9 / 53.2 / 59.9 / 57.3 / 56.1. Row losses: 256 rows 45.2 / 37.0 /
+        // 35.2 / 41.1 / 37.3 / 36.9; 128 rows 41.1 / 28.7 / 24.6 / - / 24.1 /
+        // 22.5; 512 rows 59.1 / 69.2 / 59.3 / - / 61.9 / -; 64 rows 16.7 at 5,
+        // 15.9 at 8 and 11; 200 rows 30.8 at 2, 28.4 at 4.
+        int64_t c = rows >= 3 * static_cast<int64_t>(dev.sms) ? 1 : ceil_div(9 * static_cast<int64_t>(dev.sms), 2 * rows);
         c = std::min<int64_t>(c, std::min<int64_t>(kMaxCluster, ceil_div(vocab, kStreamMinCols)));
         p.cluster = static_cast<int>(std::max<int64_t>(1, c));
     }
@@ -259,11 +255,11 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
             if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, f.path == kPathStagedPerRow, false))
                 return CE_EINVAL;
         } else if (f.path == kPathStream) {
-            plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster);
+            plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
         } else if (f.path == kPathFlat || f.path == kPathWarp || f.path == kPathRing) {
             return CE_EINVAL;
         } else if (!plan_staged(p, op, rows, vocab, dev, f.threads, f.cluster, false, true)) {
-            plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
+            plan_stream(p, rows, vocab, dev, f.threads, f.cluster ? f.cluster : kMaxCluster);
         }
     } else if (op == kOpCandidates) {
         if (f.path != kPathAuto && f.path != kPathStream) return CE_EINVAL;
@@ -287,7 +283,7 @@ int make_plan(Op op, int64_t rows, int64_t vocab, const DeviceInfo &dev, Plan *o
                ring_argmax_applies(rows, dev)) {
         plan_argmax_ring(p, rows, vocab, dev, 0);
     } else {
-        plan_stream(p, op, rows, vocab, dev, f.threads, f.cluster);
+        plan_stream(p, rows, vocab, dev, f.threads, f.cluster);
     }
     if (p.cluster < 1 || p.cluster > kMaxCluster) return CE_EINVAL;
     if (p.path == kPathStream && p.threads > kStreamMaxThreads) return CE_EINVAL;
