@@ -299,7 +299,12 @@ template <bool kStats>
 __device__ __forceinline__ void push_vec(RowState &s, float4 v, int j) {
     const float mv = max4(v);
     if (mv <= s.m && s.m != -INFINITY) {
-        if (kStats) s.t += (exp_le0(v.x - s.m) + exp_le0(v.y - s.m)) + (exp_le0(v.z - s.m) + exp_le0(v.w - s.m));
+        if (kStats) {
+            // the same bits as exp_le0 lane by lane, two lanes per f32 instruction
+            // (256 x 151936 row losses, L2 flushed: 35.3 -> 34.7 us)
+            const float4 e = exp4_sub(v, s.m);
+            s.t += (e.x + e.y) + (e.z + e.w);
+        }
     } else {
         push4<kStats>(s, v, j);
     }
