@@ -169,18 +169,28 @@ bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &
     // bandwidth), one row per cluster when it would loop over few (4096 x
     // 32000: 18 rows per cluster, 93% vs 89%).
     if (auto_form) per_row = rows < 32 * static_cast<int64_t>(active);
-    if (auto_form && !cluster && !threads && !per_row) {
-        // persistent: slices small enough for four CTAs per SM pay when they
-        // put more CTAs on the GPU at once. Measured on GB300, 8192 x 128256
-        // (8 CTAs of 66 KB per row, 408 resident: 94.8% of copy bandwidth;
-        // 10 of 53 KB, 580 resident: 98.9%; 9, 11: 87.8%, 96.3%).
+    if (auto_form && !cluster && !threads) {
+        // slices small enough for four CTAs per SM. Persistent: they pay when
+        // they put more CTAs on the GPU at once. Measured on GB300, 8192 x
+        // 128256 (8 CTAs of 66 KB per row, 408 resident: 94.8% of copy
+        // bandwidth; 10 of 53 KB, 580 resident: 98.9%; 9, 11: 87.8%, 96.3%).
+        // One row per cluster: they pay on rows of three slices or more (L2
+        // flushed, softmax rows x 151936, 10 CTAs per row vs 12: 128 rows 33.0
+        // vs 31.2 us, 256 rows 57.3 vs 54.8 us, 1024 rows 203.6 vs 190.7 us;
+        // the gradient of 256 rows 59.1 vs 56.0 us), not on two (4096 x 32000,
+        // 2 vs 3: softmax 155.9 vs 158.3 us, gradient 156.6 vs 154.3 us).
         Plan q = p;
         int active4 = 0;
         const int64_t c4 = std::max<int64_t>(1, ceil_div(vocab, kStagedTargetCols4));
-        if (c4 != c && staged_shape(q, op, vocab, dev, c4, &active4) && rows >= 32 * static_cast<int64_t>(active4) &&
-            static_cast<int64_t>(active4) * q.cluster > static_cast<int64_t>(active) * p.cluster) {
-            p = q;
-            active = active4;
+        if (c4 != c && staged_shape(q, op, vocab, dev, c4, &active4)) {
+            const bool take = per_row ? c >= 3
+                                      : rows >= 32 * static_cast<int64_t>(active4) &&
+                                            static_cast<int64_t>(active4) * q.cluster >
+                                                static_cast<int64_t>(active) * p.cluster;
+            if (take) {
+                p = q;
+                active = active4;
+            }
         }
     }
     p.clusters = per_row ? std::min<int64_t>(rows, kMaxClusters) : std::min<int64_t>(rows, active);
