@@ -1,7 +1,7 @@
 """Every entry point at once on four CUDA streams (through the C ABI): the
 calls share no scratch, so work enqueued on several streams and run
 concurrently gives each its own results -- the f64 CPU oracle's, within the
-tolerances, and the same bits in every round."""
+tolerances, and the same bits in every pass."""
 import os
 
 import numpy as np
@@ -17,7 +17,7 @@ from parity import (assert_candidates, assert_grad, assert_log_softmax, assert_l
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 THREADS = os.cpu_count() or 1
-ROUNDS = 3
+PASSES = 3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -49,8 +49,8 @@ def test_entry_points_concurrent_on_four_streams(orc):
     torch.cuda.synchronize()
 
     streams = [torch.cuda.Stream() for _ in range(4)]
-    rounds = []
-    for _ in range(ROUNDS):
+    passes = []
+    for _ in range(PASSES):
         out = {}
         # enqueue round-robin, one call per stream at a time, so the streams' work interleaves
         with torch.cuda.stream(streams[0]):
@@ -66,10 +66,10 @@ def test_entry_points_concurrent_on_four_streams(orc):
         with torch.cuda.stream(streams[3]):
             out["logp"] = ce.log_softmax_rows(dd, vocab=16385)
             out["rows"] = ce.ce_rows(dd, dyd, vocab=16385)
-        rounds.append(out)
+        passes.append(out)
     torch.cuda.synchronize()
 
-    first = rounds[0]
+    first = passes[0]
     g_ref, l_ref = orc.ce_grad(xa.numpy(), 50257, ya.numpy(), 1.0 / 1024, threads=THREADS)
     grad, lr, top, mean = first["step"]
     assert_grad(grad, g_ref, "ce_grad_step grad")
@@ -94,7 +94,7 @@ def test_entry_points_concurrent_on_four_streams(orc):
         ts = o if isinstance(o, tuple) else (o,)
         return [t.cpu().numpy().reshape(-1).view(np.uint8) for t in ts]
 
-    for k, later in enumerate(rounds[1:], 1):
+    for k, later in enumerate(passes[1:], 1):
         for name in first:
             for a, b in zip(flat(first[name]), flat(later[name])):
-                assert np.array_equal(a, b), f"{name}: round {k} differs from round 0"
+                assert np.array_equal(a, b), f"{name}: pass {k} differs from pass 0"
