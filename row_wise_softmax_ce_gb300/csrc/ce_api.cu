@@ -24,7 +24,8 @@ constexpr int kVersion = 10000;            // 1.0.0
 constexpr int64_t kMaxVocab = 1ll << 24;   // tokens are written exactly as f32
 constexpr int kMaxDevices = 64;
 constexpr int kStagedTargetCols = 16384;   // 64 KB of f32 per CTA: 3 CTAs per SM
-constexpr int kStagedTargetCols4 = 13312;  // 52 KB of f32 per CTA: 4 CTAs per SM
+constexpr int kStagedTargetCols4 = 13816;  // the widest slice of which 4 CTAs fit an SM's 228 KB
+                                           // (2 KB header, 16-byte grid, 1 KB reserved per CTA)
 constexpr int kStreamMinCols = 2048;       // columns per CTA, at least, when a row is split
 constexpr int64_t kMaxClusters = 1ll << 20;
 
@@ -175,10 +176,11 @@ bool plan_staged(Plan &p, Op op, int64_t rows, int64_t vocab, const DeviceInfo &
         // 128256 (8 CTAs of 66 KB per row, 408 resident: 94.8% of copy
         // bandwidth; 10 of 53 KB, 580 resident: 98.9%; 9, 11: 87.8%, 96.3%).
         // One row per cluster: they pay on rows of three slices or more (L2
-        // flushed, softmax rows x 151936, 10 CTAs per row vs 12: 128 rows 33.0
-        // vs 31.2 us, 256 rows 57.3 vs 54.8 us, 1024 rows 203.6 vs 190.7 us;
-        // the gradient of 256 rows 59.1 vs 56.0 us), not on two (4096 x 32000,
-        // 2 vs 3: softmax 155.9 vs 158.3 us, gradient 156.6 vs 154.3 us).
+        // flushed, softmax rows x 151936, 10 CTAs per row (3 per SM) vs 12 vs
+        // 11 (4 per SM): 128 rows 33.0 / 31.2 / - us, 256 rows 57.3 / 54.8 /
+        // 53.4 us, 1024 rows 203.6 / 190.7 / 185.0 us; the gradient of 256
+        // rows 59.1 / 55.8 / 55.2 us; 13 per row: 57.9 us), not on two (4096 x
+        // 32000, 2 vs 3: softmax 155.9 vs 158.3 us, gradient 156.6 vs 154.3 us).
         Plan q = p;
         int active4 = 0;
         const int64_t c4 = std::max<int64_t>(1, ceil_div(vocab, kStagedTargetCols4));
