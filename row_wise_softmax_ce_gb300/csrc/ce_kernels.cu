@@ -114,8 +114,13 @@ __device__ __forceinline__ float row_token(const RowState &g) {
 // compares keep the first vector of equals, and NaN never wins (fmaxf drops
 // it). A thread whose vectors hold nothing above -inf rescans them exactly
 // (only rows of -inf and NaN get there).
+//
+// The thread takes the body vectors q0, q0 + S, q0 + 2S, ... (in increasing
+// column order); `edge` is its index among the threads that read the at most
+// three columns before the first 16-byte boundary and after the last (-1:
+// none). One thread set reading [j0, j0 + n) alone: q0 = edge = tid, S = T.
 template <int kU>
-__device__ __forceinline__ RowState scan_argmax(const float *__restrict__ p, int j0, int n, int tid, int T) {
+__device__ __forceinline__ RowState scan_argmax(const float *__restrict__ p, int j0, int n, int q0, int S, int edge) {
     RowState st = empty_state();
     const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
     const int head = min(n, (4 - off) & 3);
@@ -123,25 +128,25 @@ __device__ __forceinline__ RowState scan_argmax(const float *__restrict__ p, int
     const int tail = n - head - 4 * nvec;
     const float4 *pv = reinterpret_cast<const float4 *>(p + head);
     const int jv = j0 + head;
-    if (tid < head) push<false>(st, ld_stream_f1(p + tid), j0 + tid);
+    if (edge >= 0 && edge < head) push<false>(st, ld_stream_f1(p + edge), j0 + edge);
     float best = -INFINITY;
     int bk = -1;
     float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
-    int k = tid;
-    for (; k + (kU - 1) * T < nvec; k += kU * T) {
+    int k = q0;
+    for (; k + (kU - 1) * S < nvec; k += kU * S) {
         float4 v[kU];
 #pragma unroll
-        for (int u = 0; u < kU; ++u) v[u] = ld_stream_f4(pv + k + u * T);
+        for (int u = 0; u < kU; ++u) v[u] = ld_stream_f4(pv + k + u * S);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
             const float mv = max4(v[u]);
             const bool gt = mv > best;
             best = gt ? mv : best;
-            bk = gt ? k + u * T : bk;
+            bk = gt ? k + u * S : bk;
             bv = gt ? v[u] : bv;
         }
     }
-    for (; k < nvec; k += T) {
+    for (; k < nvec; k += S) {
         const float4 v = ld_stream_f4(pv + k);
         const float mv = max4(v);
         const bool gt = mv > best;
@@ -153,9 +158,9 @@ __device__ __forceinline__ RowState scan_argmax(const float *__restrict__ p, int
         const int l = bv.x == best ? 0 : bv.y == best ? 1 : bv.z == best ? 2 : 3;
         push<false>(st, best, jv + 4 * bk + l);
     } else {
-        for (k = tid; k < nvec; k += T) push4<false>(st, ld_stream_f4(pv + k), jv + 4 * k);
+        for (k = q0; k < nvec; k += S) push4<false>(st, ld_stream_f4(pv + k), jv + 4 * k);
     }
-    if (tid < tail) push<false>(st, ld_stream_f1(p + head + 4 * nvec + tid), jv + 4 * nvec + tid);
+    if (edge >= 0 && edge < tail) push<false>(st, ld_stream_f1(p + head + 4 * nvec + edge), jv + 4 * nvec + edge);
     return st;
 }
 
@@ -164,7 +169,7 @@ __device__ __forceinline__ RowState scan_argmax(const float *__restrict__ p, int
 // vectors, a scalar tail. Each thread sees its columns in increasing order.
 template <bool kStats, int kU = kUnroll>
 __device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int j0, int n, int tid, int T) {
-    if constexpr (!kStats) return scan_argmax<kU>(p, j0, n, tid, T);
+    if constexpr (!kStats) return scan_argmax<kU>(p, j0, n, tid, T, tid);
     RowState st = empty_state();
     const int off = static_cast<int>((reinterpret_cast<uintptr_t>(p) >> 2) & 3);
     const int head = min(n, (4 - off) & 3);
@@ -194,7 +199,9 @@ __device__ __forceinline__ RowState scan_global(const float *__restrict__ p, int
 
 // ---------------------------------------------------------------------------
 // k_rows_stream: row loss (kStats) and/or argmax token; one read per logit.
-// The C CTAs of a cluster split a row; their states meet by pushes.
+// The C CTAs of a cluster split a row -- the loss in C contiguous slices of
+// `cols` columns, the argmax by taking the row's blocks of T vectors in turn
+// -- and their states meet by pushes.
 template <bool kStats>
 __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, int cols) {
     __shared__ RowState red[32];
@@ -226,7 +233,17 @@ __global__ void __launch_bounds__(kStreamMaxThreads, 6) k_rows_stream(Args a, in
             if (lab_ok && rp) xl = rp[label];
         }
         RowState st = empty_state();
-        if (n > 0 && rp) st = scan_global<kStats, kStats ? kUnroll : kArgmaxUnroll>(rp + c0, c0, n);
+        if constexpr (kStats) {
+            if (n > 0 && rp) st = scan_global<true>(rp + c0, c0, n);
+        } else if (rp) {
+            // the cluster's CTAs take the row's 4 KB blocks of vectors in turn
+            // (256 x 151936, L2 flushed: 30.3-30.6 -> 29.2 us against one
+            // contiguous third each; the loss scan, one more register short,
+            // spills with it and stays contiguous)
+            const int T = static_cast<int>(blockDim.x);
+            st = scan_argmax<kArgmaxUnroll>(rp, 0, a.vocab, static_cast<int>(rank) * T + tid, static_cast<int>(C) * T,
+                                            rank == 0 ? tid : -1);
+        }
         st = block_reduce_w0<kStats>(st, red);
         if (k == 0) cluster_wait();
         if (tid == 0) push_xchg_publish(xg, k, rank, C, st, 0.0f);

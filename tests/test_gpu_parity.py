@@ -250,6 +250,43 @@ def test_ties_at_slice_and_lane_boundaries(orc, cluster):
         check_all(res, orc, x.numpy(), V, y.numpy(), 1.0, f"ties {plan}")
 
 
+@pytest.mark.parametrize("threads", [256, 128])
+@pytest.mark.parametrize("cluster", [2, 3, 4, 16])
+@pytest.mark.parametrize("offset", [0, 1, 3])
+def test_argmax_ties_across_interleaved_blocks(orc, cluster, threads, offset):
+    """The streaming argmax's cluster CTAs take a row's blocks of T vectors (4T
+    columns past the first 16-byte boundary) in turn: equal maxima on both
+    sides of a block boundary, in blocks of one CTA two turns apart, in the
+    unaligned head and the tail, and NaN runs beside them -- the lower column
+    wins, bit-exact against the oracle, on rows starting at every 16-byte
+    phase."""
+    V = 4 * threads * (3 * cluster + 1) + 3
+    B = 4 * threads
+    h = (4 - offset) % 4  # columns before the first 16-byte boundary
+    pairs = [(h + B - 1, h + B), (h + 2 * B - 1, h + 2 * B), (h + 5, h + cluster * B + 5),
+             (h + B + 7, h + (cluster + 1) * B + 7), (0, V - 1), (max(h - 1, 0), V - 2), (V - 3, V - 1)]
+    R = len(pairs) + 2
+    S = V + 5
+    buf = torch.full((R * S + offset + 8,), 1e30)
+    x = buf[offset: offset + R * S].view(R, S)
+    x[:, :V] = torch.randn((R, V), generator=torch.Generator().manual_seed(cluster * 7 + threads + offset))
+    for i, (a, b) in enumerate(pairs):
+        x[i, a] = x[i, b] = 40.0
+    x[len(pairs), : V // 2] = float("nan")                  # NaN blocks ahead of the max
+    x[len(pairs), V // 2 + 1] = x[len(pairs), V - 1] = 40.0
+    x[len(pairs) + 1, :V] = float("nan")                    # all NaN: token 0
+    want = orc.argmax(x.numpy(), V)
+    dbuf = buf.to(DEV)
+    dx = dbuf[offset: offset + R * S].view(R, S)
+    ce.debug_force(2, cluster, threads)
+    try:
+        got = ce.argmax_rows(dx, vocab=V)
+        torch.cuda.synchronize()
+    finally:
+        ce.debug_force(0, 0, 0)
+    assert_tokens(got, want, f"interleaved argmax, cluster {cluster}, {threads} threads, offset {offset}")
+
+
 def test_bad_labels_and_error_counter(orc):
     V, R = 3000, 6
     x, y = W.random_logits(R, V, seed=9)
