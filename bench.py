@@ -559,8 +559,8 @@ def run_ours(args):
                        "GB/s": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9, 1),
                        "frac": round(argmax_bytes(wd.rows, wd.vocab) / (arg_ms * 1e-3) / 1e9 / peak, 4),
                        "l2": "flushed before each launch",
-                       "plain_read": {"what": "ce_debug_read (16-byte loads, 8 in flight per thread, one "
-                                              "resident wave) of the same padded buffer, same flush",
+                       "plain_read": {"what": "ce_debug_read (one CTA per SM, 32 KB bulk copies through four "
+                                              "shared-memory stages) of the same padded buffer, same flush",
                                       "bytes": read_bytes, "ms": round(read_ms, 5),
                                       "ms_min": round(min(read_all), 5),
                                       "GB/s": round(read_bytes / (read_ms * 1e-3) / 1e9, 1),

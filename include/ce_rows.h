@@ -398,11 +398,12 @@ CE_API int ce_debug_grid_cap(int64_t clusters);
 
 /*
  * Read probe, for measurement: reads `bytes` bytes at device address p (16-byte
- * aligned, bytes a multiple of 16) once, sixteen bytes per load with eight
- * loads in flight per thread over one resident wave of CTAs, and XORs every
- * word read into *out (4 bytes on the device, not cleared first). No page
- * defines it: it gives the ceiling of a plain read of a buffer of that size
- * on this device, to time beside a row kernel that reads the same bytes.
+ * aligned, bytes a multiple of 16) once -- one CTA per SM, 32 KB chunks by
+ * bulk asynchronous copies through four shared-memory stages, the fastest
+ * plain read of a large buffer measured on this device -- and XORs every word
+ * read into *out (4 bytes on the device, not cleared first). No page defines
+ * it: it gives the ceiling of a plain read of a buffer of that size on this
+ * device, to time beside a row kernel that reads the same bytes.
  */
 CE_API int ce_debug_read(const void *p, int64_t bytes, uint32_t *out, ce_stream_t stream);
 

@@ -1334,31 +1334,70 @@ __global__ void __launch_bounds__(kMeanThreads) k_mean(const float *__restrict__
 }
 
 // ---------------------------------------------------------------------------
-// k_read_probe: a plain read of n16 16-byte vectors, eight loads in flight per
-// thread in a grid-stride loop, folded by XOR into one word -- the ceiling of a
-// read of that size on this device, for measurement beside the row kernels.
-constexpr int kProbeThreads = 512;
+// k_read_probe: a plain read of `bytes` bytes, the ceiling of a read of that
+// size on this device, for measurement beside the row kernels. One CTA per SM
+// streams chunks c = blockIdx.x, blockIdx.x + gridDim.x, ... of 32 KB through
+// four shared-memory stages by bulk copies (the TMA engine); every thread
+// folds its 16-byte vectors of each chunk by XOR into one word. Measured on
+// GB300, 155.7 MB with L2 flushed: 27.6 us against 28.7-28.9 us for 16-byte
+// loads, eight in flight per thread over one resident wave of 512-thread CTAs.
+constexpr int kProbeThreads = 256;
+constexpr int kProbeStages = 4;
+constexpr int kProbeChunk = 32768;
+constexpr int kProbeSmem = 128 + kProbeStages * kProbeChunk;
 
-__global__ void __launch_bounds__(kProbeThreads) k_read_probe(const float4 *__restrict__ p, int64_t n16,
-                                                              uint32_t *__restrict__ out) {
-    const int64_t T = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    uint32_t acc = 0;
-    for (; i + 7 * T < n16; i += 8 * T) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = ld_stream_f4(p + i + u * T);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            acc ^= __float_as_uint(v[u].x) ^ __float_as_uint(v[u].y) ^ __float_as_uint(v[u].z) ^
-                   __float_as_uint(v[u].w);
+__global__ void __launch_bounds__(kProbeThreads, 1) k_read_probe(const char *__restrict__ p, int64_t bytes,
+                                                                 uint32_t *__restrict__ out) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    const float4 *stage = reinterpret_cast<const float4 *>(smem + 128);
+    const int tid = threadIdx.x;
+    const int64_t nch = (bytes + kProbeChunk - 1) / kProbeChunk;
+    const int64_t K = blockIdx.x < nch ? (nch - 1 - blockIdx.x) / gridDim.x + 1 : 0;  // chunks of this CTA
+    const uint64_t policy = l2_policy_evict_first();
+    auto chunk_bytes = [&](int64_t k) {
+        const int64_t rest = bytes - (blockIdx.x + k * gridDim.x) * static_cast<int64_t>(kProbeChunk);
+        return static_cast<uint32_t>(rest < kProbeChunk ? rest : kProbeChunk);
+    };
+    auto issue = [&](int64_t k) {
+        const int s = static_cast<int>(k % kProbeStages);
+        const uint32_t nb = chunk_bytes(k);
+        mbar_arrive_expect_tx(&bar[s], nb);
+        bulk_copy_g2s(smem + 128 + s * kProbeChunk, p + (blockIdx.x + k * gridDim.x) * static_cast<int64_t>(kProbeChunk),
+                      nb, &bar[s], policy);
+    };
+    if (tid == 0) {
+        for (int s = 0; s < kProbeStages; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        for (int64_t k = 0; k < K && k < kProbeStages; ++k) issue(k);
     }
-    for (; i < n16; i += T) {
-        const float4 v = ld_stream_f4(p + i);
-        acc ^= __float_as_uint(v.x) ^ __float_as_uint(v.y) ^ __float_as_uint(v.z) ^ __float_as_uint(v.w);
+    __syncthreads();
+    uint32_t acc = 0;
+    bool failed = false;
+    for (int64_t k = 0; k < K; ++k) {
+        const int s = static_cast<int>(k % kProbeStages);
+        if (!failed && !mbar_wait_bounded(&bar[s], static_cast<uint32_t>(k / kProbeStages) & 1u)) failed = true;
+        const int nv = static_cast<int>(chunk_bytes(k) / 16);
+        const float4 *sv = stage + s * (kProbeChunk / 16);
+#pragma unroll 4
+        for (int q = tid; q < nv; q += kProbeThreads) {
+            const float4 v = sv[q];
+            acc ^= __float_as_uint(v.x) ^ __float_as_uint(v.y) ^ __float_as_uint(v.z) ^ __float_as_uint(v.w);
+        }
+        __syncthreads();  // stage s is free
+        if (tid == 0 && k + kProbeStages < K) {
+            fence_proxy_async_smem();
+            issue(k + kProbeStages);
+        }
     }
     acc = __reduce_xor_sync(kFullMask, acc);
-    if ((threadIdx.x & 31) == 0) atomicXor(out, acc);
+    if ((tid & 31) == 0) atomicXor(out, acc);
+    if (__syncthreads_or(failed) && tid == 0) {
+        atomicAdd(&g_status[1], 1ull);
+        // a last bounded wait for the copies still in flight
+        for (int64_t k = K > kProbeStages ? K - kProbeStages : 0; k < K; ++k)
+            (void)mbar_wait_bounded(&bar[k % kProbeStages], static_cast<uint32_t>(k / kProbeStages) & 1u, 10000000ull);
+    }
 }
 
 cudaError_t launch_clustered(const void *fn, const Plan &p, void **args, cudaStream_t s) {
@@ -1437,7 +1476,8 @@ cudaError_t set_kernel_attributes(const DeviceInfo &dev) {
         cudaError_t e = cudaFuncSetAttribute(r.first, cudaFuncAttributeMaxDynamicSharedMemorySize, r.second);
         if (e != cudaSuccess) return e;
     }
-    return cudaSuccess;
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(&k_read_probe), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kProbeSmem);
 }
 
 cudaError_t max_active_clusters(const Plan &p, Op op, int *n) {
@@ -1554,13 +1594,9 @@ cudaError_t launch_mean(const float *loss, int64_t rows, double *out, cudaStream
 }
 
 cudaError_t launch_read_probe(const void *p, int64_t bytes, uint32_t *out, int sms, cudaStream_t s) {
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_read_probe, kProbeThreads, 0);
-    if (e != cudaSuccess) return e;
-    const int64_t n16 = bytes / 16;
-    const int64_t need = (n16 + kProbeThreads - 1) / kProbeThreads;
-    const int ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, int64_t(per_sm) * sms)));
-    k_read_probe<<<ctas, kProbeThreads, 0, s>>>(static_cast<const float4 *>(p), n16, out);
+    const int64_t nch = (bytes + kProbeChunk - 1) / kProbeChunk;
+    const int ctas = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(nch, sms)));
+    k_read_probe<<<ctas, kProbeThreads, kProbeSmem, s>>>(static_cast<const char *>(p), bytes, out);
     return cudaGetLastError();
 }
 
