@@ -474,6 +474,51 @@ def test_grad_step_replayed_from_a_cuda_graph(orc, shape):
         assert_mean(m2.item(), m_ref, "graph ce_loss mean")
 
 
+@pytest.mark.parametrize("rows", [256, 1024], ids=["decode-256", "decode-1024"])
+def test_decode_step_replayed_from_a_cuda_graph(orc, rows):
+    """A decode step's row calls -- argmax_rows, candidates_rows, softmax_rows
+    and log_softmax_rows on the logits of a 151936 vocabulary with a 152064
+    stride -- captured once in a CUDA graph and replayed on new logits: every
+    replay gives the oracle's tokens, candidates and rows (the kernels keep no
+    state between launches that a replay could see)."""
+    V, S = 151936, 152064
+    sx = torch.zeros((rows, S), device=DEV)
+    top = torch.empty((rows,), device=DEV)
+    cand = torch.empty((rows, ce.CANDIDATE_ROW), device=DEV)
+    soft = torch.empty((rows, V), device=DEV)
+    logp = torch.empty((rows, V), device=DEV)
+
+    def step():
+        ce.argmax_rows(sx, vocab=V, out=top)
+        ce.candidates_rows(sx, vocab=V, out=cand)
+        ce.softmax_rows(sx, vocab=V, out=soft)
+        ce.log_softmax_rows(sx, vocab=V, out=logp)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for i, sigma in enumerate((1.0, 5.0)):
+        x, _ = W.random_logits(rows, V, stride=S, sigma=sigma, seed=300 + rows + i, pad_value=-1e30)
+        x[5, 17] = x[5, 90001] = 50.0              # a tie: the lower column
+        x[6, :V] = float("nan")
+        sx.copy_(x.to(DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        xn = x.numpy()
+        what = f"graph replay {i}, {rows} rows"
+        assert_tokens(top, orc.argmax(xn, V, threads=THREADS), f"{what}: tokens")
+        assert_candidates(cand, orc.candidates(xn, V, threads=THREADS), f"{what}: candidates")
+        sample = list(range(0, rows, max(1, rows // 16))) + [5, 6]
+        assert_softmax(soft[sample], orc.softmax(xn[sample], V, threads=THREADS), f"{what}: softmax")
+        assert_log_softmax(logp[sample], orc.log_softmax(xn[sample], V, threads=THREADS), f"{what}: log-softmax")
+
+
 def test_every_row_family_gives_the_same_bits_every_run():
     """Fixed-shape reductions and merges: five runs, identical bits (a race in a
     split-row combine or an exchange would show as a difference)."""
