@@ -616,6 +616,7 @@ __device__ __forceinline__ int64_t flat_split(int64_t E, int64_t P, int64_t j) {
 
 __global__ void __launch_bounds__(kFlatThreads, 2) k_argmax_flat(Args a, uint64_t *__restrict__ ws) {
     __shared__ RowState red[32];
+    launch_dependents();  // the combine may be scheduled now; it waits for this grid's end
     const int64_t E = a.rows * static_cast<int64_t>(a.vocab), P = gridDim.x, j = blockIdx.x;
     const int64_t e0 = flat_split(E, P, j), e1 = flat_split(E, P, j + 1);
     for (int64_t r = e0 / a.vocab; r < a.rows && r * a.vocab < e1; ++r) {
@@ -629,6 +630,7 @@ __global__ void __launch_bounds__(kFlatThreads, 2) k_argmax_flat(Args a, uint64_
 }
 
 __global__ void k_argmax_combine(Args a, const uint64_t *__restrict__ ws, int P) {
+    wait_prerequisites();  // every segment's key is written and visible
     const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if (r >= a.rows) return;
     const int64_t E = a.rows * static_cast<int64_t>(a.vocab);
@@ -1555,8 +1557,18 @@ cudaError_t launch_argmax_flat(const Args &a, int ctas, void *ws, cudaStream_t s
     if (e != cudaSuccess) return e;
     const int threads = 256;
     const unsigned blocks = static_cast<unsigned>((a.rows + threads - 1) / threads);
-    k_argmax_combine<<<blocks, threads, 0, s>>>(a, static_cast<const uint64_t *>(ws), ctas);
-    return cudaGetLastError();
+    // a programmatic dependent of the scan: no launch gap between the two
+    // (64 x 151936, L2 flushed: 23.6 -> 21.0 us; 1024 rows 104 -> 101 us)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_argmax_combine, a, static_cast<const uint64_t *>(ws), ctas);
 }
 
 cudaError_t launch_stats_combine(const float *stats, int64_t shards, int64_t rows, int64_t vocab_total,
