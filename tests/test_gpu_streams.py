@@ -98,3 +98,55 @@ def test_entry_points_concurrent_on_four_streams(orc):
         for name in first:
             for a, b in zip(flat(first[name]), flat(later[name])):
                 assert np.array_equal(a, b), f"{name}: pass {k} differs from pass 0"
+
+
+def test_entry_points_from_four_host_threads(orc):
+    """The C ABI called from four host threads at once (ctypes releases the
+    interpreter lock during each call), each on its own stream and its own
+    batch: the library's host state -- device table, forced-plan settings,
+    the host pipe -- is shared under a lock, and every thread gets the
+    oracle's results."""
+    import threading
+    shapes = [(300, 50257), (64, 151936), (1024, 32000), (37, 100003)]
+    batches = [W.random_logits(R, V, sigma=3.0, seed=40 + i) for i, (R, V) in enumerate(shapes)]
+    results = [None] * len(shapes)
+    errors = []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(0)
+            x, y = batches[i]
+            dx, dy = x.to(DEV), y.to(DEV)
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                outs = []
+                for _ in range(3):
+                    grad, lr, top, mean = ce.ce_grad_step(dx, dy, 0.5)
+                    outs.append((grad, lr, top, mean, ce.argmax_rows(dx), ce.candidates_rows(dx)))
+            st.synchronize()
+            results[i] = [tuple(t.cpu() for t in o) for o in outs]
+        except Exception as e:  # reported by the main thread
+            errors.append((i, repr(e)))
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(shapes))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not errors, errors
+    for i, ((x, y), (R, V)) in enumerate(zip(batches, shapes)):
+        xn, yn = x.numpy(), y.numpy()
+        g_ref, l_ref = orc.ce_grad(xn, V, yn, 0.5, threads=THREADS)
+        a_ref = orc.argmax(xn, V, threads=THREADS)
+        c_ref = orc.candidates(xn, V, threads=THREADS)
+        first = results[i][0]
+        assert_grad(first[0], g_ref, f"thread {i}: gradient")
+        assert_loss(first[1], l_ref, f"thread {i}: loss rows")
+        assert_tokens(first[2], a_ref, f"thread {i}: step tokens")
+        assert_mean(first[3].item(), orc.ce_mean(l_ref), f"thread {i}: mean")
+        assert_tokens(first[4], a_ref, f"thread {i}: argmax_rows")
+        assert_candidates(first[5], c_ref, f"thread {i}: candidates")
+        for k, later in enumerate(results[i][1:], 1):
+            for a, b in zip(first, later):
+                assert torch.equal(a.reshape(-1).view(torch.uint8), b.reshape(-1).view(torch.uint8)), \
+                    f"thread {i}: call {k} differs from call 0"
